@@ -1,0 +1,424 @@
+#!/usr/bin/env python3
+"""Benchmark of exact sink-aware attention, forward + backward, on GB300.
+
+One step = one forward and one backward pass (every kernel of the path) over
+one batch of the workload.  Default workload: 2 sequences x 8192 tokens,
+64 query / 8 key-value heads, head_dim 64, full causal mask, bf16 inputs.
+
+The line's value is TFLOP/s counting only unmasked (query, key, head) pairs
+at 14 * 64 FLOP per pair (forward 4 * 64, backward 10 * 64).  Inputs are
+resident in HBM; L2 is flushed (256 MiB write) before every timed step, and
+each step is timed alone with CUDA events on the stream the kernels run on.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+       python bench.py --impl reference ...   (times the CPU float64 oracle)
+Under torchrun each rank runs its own batch (weak scaling, no collective on
+the data path; the process group only carries the barrier and the max-time
+reduction).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "sink-attn fwd+bwd TFLOP/s (bf16, S=4k/8k) and % of GB300 dense bf16 peak"
+DEFAULT_WORKLOAD = "causal_gqa_b2_s8192"
+FLOP_FWD_PER_PAIR = 4 * 64
+FLOP_BWD_PER_PAIR = 10 * 64
+L2_FLUSH_BYTES = 256 << 20
+LAUNCHES_PER_STEP = 4  # forward, backward preprocess, backward main, dQ convert
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------- accounting
+def visible_pairs(wl) -> int:
+    """Unmasked (query, key) pairs summed over sequences and query heads."""
+    total = 0
+    for n in wl.seqlens:
+        q = np.arange(int(n), dtype=np.int64)
+        lo = np.zeros_like(q) if wl.window < 0 else np.maximum(0, q - wl.window)
+        hi = q if wl.causal else np.full_like(q, int(n) - 1)
+        band = np.maximum(0, hi - lo + 1)
+        extra = np.minimum(wl.prefix, lo)  # prefix keys below the band
+        total += int(np.sum(band + extra))
+    return total * wl.num_heads_q
+
+
+def algorithmic_bytes(wl):
+    """Minimum HBM bytes: fwd reads Q,K,V and writes O,lse; bwd reads
+    Q,K,V,O,dO,lse and writes dQ,dK,dV."""
+    T, hq, hkv, d = wl.total_tokens, wl.num_heads_q, wl.num_heads_kv, wl.head_dim
+    q = T * hq * d * 2
+    kv = T * hkv * d * 2
+    lse = T * hq * 4
+    fwd = q + 2 * kv + q + lse
+    bwd = q + 2 * kv + q + q + lse + q + 2 * kv
+    return fwd, bwd
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling (200 ms) while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+# ----------------------------------------------------------------- oracle (CPU)
+def _oracle_head_job(args):
+    import oracle
+
+    q, k, v, do, sink, cu, window, prefix, causal, scale = args
+    t = time.perf_counter()
+    oracle.forward_backward(q, k, v, sink, do, cu, window, prefix, causal, scale)
+    return time.perf_counter() - t
+
+
+def _init_worker():
+    import oracle  # noqa: F401  (import cost outside the timed region)
+
+
+def oracle_sample_jobs(wl, n_heads):
+    """One sequence (the first), ``n_heads`` query heads: float64 slices."""
+    inp = W.make_inputs(wl.with_(seqlens=(wl.seqlens[0],), uniform=True))
+    group = wl.num_heads_q // wl.num_heads_kv
+    cu = np.array([0, wl.seqlens[0]], dtype=np.int64)
+    q, k, v, do, sink = (inp.f64(n) for n in ("q", "k", "v", "do", "sink"))
+    jobs = []
+    for i in range(n_heads):
+        h = i % wl.num_heads_q
+        g = h // group
+        jobs.append((np.ascontiguousarray(q[:, h:h + 1]), np.ascontiguousarray(k[:, g:g + 1]),
+                     np.ascontiguousarray(v[:, g:g + 1]), np.ascontiguousarray(do[:, h:h + 1]),
+                     sink[h:h + 1].copy(), cu, wl.window, wl.prefix, wl.causal, wl.scale))
+    one = wl.with_(seqlens=(wl.seqlens[0],), num_heads_q=1, num_heads_kv=1)
+    flops = visible_pairs(one) * (FLOP_FWD_PER_PAIR + FLOP_BWD_PER_PAIR) * n_heads
+    return jobs, flops
+
+
+class OraclePool:
+    """A spawn pool of single-threaded oracle workers (one per host core, up to 16)."""
+
+    def __init__(self):
+        import multiprocessing as mp
+
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[var] = "1"
+        self.cores = max(1, min(16, os.cpu_count() or 1))
+        self.pool = mp.get_context("spawn").Pool(self.cores, initializer=_init_worker)
+
+    def run(self, jobs):
+        t = time.perf_counter()
+        self.pool.map(_oracle_head_job, jobs, chunksize=1)
+        return time.perf_counter() - t
+
+    def close(self):
+        self.pool.terminate()
+
+
+def cpu_baseline(wl, pool=None):
+    own = pool is None
+    pool = pool or OraclePool()
+    try:
+        jobs, flops = oracle_sample_jobs(wl, pool.cores)
+        sec = pool.run(jobs)
+    finally:
+        if own:
+            pool.close()
+    return {"value": flops / sec / 1e12, "unit": "TFLOP/s", "cores": pool.cores, "kind": "oracle",
+            "sample": f"{len(jobs)} query heads x 1 sequence of {wl.seqlens[0]} tokens of {wl.name}, fwd+bwd, "
+                      f"one single-threaded worker per head, {sec:.2f} s wall"}
+
+
+def run_reference(args, rank):
+    """The oracle as the reference arm, on the host cores of rank 0."""
+    if rank != 0:
+        return 0
+    wl = W.WORKLOADS[args.workload]
+    pool = OraclePool()
+    try:
+        jobs, flops = oracle_sample_jobs(wl, pool.cores)
+        for _ in range(args.warmup):
+            pool.run(jobs[:1])
+        secs = [pool.run(jobs) for _ in range(args.steps)]
+    finally:
+        pool.close()
+    total = sum(secs)
+    value = flops * len(secs) / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(secs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "sample_per_step": f"{pool.cores} query heads x 1 sequence"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": pool.cores, "kind": "oracle",
+                         "sample": f"each step: {pool.cores} query heads x 1 sequence of {wl.seqlens[0]} tokens "
+                                   f"of {wl.name}, fwd+bwd"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- GPU arm
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(values, world, device):
+    """Max over ranks of a list of floats (identity for one rank)."""
+    if world == 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def run_gpu(args, world, rank, local):
+    import torch
+
+    import sink_aware_masked_gb300 as sa
+    from sink_aware_masked_gb300 import build as sa_build
+
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    sa_build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    base = W.WORKLOADS[args.workload]
+    wl = base.with_(seed=base.seed + 1000 * rank)  # each rank: its own batch
+    inp = W.make_inputs(wl)
+    q, k, v, do = (t.to(dev) for t in (inp.q_bf16, inp.k_bf16, inp.v_bf16, inp.do_bf16))
+    sink = inp.sink.to(dev)
+    if wl.uniform:
+        prob = dict(num_seqs=wl.num_seqs)
+    else:
+        cu = wl.cu_seqlens()
+        prob = dict(cu_seqlens=torch.tensor(cu, dtype=torch.int32, device=dev),
+                    cu_seqlens_host=[int(x) for x in cu], max_seqlen=wl.max_seqlen)
+    prob.update(window=wl.window, prefix=wl.prefix, causal=wl.causal, scale=wl.scale)
+    o = torch.empty_like(q)
+    lse = torch.empty((wl.num_heads_q, wl.total_tokens), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dsink = torch.empty_like(sink)
+    ws = torch.empty(max(16, sa.bwd_workspace_bytes(q, k, **prob)), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        sa.sinkattn_fwd(q, k, v, sink, o=o, lse=lse, **prob)
+        sa.sinkattn_bwd(q, k, v, o, lse, do, sink, dq=dq, dk=dk, dv=dv, dsink=dsink, workspace=ws, **prob)
+
+    for _ in range(max(args.warmup, 0)):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    if sa.sinkattn_get_device_status() != 0:
+        raise RuntimeError("device status reported a timed-out wait during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    for i in range(K):
+        flush.fill_(float(i))
+        e = ev[i]
+        sa.sinkattn_set_profile_events(sa.PROFILE_FWD, e[2], e[3])
+        sa.sinkattn_set_profile_events(sa.PROFILE_BWD_MAIN, e[4], e[5])
+        e[0].record()
+        step()
+        e[1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clock_info = clocks.stop()
+    sa.sinkattn_set_profile_events(sa.PROFILE_FWD)
+    sa.sinkattn_set_profile_events(sa.PROFILE_BWD_MAIN)
+    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    fwd_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    bwd_main_ms = [e[4].elapsed_time(e[5]) for e in ev]
+    if sa.sinkattn_get_device_status() != 0:
+        raise RuntimeError("device status reported a timed-out wait")
+
+    # ---- end to end through host buffers (pinned), copies inside the timed region
+    host_in = [t.cpu().pin_memory() for t in (q, k, v, do, sink)]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse, dq, dk, dv, dsink)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    dev_in = (q, k, v, do, sink)
+    dev_out = (o, lse, dq, dk, dv, dsink)
+    Ke = max(1, min(K, 5))
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ke)]
+    barrier(world)
+    for i in range(Ke):
+        flush.fill_(float(i))
+        e2e_ev[i][0].record()
+        for d_, h_ in zip(dev_in, host_in):
+            d_.copy_(h_, non_blocking=True)
+        step()
+        for h_, d_ in zip(host_out, dev_out):
+            h_.copy_(d_, non_blocking=True)
+        e2e_ev[i][1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = [a.elapsed_time(b) for a, b in e2e_ev]
+
+    # ---- reduce over ranks (max) and report
+    tot, e2e_tot = reduce_max([sum(step_ms), sum(e2e_ms)], world, dev)
+    pairs = visible_pairs(wl)
+    flop_step = pairs * (FLOP_FWD_PER_PAIR + FLOP_BWD_PER_PAIR)
+    value = world * flop_step * K / (tot / 1e3) / 1e12
+    e2e_value = world * flop_step * Ke / (e2e_tot / 1e3) / 1e12
+    peaks, peak_src = load_peaks()
+    fwd_b, bwd_b = algorithmic_bytes(wl)
+    avg_bwd = statistics.mean(bwd_main_ms)
+    avg_fwd = statistics.mean(fwd_ms)
+    dom = "bwd_main" if avg_bwd >= avg_fwd else "fwd"
+    dom_ms = avg_bwd if dom == "bwd_main" else avg_fwd
+    dom_flop = pairs * (FLOP_BWD_PER_PAIR if dom == "bwd_main" else FLOP_FWD_PER_PAIR)
+    achieved = dom_flop / (dom_ms / 1e3) / 1e12
+    traffic = _committed_traffic(args.workload, dom)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": tot / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "global_batch": wl.num_seqs * world, "seq_len": wl.max_seqlen,
+                   "heads_q": wl.num_heads_q, "heads_kv": wl.num_heads_kv, "head_dim": wl.head_dim,
+                   "window": wl.window, "prefix": wl.prefix, "causal": wl.causal,
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "flushed before every step (256 MiB write, outside the step events)",
+                   "flop_per_step": flop_step, "unmasked_pairs": pairs},
+        "pct_of_peak": 100.0 * value / world / peaks["bf16_tflops"],
+        "breakdown_ms": {"fwd_kernel": avg_fwd, "bwd_main_kernel": avg_bwd,
+                         "rest": statistics.mean(step_ms) - avg_fwd - avg_bwd},
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peaks["bf16_tflops"],
+                     "peak_source": f"{peak_src} bf16 burst", "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
+                     "hbm_gbs_equiv": (bwd_b if dom == "bwd_main" else fwd_b) / (dom_ms / 1e3) / 1e9},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": K * LAUNCHES_PER_STEP,
+        "clocks": clock_info,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def _committed_traffic(workload, kernel):
+    """DRAM bytes per launch from the committed ncu summary, if one matches."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    return d.get(workload, {}).get(kernel)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU baseline leg")
+    args = ap.parse_args(argv)
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, rank)
+    return run_gpu(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

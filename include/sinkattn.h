@@ -1,0 +1,150 @@
+/*
+ * sinkattn.h — C ABI of the GB300 (sm_103a) sink-aware attention library.
+ *
+ * The operation is exact softmax attention under the mask of the SinkFlex-RL
+ * paper ("Efficient Reinforcement Learning for Long-Horizon Tool-Use Agentic
+ * Tasks", summary page, paragraph on the sink-aware FlexAttention path):
+ *
+ *     M[q, k] = [k <= q]  and  ( [q - k <= w]  or  [k < p] )
+ *
+ * with w the local window (inclusive; w + 1 keys including the query) and p
+ * the number of always-visible prefix positions, the same mask for every
+ * sequence and head.  Scores are s_qk = scale * <Q_q, K_k>.  The attention
+ * call returns the output together with the natural-log log-sum-exp
+ * l_q = log sum_{k visible} exp(s_qk) (sink excluded), and the output is
+ * scaled by alpha_q = sigmoid(l_q - sink[h]), which is the same as appending
+ * one more softmax column with logit sink[h] and a zero value vector
+ * (section 5, "zero-value sink equivalence").  The backward returns dQ, dK,
+ * dV and the per-head sink gradient dL/dS_h ("GPT-OSS agentic RL training"
+ * page, FlashAttention v3 implementation), recomputing probabilities from l
+ * so that no S x S matrix is ever stored.
+ *
+ * Layouts (all contiguous, row-major, head_dim innermost):
+ *   q, o, dout, dq : bf16 [T, Hq, D]
+ *   k, v, dk, dv   : bf16 [T, Hkv, D]
+ *   lse            : fp32 [Hq, T]
+ *   sink, dsink    : fp32 [Hq]
+ * T is the number of tokens of all packed sequences.  Query head h reads
+ * key/value head h / (Hq / Hkv) (contiguous GQA groups).  Positions inside
+ * the mask are positions inside each packed sequence.
+ *
+ * Ownership: the caller allocates every buffer, including the workspace,
+ * and keeps it alive until the stream has run the work.  The library
+ * allocates no device memory and keeps no per-call state.  All device
+ * pointers must be 16-byte aligned.  Every call is asynchronous on `stream`
+ * (a cudaStream_t passed as void*; NULL = legacy default stream).
+ * Outputs are overwritten, never accumulated (dsink included).  No output
+ * may alias an input or another output.
+ *
+ * Errors: argument checks run on the host before anything is launched; a
+ * failing check returns its status and launches nothing.  A failed launch
+ * returns SINKATTN_ERR_CUDA.  Nothing aborts, exits or traps on the device.
+ */
+#ifndef SINKATTN_H
+#define SINKATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SINKATTN_OK = 0,
+  SINKATTN_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad mask parameter, bad cu_seqlens */
+  SINKATTN_ERR_UNSUPPORTED = 2,  /* head_dim other than 64, or sizes beyond the int32 index range */
+  SINKATTN_ERR_ALIGNMENT = 3,    /* a device pointer that is not 16-byte aligned */
+  SINKATTN_ERR_WORKSPACE = 4,    /* workspace smaller than the matching *_workspace_size() */
+  SINKATTN_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed */
+  SINKATTN_ERR_TIMEOUT = 6       /* a kernel gave up a bounded wait (see sinkattn_get_device_status) */
+} sinkattn_status;
+
+/* One attention problem.  Uniform batch: cu_seqlens == NULL, num_seqs = B,
+ * seqlen = S, total_tokens = B * S.  Packed variable-length sequences:
+ * cu_seqlens (device) and cu_seqlens_host (host) hold the same num_seqs + 1
+ * offsets, cu[0] = 0, nondecreasing, cu[num_seqs] = total_tokens, and
+ * seqlen is the largest cu[i+1] - cu[i]. */
+typedef struct {
+  int32_t num_seqs;
+  int32_t seqlen;
+  const int32_t* cu_seqlens;       /* device, [num_seqs + 1], or NULL */
+  const int32_t* cu_seqlens_host;  /* host copy of cu_seqlens (NULL iff cu_seqlens is NULL) */
+  int32_t total_tokens;
+  int32_t num_heads_q;             /* Hq, a multiple of num_heads_kv */
+  int32_t num_heads_kv;            /* Hkv >= 1 */
+  int32_t head_dim;                /* must be 64 */
+  int64_t window;                  /* w >= 0 (inclusive), or -1 for unbounded */
+  int64_t prefix;                  /* p >= 0 */
+  int32_t causal;                  /* 1: keep [k <= q]; 0: drop that term */
+  float scale;                     /* softmax scale, finite and > 0 (1/sqrt(64) usually) */
+} sinkattn_problem;
+
+/* Bytes of device workspace that sinkattn_fwd / sinkattn_bwd need for
+ * `prob` (0 when the problem is invalid). */
+size_t sinkattn_fwd_workspace_size(const sinkattn_problem* prob);
+size_t sinkattn_bwd_workspace_size(const sinkattn_problem* prob);
+
+/* Forward.  Reads q, k, v (bf16) and sink (fp32 [Hq]); writes
+ * o = alpha * softmax_M(s) V (bf16 [T, Hq, 64]) and lse = l (fp32 [Hq, T]).
+ * Rows of a sequence are never mixed with rows of another sequence. */
+sinkattn_status sinkattn_fwd(const sinkattn_problem* prob,
+                             const void* q, const void* k, const void* v, const float* sink,
+                             void* o, float* lse,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward.  Reads the forward's inputs, its outputs o and lse, and dout;
+ * writes dq, dk, dv (bf16) and dsink (fp32 [Hq]), where
+ * dsink[h] = -sum over all rows of (1 - alpha_q) * <dout_q, o_q>.
+ * The workspace holds an fp32 dQ accumulator [T, Hq, 64], the per-row
+ * terms D and l' = l + softplus(sink - l) ([Hq, T] each) and per-block
+ * partial sums of dsink. */
+sinkattn_status sinkattn_bwd(const sinkattn_problem* prob,
+                             const void* q, const void* k, const void* v, const void* o,
+                             const float* lse, const void* dout, const float* sink,
+                             void* dq, void* dk, void* dv, float* dsink,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* Packed-sequence front end (multi-turn trajectories of different lengths,
+ * SinkFlex-RL section 3).  seqlens: device int32 [num_seqs];
+ * cu_seqlens_out: device int32 [num_seqs + 1] receives the exclusive prefix
+ * sum (cu[0] = 0).  Fails with INVALID_ARG for num_seqs < 0 or null pointers.
+ * A negative length is clamped to 0 on the device. */
+sinkattn_status sinkattn_varlen_plan(const int32_t* seqlens, int32_t num_seqs, int32_t* cu_seqlens_out,
+                                     void* stream);
+
+/* Padded <-> packed copies of a bf16 [*, H, D] tensor.
+ * pack:   padded [B, Smax, H, D] -> packed [cu[B], H, D] (rows past each length are skipped).
+ * unpack: packed -> padded; padding rows of `padded` are written with zeros.
+ * cu_seqlens is the device copy of the offsets; each length must be <= Smax
+ * (rows beyond Smax are not copied).  H * D * 2 bytes must be a multiple of 16. */
+sinkattn_status sinkattn_pack(const void* padded, const int32_t* cu_seqlens, int32_t B, int32_t Smax,
+                              int32_t H, int32_t D, void* packed, void* stream);
+sinkattn_status sinkattn_unpack(const void* packed, const int32_t* cu_seqlens, int32_t B, int32_t Smax,
+                                int32_t H, int32_t D, void* padded, void* stream);
+
+/* Synchronises `stream`, then reads and clears the library's device status
+ * word: SINKATTN_OK, or SINKATTN_ERR_TIMEOUT when a kernel gave up a bounded
+ * wait since the last call (its outputs are then undefined). */
+sinkattn_status sinkattn_get_device_status(void* stream);
+
+/* Measurement hook.  kind 1 selects the forward attention kernel, kind 2
+ * the backward main kernel.  With non-NULL `start` and `stop` (cudaEvent_t
+ * handles passed as void*), every later sinkattn_fwd / sinkattn_bwd call
+ * records `start` on its stream immediately before that kernel's launch and
+ * `stop` immediately after it, so the caller can time the kernel alone with
+ * cudaEventElapsedTime.  NULL for both clears the hook.  The setting is
+ * process-wide and not thread-safe; the events must outlive the calls.
+ * Returns INVALID_ARG for an unknown kind or a half-NULL pair. */
+sinkattn_status sinkattn_set_profile_events(int32_t kind, void* start, void* stop);
+
+/* Static, human-readable name of a status. */
+const char* sinkattn_status_string(sinkattn_status s);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t sinkattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SINKATTN_H */

@@ -1,0 +1,174 @@
+"""Thin PyTorch binding of the C ABI: argument marshalling only.
+
+Every step of the computation runs in the CUDA kernels of libsinkattn.so.
+PyTorch supplies device memory (outputs and workspace are allocated with
+torch) and the current CUDA stream.  There is no CPU path: on a machine
+without the built library or without a GPU these functions raise.
+
+Tensors: q, o, dout, dq [T, Hq, 64] bf16; k, v, dk, dv [T, Hkv, 64] bf16;
+lse [Hq, T] fp32; sink, dsink [Hq] fp32.  A uniform batch is given with
+``num_seqs`` (T = num_seqs * seqlen); packed sequences with ``cu_seqlens``
+(device int32 [B + 1]) and its host copy ``cu_seqlens_host``.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import Optional, Sequence
+
+import torch
+
+from . import _lib
+
+WINDOW_INF = -1
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def make_problem(q: torch.Tensor, k: torch.Tensor, *, num_seqs: Optional[int] = None,
+                 cu_seqlens: Optional[torch.Tensor] = None,
+                 cu_seqlens_host: Optional[Sequence[int]] = None, max_seqlen: Optional[int] = None,
+                 window: int = WINDOW_INF, prefix: int = 0, causal: bool = True,
+                 scale: Optional[float] = None):
+    """Build the C problem struct; returns (struct, keep-alive objects)."""
+    T, hq, d = q.shape
+    hkv = k.shape[1]
+    keep = []
+    if cu_seqlens is None:
+        B = 1 if num_seqs is None else int(num_seqs)
+        S = T // B if B > 0 else 0
+        cu_dev = cu_host_ptr = None
+    else:
+        if cu_seqlens_host is None:
+            raise ValueError("cu_seqlens_host (a host copy of cu_seqlens) is required with cu_seqlens")
+        host = (ctypes.c_int32 * len(cu_seqlens_host))(*[int(x) for x in cu_seqlens_host])
+        keep.append(host)
+        B = len(cu_seqlens_host) - 1
+        lens = [int(cu_seqlens_host[i + 1]) - int(cu_seqlens_host[i]) for i in range(B)]
+        S = int(max_seqlen) if max_seqlen is not None else (max(lens) if lens else 0)
+        cu_dev = cu_seqlens.data_ptr()
+        cu_host_ptr = ctypes.cast(host, ctypes.c_void_p).value
+    pr = _lib.Problem(
+        num_seqs=B, seqlen=S, cu_seqlens=cu_dev, cu_seqlens_host=cu_host_ptr, total_tokens=T,
+        num_heads_q=hq, num_heads_kv=hkv, head_dim=d, window=int(window), prefix=int(prefix),
+        causal=1 if causal else 0, scale=float(scale if scale is not None else 1.0 / math.sqrt(d)))
+    return pr, keep
+
+
+def sinkattn_fwd(q, k, v, sink, *, o=None, lse=None, workspace=None, **problem):
+    """Forward: returns (o, lse).  ``problem`` keys as in make_problem."""
+    lib = _lib.load()
+    pr, keep = make_problem(q, k, **problem)
+    T, hq, d = q.shape
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((hq, T), dtype=torch.float32, device=q.device)
+    ws_bytes = lib.sinkattn_fwd_workspace_size(ctypes.byref(pr))
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    st = lib.sinkattn_fwd(ctypes.byref(pr), _ptr(q), _ptr(k), _ptr(v), _ptr(sink), _ptr(o), _ptr(lse),
+                          _ptr(workspace), ws_bytes if workspace is not None else 0, _stream())
+    _lib.check("sinkattn_fwd", st)
+    return o, lse
+
+
+def bwd_workspace_bytes(q, k, **problem) -> int:
+    lib = _lib.load()
+    pr, keep = make_problem(q, k, **problem)
+    return int(lib.sinkattn_bwd_workspace_size(ctypes.byref(pr)))
+
+
+def sinkattn_bwd(q, k, v, o, lse, dout, sink, *, dq=None, dk=None, dv=None, dsink=None, workspace=None,
+                 **problem):
+    """Backward: returns (dq, dk, dv, dsink)."""
+    lib = _lib.load()
+    pr, keep = make_problem(q, k, **problem)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    dsink = torch.empty_like(sink) if dsink is None else dsink
+    ws_bytes = int(lib.sinkattn_bwd_workspace_size(ctypes.byref(pr)))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    st = lib.sinkattn_bwd(ctypes.byref(pr), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                          _ptr(sink), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dsink), _ptr(workspace),
+                          workspace.numel(), _stream())
+    _lib.check("sinkattn_bwd", st)
+    return dq, dk, dv, dsink
+
+
+def sinkattn_varlen_plan(seqlens: torch.Tensor) -> torch.Tensor:
+    """Device int32 lengths [B] -> device int32 offsets [B + 1]."""
+    lib = _lib.load()
+    cu = torch.empty(seqlens.numel() + 1, dtype=torch.int32, device=seqlens.device)
+    _lib.check("sinkattn_varlen_plan",
+               lib.sinkattn_varlen_plan(_ptr(seqlens), seqlens.numel(), _ptr(cu), _stream()))
+    return cu
+
+
+def sinkattn_pack(padded: torch.Tensor, cu_seqlens: torch.Tensor, total_tokens: int) -> torch.Tensor:
+    """[B, Smax, H, D] bf16 -> [T, H, D] (rows past each length dropped)."""
+    lib = _lib.load()
+    B, Smax, H, D = padded.shape
+    packed = torch.empty((total_tokens, H, D), dtype=padded.dtype, device=padded.device)
+    _lib.check("sinkattn_pack", lib.sinkattn_pack(_ptr(padded), _ptr(cu_seqlens), B, Smax, H, D,
+                                                  _ptr(packed), _stream()))
+    return packed
+
+
+def sinkattn_unpack(packed: torch.Tensor, cu_seqlens: torch.Tensor, B: int, Smax: int) -> torch.Tensor:
+    """[T, H, D] -> [B, Smax, H, D] with zero padding rows."""
+    lib = _lib.load()
+    T, H, D = packed.shape
+    padded = torch.empty((B, Smax, H, D), dtype=packed.dtype, device=packed.device)
+    _lib.check("sinkattn_unpack", lib.sinkattn_unpack(_ptr(packed), _ptr(cu_seqlens), B, Smax, H, D,
+                                                      _ptr(padded), _stream()))
+    return padded
+
+
+def sinkattn_get_device_status() -> int:
+    """Synchronise the current stream and return (and clear) the device status."""
+    return int(_lib.load().sinkattn_get_device_status(_stream()))
+
+
+PROFILE_FWD, PROFILE_BWD_MAIN = 1, 2
+
+
+def sinkattn_set_profile_events(kind: int, start=None, stop=None) -> None:
+    """Record torch.cuda.Event ``start``/``stop`` around the selected kernel
+    (PROFILE_FWD or PROFILE_BWD_MAIN) of every later call; None clears."""
+    lib = _lib.load()
+    ps = None if start is None else start.cuda_event
+    pe = None if stop is None else stop.cuda_event
+    _lib.check("sinkattn_set_profile_events", lib.sinkattn_set_profile_events(kind, ps, pe))
+
+
+class SinkAttention(torch.autograd.Function):
+    """Autograd wrapper: forward and backward both run in libsinkattn.so."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, sink, problem):
+        o, lse = sinkattn_fwd(q, k, v, sink, **problem)
+        ctx.save_for_backward(q, k, v, sink, o, lse)
+        ctx.problem = problem
+        ctx.mark_non_differentiable(lse)
+        return o, lse
+
+    @staticmethod
+    def backward(ctx, do, dlse):
+        q, k, v, sink, o, lse = ctx.saved_tensors
+        dq, dk, dv, dsink = sinkattn_bwd(q, k, v, o, lse, do.contiguous(), sink, **ctx.problem)
+        return dq, dk, dv, dsink, None
+
+
+def sink_attention(q, k, v, sink, **problem):
+    """Differentiable sink-aware attention; returns the output only."""
+    o, _ = SinkAttention.apply(q, k, v, sink, problem)
+    return o

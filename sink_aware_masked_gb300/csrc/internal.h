@@ -1,0 +1,79 @@
+// Parameters handed from the C-ABI layer to the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sa {
+
+constexpr int kHeadDim = 64;
+constexpr int kMaxHeadsQ = 256;
+
+// Problem after validation and normalisation (see sinkattn_api.cu).
+struct Problem {
+  int num_seqs;
+  int seqlen;              // uniform length, or the longest packed sequence
+  const int32_t* cu;       // device offsets or nullptr (uniform batch)
+  const int32_t* cu_host;  // host offsets or nullptr
+  int total_tokens;
+  int hq, hkv;
+  int window;              // -1 = unbounded (any w >= seqlen - 1 is folded into -1)
+  int prefix;              // clamped to [0, seqlen]
+  int causal;
+  float scale;
+};
+
+struct FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* sink;
+  void* o;
+  float* lse;
+};
+
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const float* lse;
+  const void* dout;
+  const float* sink;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* dsink;
+  // workspace carve-up
+  float* dq_accum;    // [T, Hq, 64] fp32
+  float* delta;       // [Hq, T]  D = <dO, O>
+  float* lse_log2;    // [Hq, T]  (l + softplus(sink - l)) * log2(e)
+  float* dsink_part;  // [preprocess blocks, Hq]
+  int preprocess_blocks;
+};
+
+// Preprocess tokens per block (bounds the number of dsink partial rows).
+constexpr int kPreTokens = 32;
+
+inline int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+// Optional events recorded around the main kernels (measurement hook).
+struct ProfileEvents {
+  cudaEvent_t start = nullptr, stop = nullptr;
+};
+extern ProfileEvents g_prof_fwd, g_prof_bwd;
+
+inline cudaError_t prof_begin(const ProfileEvents& e, cudaStream_t s) {
+  return e.start ? cudaEventRecord(e.start, s) : cudaSuccess;
+}
+inline cudaError_t prof_end(const ProfileEvents& e, cudaStream_t s) {
+  return e.stop ? cudaEventRecord(e.stop, s) : cudaSuccess;
+}
+
+cudaError_t launch_fwd_mma(const Problem& p, const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_mma(const Problem& p, const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_varlen_plan(const int32_t* seqlens, int n, int32_t* cu, cudaStream_t s);
+cudaError_t launch_pack(const void* src, const int32_t* cu, int B, int Smax, int H, int D, void* dst, bool unpack,
+                        cudaStream_t s);
+
+}  // namespace sa

@@ -1,0 +1,232 @@
+// C ABI of the sink-aware attention library: argument checks, problem
+// normalisation, workspace layout and kernel dispatch.  Declarations and the
+// contract of every entry point are in include/sinkattn.h.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/sinkattn.h"
+#include "internal.h"
+
+namespace sa {
+ProfileEvents g_prof_fwd, g_prof_bwd;
+}
+
+namespace {
+
+// Device status word raised by kernels that give up a bounded wait.
+__device__ int g_device_status = 0;
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Validates `pr` and fills `out`.  Touches no CUDA API.
+sinkattn_status normalise(const sinkattn_problem* pr, sa::Problem& out) {
+  if (pr == nullptr) return SINKATTN_ERR_INVALID_ARG;
+  if (pr->head_dim != sa::kHeadDim) return SINKATTN_ERR_UNSUPPORTED;
+  if (pr->num_heads_kv < 1 || pr->num_heads_q < 1 || pr->num_heads_q % pr->num_heads_kv != 0)
+    return SINKATTN_ERR_INVALID_ARG;
+  if (pr->num_heads_q > sa::kMaxHeadsQ) return SINKATTN_ERR_UNSUPPORTED;
+  if (pr->num_seqs < 0 || pr->seqlen < 0 || pr->total_tokens < 0) return SINKATTN_ERR_INVALID_ARG;
+  if (pr->num_seqs > 65535) return SINKATTN_ERR_UNSUPPORTED;
+  if (!(pr->scale > 0.f) || !std::isfinite(pr->scale)) return SINKATTN_ERR_INVALID_ARG;
+  if (pr->window < -1 || pr->prefix < 0) return SINKATTN_ERR_INVALID_ARG;
+  if (pr->causal != 0 && pr->causal != 1) return SINKATTN_ERR_INVALID_ARG;
+  if ((pr->cu_seqlens == nullptr) != (pr->cu_seqlens_host == nullptr)) return SINKATTN_ERR_INVALID_ARG;
+  if (pr->cu_seqlens == nullptr) {
+    const long long t = static_cast<long long>(pr->num_seqs) * pr->seqlen;
+    if (t != pr->total_tokens) return SINKATTN_ERR_INVALID_ARG;
+  } else {
+    const int32_t* cu = pr->cu_seqlens_host;
+    if (cu[0] != 0) return SINKATTN_ERR_INVALID_ARG;
+    int32_t mx = 0;
+    for (int i = 0; i < pr->num_seqs; ++i) {
+      const int32_t len = cu[i + 1] - cu[i];
+      if (cu[i + 1] < cu[i]) return SINKATTN_ERR_INVALID_ARG;
+      if (len > mx) mx = len;
+    }
+    if (cu[pr->num_seqs] != pr->total_tokens) return SINKATTN_ERR_INVALID_ARG;
+    if (mx > pr->seqlen) return SINKATTN_ERR_INVALID_ARG;
+    if (!aligned16(pr->cu_seqlens) && pr->num_seqs > 0) return SINKATTN_ERR_ALIGNMENT;
+  }
+  // 64-bit element counts must stay addressable; the kernels index tokens as int.
+  if (static_cast<long long>(pr->total_tokens) * pr->num_heads_q * sa::kHeadDim > (1LL << 40))
+    return SINKATTN_ERR_UNSUPPORTED;
+  out.num_seqs = pr->num_seqs;
+  out.seqlen = pr->seqlen;
+  out.cu = pr->cu_seqlens;
+  out.cu_host = pr->cu_seqlens_host;
+  out.total_tokens = pr->total_tokens;
+  out.hq = pr->num_heads_q;
+  out.hkv = pr->num_heads_kv;
+  // A window reaching the whole sequence is the unbounded window; a prefix
+  // covering the whole sequence is the same as the sequence length.
+  out.window = (pr->window < 0 || pr->window >= static_cast<int64_t>(pr->seqlen) - 1)
+                   ? -1
+                   : static_cast<int>(pr->window);
+  out.prefix = static_cast<int>(pr->prefix > pr->seqlen ? pr->seqlen : pr->prefix);
+  out.causal = pr->causal;
+  out.scale = pr->scale;
+  return SINKATTN_OK;
+}
+
+struct BwdLayout {
+  size_t dq_accum, delta, lse_log2, part, total;
+  int pre_blocks;
+};
+
+BwdLayout bwd_layout(const sa::Problem& p) {
+  BwdLayout l;
+  const size_t T = static_cast<size_t>(p.total_tokens), H = static_cast<size_t>(p.hq);
+  l.pre_blocks = sa::ceil_div(p.total_tokens, sa::kPreTokens);
+  l.dq_accum = 0;
+  l.delta = l.dq_accum + round_up(T * H * sa::kHeadDim * 4, 256);
+  l.lse_log2 = l.delta + round_up(T * H * 4, 256);
+  l.part = l.lse_log2 + round_up(T * H * 4, 256);
+  l.total = l.part + round_up(static_cast<size_t>(l.pre_blocks) * H * 4, 256) + 256;
+  return l;
+}
+
+sinkattn_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SINKATTN_OK : SINKATTN_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+size_t sinkattn_fwd_workspace_size(const sinkattn_problem* prob) {
+  sa::Problem p;
+  if (normalise(prob, p) != SINKATTN_OK) return 0;
+  return 0;
+}
+
+size_t sinkattn_bwd_workspace_size(const sinkattn_problem* prob) {
+  sa::Problem p;
+  if (normalise(prob, p) != SINKATTN_OK) return 0;
+  return bwd_layout(p).total;
+}
+
+sinkattn_status sinkattn_fwd(const sinkattn_problem* prob, const void* q, const void* k, const void* v,
+                             const float* sink, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  sa::Problem p;
+  sinkattn_status st = normalise(prob, p);
+  if (st != SINKATTN_OK) return st;
+  (void)workspace;
+  (void)workspace_bytes;
+  if (p.total_tokens == 0) return SINKATTN_OK;
+  if (!q || !k || !v || !sink || !o || !lse) return SINKATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(sink))
+    return SINKATTN_ERR_ALIGNMENT;
+  sa::FwdArgs a{q, k, v, sink, o, lse};
+  return from_cuda(sa::launch_fwd_mma(p, a, static_cast<cudaStream_t>(stream)));
+}
+
+sinkattn_status sinkattn_bwd(const sinkattn_problem* prob, const void* q, const void* k, const void* v,
+                             const void* o, const float* lse, const void* dout, const float* sink, void* dq,
+                             void* dk, void* dv, float* dsink, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  sa::Problem p;
+  sinkattn_status st = normalise(prob, p);
+  if (st != SINKATTN_OK) return st;
+  if (!dsink || !sink) return SINKATTN_ERR_INVALID_ARG;
+  if (!aligned16(dsink) || !aligned16(sink)) return SINKATTN_ERR_ALIGNMENT;
+  const BwdLayout L = bwd_layout(p);
+  if (p.total_tokens > 0) {
+    if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return SINKATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+      return SINKATTN_ERR_ALIGNMENT;
+  }
+  if (workspace_bytes < L.total) return SINKATTN_ERR_WORKSPACE;
+  if (workspace == nullptr || !aligned16(workspace)) return workspace ? SINKATTN_ERR_ALIGNMENT : SINKATTN_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  sa::BwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.dout = dout;
+  a.sink = sink;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.dsink = dsink;
+  a.dq_accum = reinterpret_cast<float*>(ws + L.dq_accum);
+  a.delta = reinterpret_cast<float*>(ws + L.delta);
+  a.lse_log2 = reinterpret_cast<float*>(ws + L.lse_log2);
+  a.dsink_part = reinterpret_cast<float*>(ws + L.part);
+  a.preprocess_blocks = L.pre_blocks;
+  return from_cuda(sa::launch_bwd_mma(p, a, static_cast<cudaStream_t>(stream)));
+}
+
+sinkattn_status sinkattn_varlen_plan(const int32_t* seqlens, int32_t num_seqs, int32_t* cu_seqlens_out,
+                                     void* stream) {
+  if (num_seqs < 0 || cu_seqlens_out == nullptr || (num_seqs > 0 && seqlens == nullptr))
+    return SINKATTN_ERR_INVALID_ARG;
+  return from_cuda(sa::launch_varlen_plan(seqlens, num_seqs, cu_seqlens_out, static_cast<cudaStream_t>(stream)));
+}
+
+static sinkattn_status pack_common(const void* src, const int32_t* cu, int32_t B, int32_t Smax, int32_t H,
+                                   int32_t D, void* dst, bool unpack, void* stream) {
+  if (B < 0 || Smax < 0 || H < 1 || D < 1) return SINKATTN_ERR_INVALID_ARG;
+  if ((static_cast<long long>(H) * D * 2) % 16 != 0) return SINKATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Smax == 0) return SINKATTN_OK;
+  if (!src || !cu || !dst) return SINKATTN_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(dst)) return SINKATTN_ERR_ALIGNMENT;
+  return from_cuda(sa::launch_pack(src, cu, B, Smax, H, D, dst, unpack, static_cast<cudaStream_t>(stream)));
+}
+
+sinkattn_status sinkattn_pack(const void* padded, const int32_t* cu_seqlens, int32_t B, int32_t Smax, int32_t H,
+                              int32_t D, void* packed, void* stream) {
+  return pack_common(padded, cu_seqlens, B, Smax, H, D, packed, false, stream);
+}
+
+sinkattn_status sinkattn_unpack(const void* packed, const int32_t* cu_seqlens, int32_t B, int32_t Smax, int32_t H,
+                                int32_t D, void* padded, void* stream) {
+  return pack_common(packed, cu_seqlens, B, Smax, H, D, padded, true, stream);
+}
+
+sinkattn_status sinkattn_get_device_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SINKATTN_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return SINKATTN_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return SINKATTN_ERR_CUDA;
+    return SINKATTN_ERR_TIMEOUT;
+  }
+  return SINKATTN_OK;
+}
+
+sinkattn_status sinkattn_set_profile_events(int32_t kind, void* start, void* stop) {
+  if ((start == nullptr) != (stop == nullptr)) return SINKATTN_ERR_INVALID_ARG;
+  sa::ProfileEvents ev;
+  ev.start = static_cast<cudaEvent_t>(start);
+  ev.stop = static_cast<cudaEvent_t>(stop);
+  if (kind == 1)
+    sa::g_prof_fwd = ev;
+  else if (kind == 2)
+    sa::g_prof_bwd = ev;
+  else
+    return SINKATTN_ERR_INVALID_ARG;
+  return SINKATTN_OK;
+}
+
+const char* sinkattn_status_string(sinkattn_status s) {
+  switch (s) {
+    case SINKATTN_OK: return "ok";
+    case SINKATTN_ERR_INVALID_ARG: return "invalid argument";
+    case SINKATTN_ERR_UNSUPPORTED: return "unsupported problem";
+    case SINKATTN_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case SINKATTN_ERR_WORKSPACE: return "workspace too small";
+    case SINKATTN_ERR_CUDA: return "CUDA error";
+    case SINKATTN_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+int32_t sinkattn_version(void) { return 100; }
+
+}  // extern "C"

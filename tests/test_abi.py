@@ -1,0 +1,137 @@
+"""The C-ABI library builds, loads and exports every declared entry point;
+host-side argument checks return their statuses without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sinkattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sink_aware_masked_gb300 import _lib, build
+
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sinkattn_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for n in ("sinkattn_fwd", "sinkattn_bwd", "sinkattn_varlen_plan", "sinkattn_pack", "sinkattn_unpack",
+              "sinkattn_fwd_workspace_size", "sinkattn_bwd_workspace_size", "sinkattn_get_device_status",
+              "sinkattn_status_string", "sinkattn_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from sink_aware_masked_gb300 import _lib
+
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared but not exported"
+        assert name in _lib.SIGNATURES, f"{name} has no binding signature"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.sinkattn_version() >= 100
+    assert lib.sinkattn_status_string(0) == b"ok"
+    assert lib.sinkattn_status_string(3).startswith(b"pointer")
+    assert lib.sinkattn_status_string(99) == b"unknown status"
+
+
+def problem(**kw):
+    from sink_aware_masked_gb300 import _lib
+
+    base = dict(num_seqs=1, seqlen=256, cu_seqlens=None, cu_seqlens_host=None, total_tokens=256,
+                num_heads_q=8, num_heads_kv=2, head_dim=64, window=-1, prefix=0, causal=1, scale=0.125)
+    base.update(kw)
+    return _lib.Problem(**base)
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call below fails validation first
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=128), 2),
+    (dict(num_heads_q=6, num_heads_kv=4), 1),
+    (dict(num_heads_kv=0), 1),
+    (dict(num_heads_q=512, num_heads_kv=2), 2),
+    (dict(window=-2), 1),
+    (dict(prefix=-1), 1),
+    (dict(scale=0.0), 1),
+    (dict(scale=float("nan")), 1),
+    (dict(scale=float("inf")), 1),
+    (dict(causal=2), 1),
+    (dict(total_tokens=255), 1),
+    (dict(num_seqs=-1), 1),
+])
+def test_invalid_problem(lib, kw, status):
+    pr = problem(**kw)
+    assert lib.sinkattn_fwd(ctypes.byref(pr), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, None) == status
+    assert lib.sinkattn_fwd_workspace_size(ctypes.byref(pr)) == 0
+    assert lib.sinkattn_bwd_workspace_size(ctypes.byref(pr)) == 0
+
+
+def test_null_and_misaligned_pointers(lib):
+    pr = problem()
+    assert lib.sinkattn_fwd(ctypes.byref(pr), None, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, None) == 1
+    assert lib.sinkattn_fwd(ctypes.byref(pr), FAKE + 8, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, None) == 3
+    ws = lib.sinkattn_bwd_workspace_size(ctypes.byref(pr))
+    args = [FAKE] * 11
+    # workspace too small
+    assert lib.sinkattn_bwd(ctypes.byref(pr), *args, FAKE, ws - 1, None) == 4
+    # misaligned dq
+    bad = list(args)
+    bad[7] = FAKE + 2
+    assert lib.sinkattn_bwd(ctypes.byref(pr), *bad, FAKE, ws, None) == 3
+    assert lib.sinkattn_bwd(ctypes.byref(pr), *args, None, ws, None) == 1
+
+
+def test_workspace_sizes_are_linear_in_tokens(lib):
+    sizes = []
+    for S in (1024, 2048, 4096, 8192):
+        pr = problem(seqlen=S, total_tokens=S, num_heads_q=64, num_heads_kv=8)
+        sizes.append(lib.sinkattn_bwd_workspace_size(ctypes.byref(pr)))
+        # dQ accumulator fp32 + two [Hq, T] fp32 rows + dsink partials: linear in T
+        assert sizes[-1] >= S * 64 * 64 * 4 + 2 * S * 64 * 4
+    d1, d2, d3 = sizes[1] - sizes[0], sizes[2] - sizes[1], sizes[3] - sizes[2]
+    assert abs(d2 - 2 * d1) <= 1024 and abs(d3 - 2 * d2) <= 2048
+    assert lib.sinkattn_fwd_workspace_size(ctypes.byref(problem())) == 0
+
+
+def test_varlen_offsets_validation(lib):
+    from sink_aware_masked_gb300 import _lib
+
+    def mk(host, total, seqlen):
+        arr = (ctypes.c_int32 * len(host))(*host)
+        pr = _lib.Problem(num_seqs=len(host) - 1, seqlen=seqlen, cu_seqlens=FAKE,
+                          cu_seqlens_host=ctypes.cast(arr, ctypes.c_void_p).value, total_tokens=total,
+                          num_heads_q=4, num_heads_kv=4, head_dim=64, window=-1, prefix=0, causal=1, scale=0.1)
+        return pr, arr
+
+    for host, total, seqlen in (([1, 5], 5, 5), ([0, 5, 3], 3, 5), ([0, 5, 9], 8, 5), ([0, 5, 9], 9, 4)):
+        pr, keep = mk(host, total, seqlen)
+        assert lib.sinkattn_fwd(ctypes.byref(pr), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, None) == 1
+    pr, keep = mk([0, 5, 9], 9, 5)
+    assert lib.sinkattn_bwd_workspace_size(ctypes.byref(pr)) > 0
+    # cu_seqlens given without its host copy
+    pr = _lib.Problem(num_seqs=1, seqlen=4, cu_seqlens=FAKE, cu_seqlens_host=None, total_tokens=4,
+                      num_heads_q=4, num_heads_kv=4, head_dim=64, window=-1, prefix=0, causal=1, scale=0.1)
+    assert lib.sinkattn_fwd(ctypes.byref(pr), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, None) == 1
+
+
+def test_pack_validation(lib):
+    assert lib.sinkattn_pack(FAKE, FAKE, -1, 4, 2, 64, FAKE, None) == 1
+    assert lib.sinkattn_pack(FAKE, FAKE, 2, 4, 1, 4, FAKE, None) == 2       # 8-byte rows
+    assert lib.sinkattn_unpack(FAKE + 4, FAKE, 2, 4, 2, 64, FAKE, None) == 3
+    assert lib.sinkattn_varlen_plan(FAKE, -3, FAKE, None) == 1
+    assert lib.sinkattn_varlen_plan(None, 3, FAKE, None) == 1

@@ -1,0 +1,229 @@
+"""CUDA path vs the CPU float64 oracle, element by element (needs a GB300).
+
+All calls go through the C ABI (libsinkattn.so) via the thin binding.
+Small problems are compared in full; the full-size workloads run complete
+on the GPU and are compared on whole GQA groups (every query head of one
+key/value head, all sequences), which the oracle computes one head per
+process.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from tests import parity_util as pu
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from sink_aware_masked_gb300 import build
+
+    build.build()
+
+
+def problem_kwargs(wl, window=None):
+    kw = dict(window=wl.window if window is None else window, prefix=wl.prefix, causal=wl.causal, scale=wl.scale)
+    if wl.uniform:
+        kw["num_seqs"] = wl.num_seqs
+    else:
+        cu = wl.cu_seqlens()
+        kw.update(cu_seqlens=torch.tensor(cu, dtype=torch.int32, device=DEV), cu_seqlens_host=[int(x) for x in cu],
+                  max_seqlen=wl.max_seqlen)
+    return kw
+
+
+def gpu_run(inp, wl, sink=None, window=None):
+    import sink_aware_masked_gb300 as sa
+
+    q, k, v, do = (t.to(DEV) for t in (inp.q_bf16, inp.k_bf16, inp.v_bf16, inp.do_bf16))
+    s = (inp.sink if sink is None else sink).to(DEV)
+    kw = problem_kwargs(wl, window)
+    o, lse = sa.sinkattn_fwd(q, k, v, s, **kw)
+    dq, dk, dv, dsink = sa.sinkattn_bwd(q, k, v, o, lse, do, s, **kw)
+    assert sa.sinkattn_get_device_status() == 0
+    return dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv, dsink=dsink)
+
+
+def full_compare(wl, inp=None, label=None):
+    inp = inp or W.make_inputs(wl)
+    gpu = gpu_run(inp, wl)
+    heads = list(range(wl.num_heads_q))
+    ref = pu.oracle_heads(inp, wl, heads)
+    errs = pu.errors(gpu, ref, heads, list(range(wl.num_heads_kv)))
+    pu.assert_within(errs, label or wl.name)
+    return errs
+
+
+def test_tiny_workload():
+    full_compare(W.WORKLOADS["tiny_s128_w32_p4"])
+
+
+SMALL = [
+    W.custom((300,), 4, 2, seed=10, name="s300_causal"),
+    W.custom((300,), 4, 2, window=37, prefix=5, seed=11, name="s300_w37_p5"),
+    W.custom((513,), 4, 1, window=128, prefix=4, seed=12, name="s513_w128_p4_mqa"),
+    W.custom((200,), 2, 2, window=0, seed=13, name="s200_w0"),
+    W.custom((257,), 4, 4, causal=False, seed=14, name="s257_noncausal"),
+    W.custom((190,), 4, 2, window=50, prefix=70, causal=False, seed=15, name="s190_noncausal_w50_p70"),
+    W.custom((1, 130, 257, 64, 0, 129), 8, 2, seed=16, name="varlen_causal"),
+    W.custom((1, 130, 257, 64, 0, 129), 8, 2, window=128, prefix=4, seed=17, name="varlen_w128_p4"),
+    W.custom((1,), 2, 1, seed=18, name="s1"),
+    W.custom((128,), 8, 1, window=64, seed=19, name="s128_group8_w64"),
+    W.custom((384,), 4, 2, window=16, prefix=200, seed=20, name="s384_w16_p200"),
+    W.custom((640,), 2, 1, window=127, seed=21, name="s640_w127"),
+    W.custom((640,), 2, 1, window=129, prefix=1, seed=22, name="s640_w129_p1"),
+    W.custom((777, 1025), 4, 2, seed=23, sink_dist="uniform2", name="varlen2_ragged"),
+]
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+def test_small_cases(wl):
+    full_compare(wl)
+
+
+@pytest.mark.parametrize("sinkval", [float("-inf"), float("inf"), -30.0, 30.0])
+def test_sink_extremes(sinkval):
+    wl = W.custom((200,), 4, 2, window=40, prefix=3, seed=30, name="sink_extreme")
+    inp = W.make_inputs(wl)
+    inp.sink = torch.full((4,), sinkval, dtype=torch.float32)
+    gpu = gpu_run(inp, wl)
+    for key in ("o", "dq", "dk", "dv", "dsink"):
+        assert torch.isfinite(gpu[key]).all(), key
+    ref = pu.oracle_heads(inp, wl, range(4))
+    errs = pu.errors(gpu, ref, range(4), [0, 1])
+    if sinkval == float("inf"):
+        # alpha = 0: every output and gradient is exactly zero
+        for key in ("o", "dq", "dk", "dv", "dsink"):
+            assert float(gpu[key].abs().max()) == 0.0, key
+        errs.pop("dsink")
+    pu.assert_within(errs, f"sink={sinkval}")
+
+
+FULL = ["causal_gqa_s4096", "window128_gqa_s4096", "causal_gqa_b2_s8192", "window128_prefix4_gqa_b2_s8192",
+        "varlen8_window128", "varlen8_causal"]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workload_group(name):
+    """Full-size run on the GPU; one whole GQA group (8 query heads) checked."""
+    wl = W.WORKLOADS[name]
+    inp = W.make_inputs(wl)
+    gpu = gpu_run(inp, wl)
+    for key in ("o", "lse", "dq", "dk", "dv", "dsink"):
+        assert torch.isfinite(gpu[key]).all(), key
+    group = wl.num_heads_q // wl.num_heads_kv
+    g = 3 if wl.num_heads_kv > 3 else 0
+    heads = list(range(g * group, (g + 1) * group))
+    ref = pu.oracle_heads(inp, wl, heads)
+    pu.assert_within(pu.errors(gpu, ref, heads, [g]), name)
+
+
+def test_determinism_and_window_fold():
+    wl = W.custom((1500,), 8, 2, seed=40, sink_dist="uniform2", name="det")
+    inp = W.make_inputs(wl)
+    a = gpu_run(inp, wl)
+    b = gpu_run(inp, wl)
+    for key in ("o", "lse", "dk", "dv", "dsink"):
+        assert torch.equal(a[key], b[key]), key
+    assert pu.rel_l2(a["dq"].double().cpu().numpy(), b["dq"].double().cpu().numpy()) < 1e-3
+    for w in (1499, 1500, 10**9):
+        c = gpu_run(inp, wl, window=w)
+        for key in ("o", "lse", "dk", "dv", "dsink"):
+            assert torch.equal(a[key], c[key]), (w, key)
+
+
+def test_packed_equals_per_sequence():
+    lens = (513, 1, 200, 1000)
+    wl = W.custom(lens, 8, 2, window=100, prefix=3, seed=41, name="packed")
+    inp = W.make_inputs(wl)
+    packed = gpu_run(inp, wl)
+    cu = wl.cu_seqlens()
+    dsink = torch.zeros(8, dtype=torch.float64)
+    for i, n in enumerate(lens):
+        t0, t1 = int(cu[i]), int(cu[i + 1])
+        one_wl = W.custom((n,), 8, 2, window=100, prefix=3, seed=41, name="one")
+        one = W.Inputs(one_wl, inp.q_bf16[t0:t1].clone(), inp.k_bf16[t0:t1].clone(), inp.v_bf16[t0:t1].clone(),
+                       inp.do_bf16[t0:t1].clone(), inp.sink.clone())
+        r = gpu_run(one, one_wl)
+        for key in ("o", "dk", "dv"):
+            assert torch.equal(packed[key][t0:t1], r[key]), (i, key)
+        assert torch.equal(packed["lse"][:, t0:t1], r["lse"]), i
+        assert pu.rel_l2(packed["dq"][t0:t1].double().cpu().numpy(), r["dq"].double().cpu().numpy()) < 1e-3
+        dsink += r["dsink"].double().cpu()
+    assert pu.rel_l2(packed["dsink"].double().cpu().numpy(), dsink.numpy()) < 1e-5
+
+
+def test_empty_problem():
+    import sink_aware_masked_gb300 as sa
+
+    q = torch.empty((0, 4, 64), dtype=torch.bfloat16, device=DEV)
+    k = torch.empty((0, 2, 64), dtype=torch.bfloat16, device=DEV)
+    sink = torch.randn(4, device=DEV)
+    o, lse = sa.sinkattn_fwd(q, k, k, sink, num_seqs=0)
+    dq, dk, dv, dsink = sa.sinkattn_bwd(q, k, k, o, lse, q, sink, num_seqs=0)
+    torch.cuda.synchronize()
+    assert o.shape == (0, 4, 64) and float(dsink.abs().max()) == 0.0
+
+
+def test_varlen_plan_pack_unpack_exact():
+    import sink_aware_masked_gb300 as sa
+
+    g = torch.Generator().manual_seed(5)
+    for n in (1, 8, 1000, 2500):
+        lens = torch.randint(0, 3000, (n,), generator=g, dtype=torch.int32)
+        cu = sa.sinkattn_varlen_plan(lens.to(DEV)).cpu()
+        want = torch.zeros(n + 1, dtype=torch.int64)
+        want[1:] = torch.cumsum(lens.to(torch.int64), 0)
+        assert torch.equal(cu.to(torch.int64), want), n
+    lens = [5, 0, 17, 3]
+    B, Smax, H, D = 4, 17, 3, 64
+    padded = torch.randn((B, Smax, H, D), generator=g).to(torch.bfloat16)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
+    packed = sa.sinkattn_pack(padded.to(DEV), cu.to(DEV), int(cu[-1])).cpu()
+    want = torch.cat([padded[b, :lens[b]] for b in range(B)], 0)
+    assert torch.equal(packed, want)
+    back = sa.sinkattn_unpack(packed.to(DEV), cu.to(DEV), B, Smax).cpu()
+    for b in range(B):
+        assert torch.equal(back[b, :lens[b]], padded[b, :lens[b]])
+        assert float(back[b, lens[b]:].float().abs().max() if lens[b] < Smax else 0.0) == 0.0
+
+
+def test_autograd_matches_direct_calls():
+    import sink_aware_masked_gb300 as sa
+
+    wl = W.custom((333,), 4, 2, window=64, prefix=2, seed=50, name="autograd")
+    inp = W.make_inputs(wl)
+    direct = gpu_run(inp, wl)
+    q, k, v = (t.to(DEV).requires_grad_() for t in (inp.q_bf16, inp.k_bf16, inp.v_bf16))
+    s = inp.sink.to(DEV).requires_grad_()
+    o = sa.sink_attention(q, k, v, s, **problem_kwargs(wl))
+    o.backward(inp.do_bf16.to(DEV))
+    assert torch.equal(o.detach(), direct["o"])
+    for t, key in ((k, "dk"), (v, "dv"), (s, "dsink")):
+        assert torch.equal(t.grad, direct[key]), key
+    assert pu.rel_l2(q.grad.double().cpu().numpy(), direct["dq"].double().cpu().numpy()) < 1e-3
+
+
+def test_peak_memory_linear_in_sequence_length():
+    import sink_aware_masked_gb300 as sa
+
+    peaks = []
+    for S in (2048, 4096, 8192, 16384):
+        wl = W.custom((S,), 16, 2, seed=60, name="mem")
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        base = torch.cuda.memory_allocated()
+        torch.cuda.reset_peak_memory_stats()
+        gpu_run(W.make_inputs(wl), wl)
+        torch.cuda.synchronize()
+        peaks.append(torch.cuda.max_memory_allocated() - base)
+    d = np.diff(peaks) / np.diff([2048, 4096, 8192, 16384])
+    # bytes per extra token stay constant (no S^2 term)
+    assert np.max(d) / np.min(d) < 1.05, peaks
