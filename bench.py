@@ -192,13 +192,14 @@ def cpu_baseline(wl, pool=None):
     pool = pool or OraclePool()
     try:
         jobs, flops = oracle_sample_jobs(wl, pool.cores)
-        sec = pool.run(jobs)
+        rounds = 3
+        sec = sum(pool.run(jobs) for _ in range(rounds))
     finally:
         if own:
             pool.close()
-    return {"value": flops / sec / 1e12, "unit": "TFLOP/s", "cores": pool.cores, "kind": "oracle",
-            "sample": f"{len(jobs)} query heads x 1 sequence of {wl.seqlens[0]} tokens of {wl.name}, fwd+bwd, "
-                      f"one single-threaded worker per head, {sec:.2f} s wall"}
+    return {"value": rounds * flops / sec / 1e12, "unit": "TFLOP/s", "cores": pool.cores, "kind": "oracle",
+            "sample": f"{rounds} rounds of {len(jobs)} query heads x 1 sequence of {wl.seqlens[0]} tokens of "
+                      f"{wl.name}, fwd+bwd, one single-threaded worker per head, {sec:.2f} s wall"}
 
 
 def run_reference(args, rank):
@@ -302,6 +303,10 @@ def run_gpu(args, world, rank, local):
 
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for e in ev:  # torch creates the CUDA event on first record(); the hook needs the handle
+        for x in e:
+            x.record()
+    torch.cuda.synchronize()
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     barrier(world)
     torch.cuda.synchronize()
@@ -402,7 +407,18 @@ def _committed_traffic(workload, kernel):
         return None
     with open(path) as f:
         d = json.load(f)
-    return d.get(workload, {}).get(kernel)
+    rec = d.get(workload, {}).get(kernel)
+    if not rec:
+        return None
+    import hashlib
+
+    src = os.path.join(ROOT, rec["source"])
+    if not os.path.exists(src):
+        return None
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != rec["sha256"]:
+            return None  # the kernel changed since the counters were taken
+    return rec["bytes"]
 
 
 def main(argv=None):

@@ -147,6 +147,8 @@ def sinkattn_set_profile_events(kind: int, start=None, stop=None) -> None:
     lib = _lib.load()
     ps = None if start is None else start.cuda_event
     pe = None if stop is None else stop.cuda_event
+    if start is not None and (not ps or not pe):
+        raise ValueError("record the events once before installing them (torch creates them lazily)")
     _lib.check("sinkattn_set_profile_events", lib.sinkattn_set_profile_events(kind, ps, pe))
 
 
