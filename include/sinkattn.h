@@ -105,6 +105,25 @@ sinkattn_status sinkattn_bwd(const sinkattn_problem* prob,
                              void* dq, void* dk, void* dv, float* dsink,
                              void* workspace, size_t workspace_bytes, void* stream);
 
+/* Backward without a caller-provided workspace, for callers that cannot
+ * allocate device memory (a host program with no device allocator of its
+ * own, a runtime whose memory pool is fixed at start-up, a hot loop where an
+ * allocation is not acceptable).  The paper has no counterpart: this is a
+ * deployment variant of sinkattn_bwd, same arguments minus the workspace,
+ * same results.  It uses a 32 MiB workspace compiled into the library as a
+ * device array (held by every GPU that loads the library until the process
+ * ends) and allocates nothing.  Problems whose sinkattn_bwd_workspace_size()
+ * exceeds 32 MiB return SINKATTN_ERR_WORKSPACE and launch nothing.  The
+ * first call on each device looks up the array's device address while that
+ * device is current; make it before any stream capture.  All calls share
+ * the array: calls whose kernels overlap on the GPU race and must be
+ * serialised by the caller.  Nothing in the array needs clearing between
+ * calls (the kernels clear what they accumulate into). */
+sinkattn_status sinkattn_bwd_noalloc(const sinkattn_problem* prob,
+                                     const void* q, const void* k, const void* v, const void* o,
+                                     const float* lse, const void* dout, const float* sink,
+                                     void* dq, void* dk, void* dv, float* dsink, void* stream);
+
 /* Packed-sequence front end (multi-turn trajectories of different lengths,
  * SinkFlex-RL section 3).  seqlens: device int32 [num_seqs];
  * cu_seqlens_out: device int32 [num_seqs + 1] receives the exclusive prefix
