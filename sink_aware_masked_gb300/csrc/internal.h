@@ -70,7 +70,7 @@ inline cudaError_t prof_end(const ProfileEvents& e, cudaStream_t s) {
   return e.stop ? cudaEventRecord(e.stop, s) : cudaSuccess;
 }
 
-cudaError_t launch_fwd_mma(const Problem& p, const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_fwd_tc(const Problem& p, const FwdArgs& a, int* status, cudaStream_t s);
 cudaError_t launch_bwd_mma(const Problem& p, const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_varlen_plan(const int32_t* seqlens, int n, int32_t* cu, cudaStream_t s);
 cudaError_t launch_pack(const void* src, const int32_t* cu, int B, int Smax, int H, int D, void* dst, bool unpack,

@@ -17,6 +17,19 @@ namespace {
 // Device status word raised by kernels that give up a bounded wait.
 __device__ int g_device_status = 0;
 
+// Device address of g_device_status for the current device (looked up once).
+int* status_word() {
+  static int* ptr[256] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return nullptr;
+  if (ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    ptr[dev] = static_cast<int*>(p);
+  }
+  return ptr[dev];
+}
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -119,7 +132,9 @@ sinkattn_status sinkattn_fwd(const sinkattn_problem* prob, const void* q, const 
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(sink))
     return SINKATTN_ERR_ALIGNMENT;
   sa::FwdArgs a{q, k, v, sink, o, lse};
-  return from_cuda(sa::launch_fwd_mma(p, a, static_cast<cudaStream_t>(stream)));
+  int* status = status_word();
+  if (status == nullptr) return SINKATTN_ERR_CUDA;
+  return from_cuda(sa::launch_fwd_tc(p, a, status, static_cast<cudaStream_t>(stream)));
 }
 
 sinkattn_status sinkattn_bwd(const sinkattn_problem* prob, const void* q, const void* k, const void* v,
