@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const ConvK p) {
 
 }  // namespace
 
-cudaError_t launch_bwd_mma(const Problem& pr, const BwdArgs& a, cudaStream_t stream) {
+cudaError_t launch_bwd(const Problem& pr, const BwdArgs& a, int* status, cudaStream_t stream) {
   const long long T = pr.total_tokens;
   {
     PreK k{static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.sink,
@@ -420,34 +420,9 @@ cudaError_t launch_bwd_mma(const Problem& pr, const BwdArgs& a, cudaStream_t str
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  const int n_kt = ceil_div(pr.seqlen, BNK);
-  if (n_kt > 0 && pr.num_seqs > 0) {
-    MainK k;
-    k.q = static_cast<const __nv_bfloat16*>(a.q);
-    k.k = static_cast<const __nv_bfloat16*>(a.k);
-    k.v = static_cast<const __nv_bfloat16*>(a.v);
-    k.dout = static_cast<const __nv_bfloat16*>(a.dout);
-    k.lse_log2 = a.lse_log2;
-    k.delta = a.delta;
-    k.dq_accum = a.dq_accum;
-    k.dk = static_cast<__nv_bfloat16*>(a.dk);
-    k.dv = static_cast<__nv_bfloat16*>(a.dv);
-    k.cu = pr.cu;
-    k.seqlen = pr.seqlen;
-    k.T = T;
-    k.hq = pr.hq;
-    k.hkv = pr.hkv;
-    k.group = pr.hq / pr.hkv;
-    k.mask = MaskParams{pr.window, pr.prefix, pr.causal};
-    k.scale = pr.scale;
-    k.scale_log2 = pr.scale * kLog2e;
-    cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAIN);
+  {
+    cudaError_t e = launch_bwd_tc_main(pr, a, status, stream);
     if (e != cudaSuccess) return e;
-    dim3 grid(pr.hkv, pr.num_seqs, n_kt);
-    if ((e = prof_begin(g_prof_bwd, stream)) != cudaSuccess) return e;
-    bwd_main_kernel<<<grid, NTHR, SMEM_MAIN, stream>>>(k);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = prof_end(g_prof_bwd, stream)) != cudaSuccess) return e;
   }
   {
     ConvK k{a.dq_accum, static_cast<__nv_bfloat16*>(a.dq), T * pr.hq * D / 8, pr.scale, a.dsink_part,

@@ -71,7 +71,8 @@ inline cudaError_t prof_end(const ProfileEvents& e, cudaStream_t s) {
 }
 
 cudaError_t launch_fwd_tc(const Problem& p, const FwdArgs& a, int* status, cudaStream_t s);
-cudaError_t launch_bwd_mma(const Problem& p, const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd(const Problem& p, const BwdArgs& a, int* status, cudaStream_t s);
+cudaError_t launch_bwd_tc_main(const Problem& p, const BwdArgs& a, int* status, cudaStream_t s);
 cudaError_t launch_varlen_plan(const int32_t* seqlens, int n, int32_t* cu, cudaStream_t s);
 cudaError_t launch_pack(const void* src, const int32_t* cu, int B, int Smax, int H, int D, void* dst, bool unpack,
                         cudaStream_t s);

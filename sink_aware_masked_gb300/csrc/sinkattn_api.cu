@@ -173,7 +173,9 @@ sinkattn_status sinkattn_bwd(const sinkattn_problem* prob, const void* q, const 
   a.lse_log2 = reinterpret_cast<float*>(ws + L.lse_log2);
   a.dsink_part = reinterpret_cast<float*>(ws + L.part);
   a.preprocess_blocks = L.pre_blocks;
-  return from_cuda(sa::launch_bwd_mma(p, a, static_cast<cudaStream_t>(stream)));
+  int* status = status_word();
+  if (status == nullptr) return SINKATTN_ERR_CUDA;
+  return from_cuda(sa::launch_bwd(p, a, status, static_cast<cudaStream_t>(stream)));
 }
 
 sinkattn_status sinkattn_varlen_plan(const int32_t* seqlens, int32_t num_seqs, int32_t* cu_seqlens_out,

@@ -81,6 +81,23 @@ SA_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, ui
       : "memory");
 }
 
+// Element-wise atomic add of a shared-memory tile into global memory (fp32).
+SA_DEV void tma_reduce_add_2d(const CUtensorMap* map, int c0, int c1, uint32_t src) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];\n" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(c0), "r"(c1), "r"(src)
+      : "memory");
+}
+SA_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+// Wait until the source shared memory of committed bulk groups may be reused.
+SA_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+// Wait until every committed bulk group has completed.
+SA_DEV void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+
+// Named barrier over `n` threads (id 1..15; id 0 is __syncthreads).
+SA_DEV void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory"); }
+
 // ------------------------------------------------------------------ TMEM
 SA_DEV void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(dst_smem), "r"(ncols)
@@ -156,6 +173,14 @@ SA_DEV void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
       "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
       SA_W8(0), SA_W8(8), SA_W8(16), SA_W8(24)
+      : "memory");
+}
+// 16 consecutive 32-bit columns.
+SA_DEV void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
+          taddr),
+      SA_W8(0), SA_W8(8)
       : "memory");
 }
 SA_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }

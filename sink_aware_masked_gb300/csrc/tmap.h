@@ -43,4 +43,18 @@ inline bool make_rows_map(CUtensorMap* m, const void* base, long long tokens, in
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 [T, H * 64] accumulator: boxes of 32 floats (128 B) x box_rows tokens,
+// 128-byte swizzled in shared memory; used for element-wise reduce-adds.
+inline bool make_f32_rows_map(CUtensorMap* m, void* base, long long tokens, int heads, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(heads) * 64, static_cast<cuuint64_t>(tokens)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(heads) * 64 * 4};
+  cuuint32_t box[2] = {32, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace sa
