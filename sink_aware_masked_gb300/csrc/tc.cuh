@@ -81,6 +81,21 @@ SA_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, ui
       : "memory");
 }
 
+// 4-byte asynchronous copy global -> shared (Ampere-style cp.async).
+SA_DEV void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");
+}
+// Arrive on `bar` once every cp.async this thread issued so far has landed;
+// the arrival counts toward the barrier's expected count.
+SA_DEV void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
+}
+SA_DEV float4 ld_shared_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];\n" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
+}
+
 // Element-wise atomic add of a shared-memory tile into global memory (fp32).
 SA_DEV void tma_reduce_add_2d(const CUtensorMap* map, int c0, int c1, uint32_t src) {
   asm volatile(
