@@ -12,28 +12,32 @@
 //
 // Work unit (one CTA): 128 keys of one sequence and one kv head; the CTA
 // loops over the query heads of the GQA group x the 128-row query tiles that
-// can see those keys, so dK and dV accumulate in Tensor Memory without
-// atomics.  Warp roles (16 warps, four warpgroups):
+// can see those keys ("steps"), so dK and dV accumulate in Tensor Memory
+// without atomics.  Each step's 128 query rows are split into two 64-row
+// halves A and B, each with its own S^T / dP^T buffers and its own
+// element-wise warpgroup, so the tensor core works on one half while the
+// other half's element-wise pass runs.
+// Warp roles (16 warps, four warpgroups):
 //   warp 0      loader: K, V once; per step Q and dO tiles by TMA (2-stage
 //               ring) and the 128 l' and D values of the query tile by
 //               cp.async, all completing on the stage's full barrier.
-//   warp 1      MMA issuer and TMEM owner.  Per step t:
-//                 S^T(t+1) = K Q^T, dP^T(t+1) = V dO^T   (SS, K-major)
-//                 dV += P^T(t) dO(t)    (A = P^T in TMEM, B = dO MN-major)
-//                 dK += dS^T(t) Q(t)    (A = dS^T K-major in smem, B = Q MN-major)
-//                 dQ(t) = dS(t) K       (A = the same smem tile read MN-major,
-//                                        B = K MN-major)
-//               so the tensor core computes the next step's S^T and dP^T while
-//               the element-wise warps work on this step.
-//   warps 4-11  element-wise, two warpgroups splitting the 128 query columns:
-//               thread = key row.  P^T -> TMEM (packed bf16), dS^T -> a
-//               double-buffered 128 x 128 bf16 shared tile in the
-//               128-byte-swizzled layout both MMAs read; at the end one
-//               warpgroup writes dV, the other dK.  Fully visible tiles take
-//               a path without the mask predicate.
+//   warp 1      MMA issuer and TMEM owner (whole warp, one elected lane
+//               issues).  Per half h of step t:
+//                 dV += P_h^T dO_h, dK += dS_h^T Q_h   (A in TMEM, B MN-major)
+//                 S_h^T(t+1) = K Q_h^T, dP_h^T(t+1) = V dO_h^T   (A = K, V in TMEM)
+//               then for the whole step dQ(t) = dS(t) K (A = dS^T tile in
+//               shared memory read MN-major, B = K MN-major).
+//   warps 4-7   element-wise for half A, warps 8-11 for half B; thread = key
+//               row.  P^T and dS^T (packed bf16) overwrite the S^T and dP^T
+//               columns they were computed from; dS^T also goes to a
+//               double-buffered 128 x 128 bf16 shared tile (128-byte
+//               swizzle) for the dQ product.  At start they copy K and V
+//               into TMEM; at the end one warpgroup writes dV, the other dK.
+//               Fully visible tiles take a path without the mask predicate.
 //   warps 12-15 dQ drain: thread = query row; TMEM -> swizzled fp32 staging
 //               tile -> TMA reduce-add into the fp32 dQ accumulator.
-// Tensor Memory (512 columns): S^T 128 | dP^T 128 | P^T 64 | dV 64 | dK 64 | dQ 64.
+// Tensor Memory (512 columns): S^T A|B (64 each) | dP^T A|B (64 each) |
+// dV 64 | dK 64 | dQ 64 | K 32 | V 32 (bf16 pairs).
 // Every mbarrier wait is bounded; a timeout raises the status word and all
 // warps leave through the common exit, which drains copies and MMAs first.
 #include "common.cuh"
@@ -81,7 +85,8 @@ constexpr int OFF_L = OFF_STG + 2 * TILE;
 constexpr int OFF_DL = OFF_L + NS * BM * 4;
 constexpr int SMEM_DYN = OFF_DL + NS * BM * 4 + 1024;
 
-constexpr uint32_t TM_S = 0, TM_DP = 128, TM_P = 256, TM_DV = 320, TM_DK = 384, TM_DQ = 448;
+constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 320, TM_DQ = 384, TM_K = 448, TM_V = 480;
+constexpr int HALF = BM / 2;
 
 struct BwdTcK {
   CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dq;
@@ -99,9 +104,10 @@ struct BwdTcK {
 };
 
 struct Bars {
-  uint64_t kv_full;
+  uint64_t kv_full, kv_tmem;
   uint64_t q_full[NS], q_empty[NS];
-  uint64_t s_full, p_full, pv_done, dq_full, dq_free, kv_done, drain;
+  uint64_t s_full[2], p_full[2];
+  uint64_t dq_full, dq_free, kv_done, drain;
 };
 
 SA_DEV void wait_drain(uint32_t bar, uint32_t parity) {
@@ -109,6 +115,12 @@ SA_DEV void wait_drain(uint32_t bar, uint32_t parity) {
   while (!mbar_try_wait(bar, parity)) {
     if (clock64() - t0 > kTimeoutCycles) return;
   }
+}
+
+SA_DEV uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
 }
 
 SA_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -119,18 +131,20 @@ SA_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint
 // P^T = exp2(S^T * scale * log2(e) - l'), dS^T = P^T (dP^T - D), packed to bf16
 // pairs.  FULL skips the mask predicate (every pair of the tile visible).
 template <bool FULL>
-SA_DEV void ew_chunk(uint32_t tS, uint32_t tDP, uint32_t sL, uint32_t sD, int c, float sl2, int q0, int key, int len,
+SA_DEV void ew_chunk(uint32_t tS, uint32_t tDP, uint32_t sL, uint32_t sD, float sl2, int qb, int key, int len,
                      const MaskParams& mask, uint32_t (&pp)[16], uint32_t (&dd)[16]) {
+  // tS, tDP: TMEM address of this chunk's 32 columns; sL, sD: shared address
+  // of its 32 l' and D values; qb: position of its first query.
   uint32_t sr[32], dr[32];
-  tmem_ld32(tS + 32 * c, sr);
-  tmem_ld32(tDP + 32 * c, dr);
+  tmem_ld32(tS, sr);
+  tmem_ld32(tDP, dr);
   tmem_ld_wait();
   reg_fence32(sr);
   reg_fence32(dr);
 #pragma unroll
   for (int e = 0; e < 32; e += 4) {
-    const float4 l4 = ld_shared_f4(sL + (32 * c + e) * 4);
-    const float4 d4 = ld_shared_f4(sD + (32 * c + e) * 4);
+    const float4 l4 = ld_shared_f4(sL + e * 4);
+    const float4 d4 = ld_shared_f4(sD + e * 4);
     const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
     const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
     float pe[4], de[4];
@@ -139,7 +153,7 @@ SA_DEV void ew_chunk(uint32_t tS, uint32_t tDP, uint32_t sL, uint32_t sD, int c,
       pe[u] = ex2(fmaf(__uint_as_float(sr[e + u]), sl2, -lv[u]));
       de[u] = pe[u] * (__uint_as_float(dr[e + u]) - dv[u]);
       if (!FULL) {
-        const int q = q0 + 32 * c + e + u;
+        const int q = qb + e + u;
         if (!(q < len && visible(q, key, len, mask))) pe[u] = de[u] = 0.f;
       }
     }
@@ -171,8 +185,10 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
-  const uint32_t b_kv = smem_u32(&bars.kv_full), b_s = smem_u32(&bars.s_full), b_p = smem_u32(&bars.p_full);
-  const uint32_t b_pv = smem_u32(&bars.pv_done), b_dqf = smem_u32(&bars.dq_full), b_dqe = smem_u32(&bars.dq_free);
+  const uint32_t b_kv = smem_u32(&bars.kv_full), b_kvt = smem_u32(&bars.kv_tmem);
+  const uint32_t b_dqf = smem_u32(&bars.dq_full), b_dqe = smem_u32(&bars.dq_free);
+  auto b_s = [&](int h) { return smem_u32(&bars.s_full[h]); };
+  auto b_p = [&](int h) { return smem_u32(&bars.p_full[h]); };
   const uint32_t b_done = smem_u32(&bars.kv_done), b_dr = smem_u32(&bars.drain);
   auto b_qf = [&](int s) { return smem_u32(&bars.q_full[s]); };
   auto b_qe = [&](int s) { return smem_u32(&bars.q_empty[s]); };
@@ -184,9 +200,11 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
       mbar_init(b_qf(s), 33);  // 32 cp.async arrivals + the TMA expect-tx arrival
       mbar_init(b_qe(s), 1);
     }
-    mbar_init(b_s, 1);
-    mbar_init(b_p, 8);
-    mbar_init(b_pv, 1);
+    mbar_init(b_kvt, 8);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(b_s(h), 1);
+      mbar_init(b_p(h), 4);
+    }
     mbar_init(b_dqf, 1);
     mbar_init(b_dqe, 4);
     mbar_init(b_done, 1);
@@ -247,123 +265,150 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
     }
     } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t id_s = idesc_bf16(BN, BM, false, false);   // S^T, dP^T: 128 keys x 128 queries
-      const uint32_t id_kv = idesc_bf16(BN, D, false, true);    // dV, dK: 128 keys x 64
-      const uint32_t id_q = idesc_bf16(BM, D, true, true);      // dQ: 128 queries x 64
-      const uint32_t sK = sb + OFF_K, sV = sb + OFF_V;
-      auto issue_s_dp = [&](int s) {
-        const uint32_t sQ = sb + OFF_Q + s * TILE, sO = sb + OFF_DO + s * TILE;
+    // The whole warp runs this code so every descriptor is warp-uniform; one
+    // elected lane issues the MMAs and the commits that track them.
+    {
+      const bool leader = elect_one();
+      const uint32_t id_s = idesc_bf16(BN, HALF, false, false);  // S_h^T, dP_h^T: 128 keys x 64 queries
+      const uint32_t id_kv = idesc_bf16(BN, D, false, true);     // dV, dK: 128 keys x 64
+      const uint32_t id_q = idesc_bf16(BM, D, true, true);       // dQ: 128 queries x 64
+      const uint64_t d_k = sdesc_sw128(sb + OFF_K, 16, 1024);    // MN-major B of dQ
+      const uint64_t d_q = sdesc_sw128(sb + OFF_Q, 16, 1024);    // stage s: + s * TILE, half h: + h * 8 KB
+      const uint64_t d_o = sdesc_sw128(sb + OFF_DO, 16, 1024);
+      const uint64_t d_dsm = sdesc_sw128(sb + OFF_DS, TILE, 1024);  // MN-major A of dQ (two 64-query blocks)
+      auto issue_s_dp = [&](int h, int s) {
+        const uint64_t q = sdesc_add(d_q, s * TILE + h * HALF * 128), o = sdesc_add(d_o, s * TILE + h * HALF * 128);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          mma_ss(tmem + TM_S, sdesc_sw128(sK + kk * 32, 16, 1024), sdesc_sw128(sQ + kk * 32, 16, 1024), id_s, kk > 0);
-          mma_ss(tmem + TM_DP, sdesc_sw128(sV + kk * 32, 16, 1024), sdesc_sw128(sO + kk * 32, 16, 1024), id_s,
-                 kk > 0);
+          if (leader) {
+            mma_ts(tmem + TM_S + HALF * h, tmem + TM_K + kk * 8, sdesc_add(q, kk * 32), id_s, kk > 0);
+            mma_ts(tmem + TM_DP + HALF * h, tmem + TM_V + kk * 8, sdesc_add(o, kk * 32), id_s, kk > 0);
+          }
         }
       };
-      bool ok = mbar_wait(b_kv, 0, ab) && mbar_wait(b_qf(0), 0, ab);
+      bool ok = __all_sync(0xffffffffu, mbar_wait(b_kvt, 0, ab)) && __all_sync(0xffffffffu, mbar_wait(b_qf(0), 0, ab));
       if (ok) {
         fence_after_sync();
-        issue_s_dp(0);
-        mma_commit(b_s);
+        for (int h = 0; h < 2; ++h) {
+          issue_s_dp(h, 0);
+          if (leader) mma_commit(b_s(h));
+        }
       }
       for (int t = 0; ok && t < nsteps; ++t) {
         const int s = t % NS, db = t & 1;
-        SA_TRACE(1, t, 0);
-        if (!(ok = mbar_wait(b_p, t & 1, ab))) break;
-        SA_TRACE(1, t, 1);
-        fence_after_sync();
-        if (t + 1 < nsteps) {
-          if (!(ok = mbar_wait(b_qf((t + 1) % NS), ((t + 1) / NS) & 1, ab))) break;
+        if (lane == 0) SA_TRACE(1, t, 0);
+        for (int h = 0; h < 2 && ok; ++h) {
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_p(h), t & 1, ab)))) break;
+          if (lane == 0) SA_TRACE(1, t, 1 + 2 * h);
           fence_after_sync();
-          SA_TRACE(1, t, 2);
-          issue_s_dp((t + 1) % NS);
-          mma_commit(b_s);
-        }
-        SA_TRACE(1, t, 3);
-        const uint32_t sQ = sb + OFF_Q + s * TILE, sO = sb + OFF_DO + s * TILE;
-        const uint32_t sdS = sb + OFF_DS + db * 2 * TILE;
+          if (h == 0 && t + 1 < nsteps) {
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_qf((t + 1) % NS), ((t + 1) / NS) & 1, ab)))) break;
+            fence_after_sync();
+          }
+          // dV += P_h^T dO_h and dK += dS_h^T Q_h, A operands in the S^T / dP^T columns of half h.
+          const uint64_t q = sdesc_add(d_q, s * TILE + h * HALF * 128), o = sdesc_add(d_o, s * TILE + h * HALF * 128);
 #pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk) {
-          const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
-          mma_ts(tmem + TM_DV, tmem + TM_P + kk * 8, sdesc_sw128(sO + kk * 2048, 16, 1024), id_kv, acc);
-          mma_ss(tmem + TM_DK, sdesc_sw128(sdS + (kk >> 2) * TILE + (kk & 3) * 32, 16, 1024),
-                 sdesc_sw128(sQ + kk * 2048, 16, 1024), id_kv, acc);
+          for (int kk = 0; kk < HALF / 16; ++kk) {
+            const uint32_t acc = (t > 0 || h > 0 || kk > 0) ? 1u : 0u;
+            if (leader) {
+              mma_ts(tmem + TM_DV, tmem + TM_S + HALF * h + kk * 8, sdesc_add(o, kk * 2048), id_kv, acc);
+              mma_ts(tmem + TM_DK, tmem + TM_DP + HALF * h + kk * 8, sdesc_add(q, kk * 2048), id_kv, acc);
+            }
+          }
+          // The next step's S^T and dP^T of this half overwrite those columns;
+          // the tensor core runs MMAs in issue order.
+          if (t + 1 < nsteps) {
+            issue_s_dp(h, (t + 1) % NS);
+            if (leader) mma_commit(b_s(h));
+          }
+          if (lane == 0) SA_TRACE(1, t, 2 + 2 * h);
         }
-        mma_commit(b_pv);
-        mma_commit(b_qe(s));  // Q(t), dO(t), l'(t), D(t) have no later reader
-        SA_TRACE(1, t, 4);
+        if (!ok) break;
+        if (leader) mma_commit(b_qe(s));  // Q(t), dO(t), l'(t), D(t) have no later reader
         if (t > 0) {
-          if (!(ok = mbar_wait(b_dqe, (t - 1) & 1, ab))) break;
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_dqe, (t - 1) & 1, ab)))) break;
           fence_after_sync();
         }
-        SA_TRACE(1, t, 5);
+        if (lane == 0) SA_TRACE(1, t, 5);
+        const uint64_t dsm = sdesc_add(d_dsm, db * 2 * TILE);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ss(tmem + TM_DQ, sdesc_sw128(sdS + kk * 2048, TILE, 1024), sdesc_sw128(sK + kk * 2048, 16, 1024), id_q,
-                 kk > 0);
-        mma_commit(b_dqf);
+          if (leader) mma_ss(tmem + TM_DQ, sdesc_add(dsm, kk * 2048), sdesc_add(d_k, kk * 2048), id_q, kk > 0);
+        if (leader) mma_commit(b_dqf);
       }
-      if (ok) mma_commit(b_done);
-      mma_commit(b_dr);
+      if (ok && leader) mma_commit(b_done);
+      if (leader) mma_commit(b_dr);
+      __syncwarp();
       wait_drain(b_dr, 0);
     }
     }
   } else if (warp < 12) {
     // ------------------------------------------------------------ element-wise
     regs_inc<REGS_EW>();
-    const int half = (warp - 4) >> 2;  // query columns [64 * half, 64 * half + 64)
+    const int half = (warp - 4) >> 2;  // query rows [64 * half, 64 * half + 64) of each step
     const int kr = (warp & 3) * 32 + lane;
     const int key = k0 + kr;
     const uint32_t lb = lane_base(warp);
-    const uint32_t tS = tmem + TM_S + lb, tDP = tmem + TM_DP + lb, tP = tmem + TM_P + lb;
+    const uint32_t tS = tmem + TM_S + HALF * half + lb, tDP = tmem + TM_DP + HALF * half + lb;
     const float sl2 = p.scale_log2;
-    bool ok = true;
-    for (int t = 0; t < nsteps; ++t) {
+    bool ok = __all_sync(0xffffffffu, mbar_wait(b_kv, 0, ab));
+    if (ok) {
+      // Copy this thread's row of K (first half) or V (second half) into TMEM,
+      // where it is the A operand of S^T = K Q^T / dP^T = V dO^T.
+      const uint32_t src = sb + (half ? OFF_V : OFF_K) + kr * 128;
+      uint32_t r[32];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = ld_shared_v4(src + ((c ^ (kr & 7)) << 4));
+        r[4 * c] = v.x, r[4 * c + 1] = v.y, r[4 * c + 2] = v.z, r[4 * c + 3] = v.w;
+      }
+      tmem_st32(tmem + (half ? TM_V : TM_K) + lb, r);
+      tmem_st_wait();
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_kvt);
+    }
+    for (int t = 0; ok && t < nsteps; ++t) {
       const int s = t % NS;
       if (tid == 128) SA_TRACE(2, t, 0);
-      ok = __all_sync(0xffffffffu, mbar_wait(b_s, t & 1, ab)) &&
+      ok = __all_sync(0xffffffffu, mbar_wait(b_s(half), t & 1, ab)) &&
            __all_sync(0xffffffffu, mbar_wait(b_qf(s), (t / NS) & 1, ab));
       if (!ok) break;
       if (tid == 128) SA_TRACE(2, t, 1);
       fence_after_sync();
-      const int q0 = step_q0(t);
-      const bool full = block_full(q0, BM, k0, BN, sp.len, p.mask);
+      const int qh = step_q0(t) + HALF * half;
+      const bool full = block_full(qh, HALF, k0, BN, sp.len, p.mask);
       const uint32_t rowb = sb + OFF_DS + (t & 1) * 2 * TILE + half * TILE + kr * 128;
-      const uint32_t sL = sb + OFF_L + s * BM * 4, sD = sb + OFF_DL + s * BM * 4;
+      const uint32_t sL = sb + OFF_L + (s * BM + HALF * half) * 4, sD = sb + OFF_DL + (s * BM + HALF * half) * 4;
 #pragma unroll 1
-      for (int cc2 = 0; cc2 < 2; ++cc2) {
-        const int c = 2 * half + cc2;
+      for (int c = 0; c < HALF / 32; ++c) {
         uint32_t pp[16], dd[16];
         if (full)
-          ew_chunk<true>(tS, tDP, sL, sD, c, sl2, q0, key, sp.len, p.mask, pp, dd);
+          ew_chunk<true>(tS + 32 * c, tDP + 32 * c, sL + 128 * c, sD + 128 * c, sl2, qh + 32 * c, key, sp.len, p.mask,
+                         pp, dd);
         else
-          ew_chunk<false>(tS, tDP, sL, sD, c, sl2, q0, key, sp.len, p.mask, pp, dd);
-        if (cc2 == 0 && tid == 128) SA_TRACE(2, t, 2);
-        if (cc2 == 0 && t > 0) {
-          // P^T of the previous step is read by dV(t-1): wait for it before overwriting.
-          if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_pv, (t - 1) & 1, ab)))) break;
-          fence_after_sync();
-        }
-        if (cc2 == 0 && tid == 128) SA_TRACE(2, t, 3);
-        tmem_st16(tP + 16 * c, pp);
+          ew_chunk<false>(tS + 32 * c, tDP + 32 * c, sL + 128 * c, sD + 128 * c, sl2, qh + 32 * c, key, sp.len,
+                          p.mask, pp, dd);
+        // Packed P^T / dS^T of these 32 queries go to the first 16 columns of
+        // this half's S^T / dP^T columns, which this thread has already read.
+        tmem_st16(tS + 16 * c, pp);
+        tmem_st16(tDP + 16 * c, dd);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int cc = cc2 * 4 + i;
+          const int cc = c * 4 + i;
           st_shared_v4(rowb + ((cc ^ (kr & 7)) << 4), dd[4 * i], dd[4 * i + 1], dd[4 * i + 2], dd[4 * i + 3]);
         }
       }
-      if (!ok) break;
       tmem_st_wait();
       fence_before_sync();
       fence_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(b_p);
+      if (lane == 0) mbar_arrive(b_p(half));
       if (tid == 128) SA_TRACE(2, t, 4);
     }
     ok = ok && __all_sync(0xffffffffu, mbar_wait(b_done, 0, ab));
     if (ok) {
-      // First half writes dV, second half writes dK (scaled).
+      // First warpgroup writes dV, second writes dK (scaled).
       fence_after_sync();
       uint32_t a[32], b2[32];
       const uint32_t src = tmem + (half ? TM_DK : TM_DV) + lb;

@@ -175,50 +175,56 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
     }
     } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // Whole warp: descriptors are warp-uniform; one elected lane issues.
+    {
+      const bool leader = elect_one();
       const uint32_t id_s = idesc_bf16(BM, BN, false, false);
       const uint32_t id_o = idesc_bf16(BM, D, false, true);
+      const uint64_t d_q = sdesc_sw128(sb + OFF_Q, 16, 1024);  // head i: + i * TILE
+      const uint64_t d_k = sdesc_sw128(sb + OFF_K, 16, 1024);  // stage s: + s * TILE
+      const uint64_t d_v = sdesc_sw128(sb + OFF_V, 16, 1024);
       auto issue_s = [&](int i, int s) {
-        const uint32_t qa = sb + OFF_Q + i * TILE, kb = sb + OFF_K + s * TILE;
+        const uint64_t qa = sdesc_add(d_q, i * TILE), kb = sdesc_add(d_k, s * TILE);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + TM_S + 128 * i, sdesc_sw128(qa + kk * 32, 16, 1024), sdesc_sw128(kb + kk * 32, 16, 1024),
-                 id_s, kk > 0);
+          if (leader) mma_ss(tmem + TM_S + 128 * i, sdesc_add(qa, kk * 32), sdesc_add(kb, kk * 32), id_s, kk > 0);
       };
       auto issue_pv = [&](int i, int s, bool first) {
-        const uint32_t vb = sb + OFF_V + s * TILE;
+        const uint64_t vb = sdesc_add(d_v, s * TILE);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tmem + TM_O + 64 * i, tmem + TM_P + 64 * i + kk * 8, sdesc_sw128(vb + kk * 2048, 16, 1024), id_o,
-                 (!first || kk > 0) ? 1u : 0u);
+          if (leader)
+            mma_ts(tmem + TM_O + 64 * i, tmem + TM_P + 64 * i + kk * 8, sdesc_add(vb, kk * 2048), id_o,
+                   (!first || kk > 0) ? 1u : 0u);
       };
-      bool ok = mbar_wait(b_q, 0, ab) && mbar_wait(b_k(0), 0, ab);
+      bool ok = __all_sync(0xffffffffu, mbar_wait(b_q, 0, ab)) && __all_sync(0xffffffffu, mbar_wait(b_k(0), 0, ab));
       if (ok) {
         fence_after_sync();
         for (int i = 0; i < nh; ++i) {
           issue_s(i, 0);
-          mma_commit(b_s(i));
+          if (leader) mma_commit(b_s(i));
         }
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int s = j % NS;
-        if (!(ok = mbar_wait(b_v(s), (j / NS) & 1, ab))) break;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_v(s), (j / NS) & 1, ab)))) break;
         for (int i = 0; i < nh && ok; ++i) {
-          if (!(ok = mbar_wait(b_p(i), j & 1, ab))) break;
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_p(i), j & 1, ab)))) break;
           fence_after_sync();
           issue_pv(i, s, j == 0);
           if (j + 1 < n_tiles) {
             const int s2 = (j + 1) % NS;
-            if (i == 0 && !(ok = mbar_wait(b_k(s2), ((j + 1) / NS) & 1, ab))) break;
+            if (i == 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(b_k(s2), ((j + 1) / NS) & 1, ab)))) break;
             fence_after_sync();
             issue_s(i, s2);
-            mma_commit(b_s(i));
+            if (leader) mma_commit(b_s(i));
           }
         }
-        if (ok) mma_commit(b_e(s));
+        if (ok && leader) mma_commit(b_e(s));
       }
-      if (ok) mma_commit(b_of);
-      mma_commit(b_dr);
+      if (ok && leader) mma_commit(b_of);
+      if (leader) mma_commit(b_dr);
+      __syncwarp();
       wait_drain(b_dr, 0);
     }
     }

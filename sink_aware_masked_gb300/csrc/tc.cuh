@@ -147,6 +147,18 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Advance a shared-memory descriptor's start address by `bytes` (multiple of
+// 16; the start field holds address >> 4 and shared addresses stay below
+// 256 KB, so the add never carries out of the field).
+__host__ __device__ constexpr uint64_t sdesc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
+// One elected lane of a converged warp (the lowest active lane).
+SA_DEV bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n" : "=r"(pred));
+  return pred != 0;
+}
+
 // ------------------------------------------------------------------ MMA
 // D[tmem] (+)= A[smem desc] * B[smem desc]^T ; accumulate when acc != 0.
 SA_DEV void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t acc) {
