@@ -125,6 +125,53 @@ SA_DEV float ex2(float x) {
   return y;
 }
 
+// 2^x on the FMA pipe (frees the MUFU unit for the other exponentials).
+// x = j + f with j = round(x) taken from the low mantissa bits of x + 1.5*2^23
+// and f in [-0.5, 0.5]; 2^f is a degree-3 polynomial fitted for relative
+// error 7.5e-5 on that interval (fit_exp2_poly.py); 2^j is added to the
+// exponent field.  x is clamped to >= -125 so the result stays a normal
+// number (masked scores, x = -inf, give 2^-125, which is zero to every
+// bf16/fp32 sum they enter).  Valid for x <= 127.
+SA_DEV float exp2_fma(float x) {
+  x = fmaxf(x, -125.f);
+  const float t = x + 12582912.f;
+  const float j = t - 12582912.f;
+  const float f = x - j;
+  const float p = fmaf(fmaf(fmaf(0.0551716648f, f, 0.242611125f), f, 0.693260968f), f, 0.999928057f);
+  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+}
+
+// Three-input maximum (sm_100 family).
+SA_DEV float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;\n" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Packed pairs of fp32 (sm_100 family f32x2 instructions).
+SA_DEV float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;\n"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)),
+        "l"(*reinterpret_cast<uint64_t*>(&c)));
+  return *reinterpret_cast<float2*>(&d);
+}
+SA_DEV float2 fadd2(float2 a, float2 b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;\n"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
+  return *reinterpret_cast<float2*>(&d);
+}
+SA_DEV float2 fmul2(float2 a, float2 b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;\n"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
+  return *reinterpret_cast<float2*>(&d);
+}
+
 // Offset in bytes of 16-byte chunk `c` (0..7) of row `r` in a tile whose rows
 // are 64 bf16 (128 bytes): chunks are XOR-swizzled by the row's low 3 bits so
 // that ldmatrix reads of 8 rows at one chunk column hit 8 different banks.

@@ -8,7 +8,8 @@
 //               128 keys through an NS-stage ring (separate K and V barriers
 //               so S = QK^T can start before V lands).
 //   warp 1      MMA issuer (one thread) and TMEM owner:
-//               S_i = Q_i K_j^T   (M=128, N=128, K=64; A, B K-major in smem)
+//               S_i = Q_i K_j^T   (M=128, N=128, K=64; A = Q_i in TMEM,
+//                                   B = K_j K-major in smem)
 //               O_i += P_i V_j    (M=128, N=64,  K=128; A = P_i in TMEM,
 //                                   B = V_j MN-major in smem)
 //               issued ping-pong between the two heads so the tensor core
@@ -21,8 +22,13 @@
 //               no shuffles.  Online softmax in log2 units; the O rescale is
 //               skipped unless the running max grows by more than 8 (P stays
 //               below 2^8, exact in fp32 sums); P is written to TMEM as
-//               packed bf16.
-// Tensor Memory (512 columns): S0 | S1 (128 each) | O0 | O1 (64 each) | P0 | P1 (64 each).
+//               packed bf16.  One exponential in four runs on the FMA pipe
+//               (exp2_fma) to offload the MUFU unit; the row maximum uses independent
+//               three-input max chains; scale/subtract and row
+//               sums use packed f32x2 arithmetic.  At start each softmax
+//               warpgroup copies its head's Q tile into TMEM.
+// Tensor Memory (448 of 512 columns): S0 | S1 (128 each; P_i overwrites the
+// first 64 columns of S_i) | O0 | O1 (64 each) | Q0 | Q1 (32 each, A operands).
 //
 // Epilogue (SinkFlex-RL summary page: auxiliary log-sum-exp and the sink
 // scaling function; section 5: zero-value sink equivalence):
@@ -37,6 +43,21 @@
 #include "internal.h"
 #include "tc.cuh"
 #include "tmap.h"
+
+// Optional timeline instrumentation for performance work: compiled in only
+// when SA_FWD_TRACE is defined (never in the library build).
+#ifdef SA_FWD_TRACE
+__device__ long long* g_fwd_trace;
+#define SA_TRACE(role, step, ev)                                                                        \
+  do {                                                                                                 \
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && g_fwd_trace != nullptr && (step) < 256) \
+      g_fwd_trace[((role) * 256 + (step)) * 8 + (ev)] = clock64();                                     \
+  } while (0)
+#else
+#define SA_TRACE(role, step, ev) \
+  do {                           \
+  } while (0)
+#endif
 
 namespace sa {
 namespace {
@@ -56,7 +77,9 @@ constexpr int OFF_K = OFF_Q + 2 * TILE;
 constexpr int OFF_V = OFF_K + NS * TILE;
 constexpr int SMEM_DYN = OFF_V + NS * TILE + 1024;  // + alignment slack
 
-constexpr uint32_t TM_S = 0, TM_O = 256, TM_P = 384;  // + 128*i, 64*i, 64*i
+// S_i at 128 i (P_i, packed bf16, overwrites its first 64 columns), O_i at
+// 256 + 64 i, Q_i (packed bf16, A operand of S_i) at 384 + 32 i.
+constexpr uint32_t TM_S = 0, TM_O = 256, TM_Q = 384;
 
 struct FwdTcK {
   CUtensorMap tm_q, tm_k, tm_v;
@@ -76,7 +99,7 @@ struct FwdTcK {
 struct Bars {
   uint64_t q_full;
   uint64_t k_full[NS], v_full[NS], kv_empty[NS];
-  uint64_t s_full[2], p_full[2];
+  uint64_t s_full[2], p_full[2], q_tmem[2];
   uint64_t o_final, drain;
 };
 
@@ -118,6 +141,7 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
   auto b_e = [&](int s) { return smem_u32(&bars.kv_empty[s]); };
   auto b_s = [&](int i) { return smem_u32(&bars.s_full[i]); };
   auto b_p = [&](int i) { return smem_u32(&bars.p_full[i]); };
+  auto b_qt = [&](int i) { return smem_u32(&bars.q_tmem[i]); };
 
   if (tid == 0) {
     abort_flag = 0;
@@ -130,6 +154,7 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_s(i), 1);
       mbar_init(b_p(i), 4);
+      mbar_init(b_qt(i), 4);
     }
     mbar_init(b_of, 1);
     mbar_init(b_dr, 1);
@@ -180,36 +205,36 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
       const bool leader = elect_one();
       const uint32_t id_s = idesc_bf16(BM, BN, false, false);
       const uint32_t id_o = idesc_bf16(BM, D, false, true);
-      const uint64_t d_q = sdesc_sw128(sb + OFF_Q, 16, 1024);  // head i: + i * TILE
       const uint64_t d_k = sdesc_sw128(sb + OFF_K, 16, 1024);  // stage s: + s * TILE
       const uint64_t d_v = sdesc_sw128(sb + OFF_V, 16, 1024);
       auto issue_s = [&](int i, int s) {
-        const uint64_t qa = sdesc_add(d_q, i * TILE), kb = sdesc_add(d_k, s * TILE);
+        const uint64_t kb = sdesc_add(d_k, s * TILE);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          if (leader) mma_ss(tmem + TM_S + 128 * i, sdesc_add(qa, kk * 32), sdesc_add(kb, kk * 32), id_s, kk > 0);
+          if (leader) mma_ts(tmem + TM_S + 128 * i, tmem + TM_Q + 32 * i + kk * 8, sdesc_add(kb, kk * 32), id_s, kk > 0);
       };
       auto issue_pv = [&](int i, int s, bool first) {
         const uint64_t vb = sdesc_add(d_v, s * TILE);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           if (leader)
-            mma_ts(tmem + TM_O + 64 * i, tmem + TM_P + 64 * i + kk * 8, sdesc_add(vb, kk * 2048), id_o,
+            mma_ts(tmem + TM_O + 64 * i, tmem + TM_S + 128 * i + kk * 8, sdesc_add(vb, kk * 2048), id_o,
                    (!first || kk > 0) ? 1u : 0u);
       };
-      bool ok = __all_sync(0xffffffffu, mbar_wait(b_q, 0, ab)) && __all_sync(0xffffffffu, mbar_wait(b_k(0), 0, ab));
-      if (ok) {
+      bool ok = __all_sync(0xffffffffu, mbar_wait(b_k(0), 0, ab));
+      for (int i = 0; i < nh && ok; ++i) {
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_qt(i), 0, ab)))) break;
         fence_after_sync();
-        for (int i = 0; i < nh; ++i) {
-          issue_s(i, 0);
-          if (leader) mma_commit(b_s(i));
-        }
+        issue_s(i, 0);
+        if (leader) mma_commit(b_s(i));
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int s = j % NS;
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_v(s), (j / NS) & 1, ab)))) break;
         for (int i = 0; i < nh && ok; ++i) {
+          if (lane == 0) SA_TRACE(0, j, 2 * i);
           if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_p(i), j & 1, ab)))) break;
+          if (lane == 0) SA_TRACE(0, j, 2 * i + 1);
           fence_after_sync();
           issue_pv(i, s, j == 0);
           if (j + 1 < n_tiles) {
@@ -219,6 +244,7 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
             issue_s(i, s2);
             if (leader) mma_commit(b_s(i));
           }
+          if (lane == 0) SA_TRACE(0, j, 4 + i);
         }
         if (ok && leader) mma_commit(b_e(s));
       }
@@ -237,13 +263,33 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
     const int row = (warp & 3) * 32 + lane;
     const int q = q0 + row;
     const uint32_t lb = lane_base(warp);
-    const uint32_t tS = tmem + TM_S + 128 * i + lb, tO = tmem + TM_O + 64 * i + lb, tP = tmem + TM_P + 64 * i + lb;
+    const uint32_t tS = tmem + TM_S + 128 * i + lb, tO = tmem + TM_O + 64 * i + lb;
     const float sl2 = p.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
+    bool ok = __all_sync(0xffffffffu, mbar_wait(b_q, 0, ab));
+    if (ok) {
+      // Copy this thread's query row into TMEM: the A operand of S_i = Q_i K^T.
+      const uint32_t src = sb + OFF_Q + i * TILE + row * 128;
+      uint32_t r[32];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint4 v;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "r"(src + ((c ^ (row & 7)) << 4)));
+        r[4 * c] = v.x, r[4 * c + 1] = v.y, r[4 * c + 2] = v.z, r[4 * c + 3] = v.w;
+      }
+      tmem_st32(tmem + TM_Q + 32 * i + lb, r);
+      tmem_st_wait();
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_qt(i));
+    }
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      if ((warp & 3) == 0 && lane == 0) SA_TRACE(1 + i, j, 0);
       ok = __all_sync(0xffffffffu, mbar_wait(b_s(i), j & 1, ab));
       if (!ok) break;
+      if ((warp & 3) == 0 && lane == 0) SA_TRACE(1 + i, j, 1);
       fence_after_sync();
       uint32_t r[4][32];
 #pragma unroll
@@ -253,17 +299,21 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
       for (int c = 0; c < 4; ++c) reg_fence32(r[c]);
 #define S_(c) r[(c) >> 5][(c) & 31]
       const int k0 = tile_k0(j);
-      float mx = -INFINITY;
-      if (block_full(q0, BM, k0, BN, sp.len, p.mask)) {
+      if (!block_full(q0, BM, k0, BN, sp.len, p.mask)) {
 #pragma unroll
-        for (int c = 0; c < BN; ++c) mx = fmaxf(mx, __uint_as_float(S_(c)));
-      } else {
-#pragma unroll
-        for (int c = 0; c < BN; ++c) {
+        for (int c = 0; c < BN; ++c)
           if (!visible(q, k0 + c, sp.len, p.mask)) S_(c) = __float_as_uint(-INFINITY);
-          mx = fmaxf(mx, __uint_as_float(S_(c)));
-        }
       }
+      // Row maximum as 8 independent three-input chains (no 128-long dependency).
+      float pm[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) pm[k] = fmaxf(__uint_as_float(S_(2 * k)), __uint_as_float(S_(2 * k + 1)));
+#pragma unroll
+      for (int c = 16; c < BN; c += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          pm[k] = fmax3(pm[k], __uint_as_float(S_(c + 2 * k)), __uint_as_float(S_(c + 2 * k + 1)));
+      const float mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
       const float m_new = fmaxf(m_ref, mx * sl2);
       const bool resc = (m_ref != -INFINITY) && (m_new > m_ref + 8.f);
       float factor = 1.f;
@@ -290,26 +340,41 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
         tmem_st32(tO, o[0]);
         tmem_st32(tO + 32, o[1]);
       }
+      if ((warp & 3) == 0 && lane == 0) SA_TRACE(1 + i, j, 2);
       const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
-      float ls = 0.f;
+      const float2 sl2x2 = make_float2(sl2, sl2), negx2 = make_float2(neg, neg);
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          const float a = ex2(fmaf(__uint_as_float(S_(64 * hh + 2 * c)), sl2, neg));
-          const float bb = ex2(fmaf(__uint_as_float(S_(64 * hh + 2 * c + 1)), sl2, neg));
-          ls += a + bb;
-          pk[c] = pack_bf16(a, bb);
+          const float2 x = ffma2(make_float2(__uint_as_float(S_(64 * hh + 2 * c)), __uint_as_float(S_(64 * hh + 2 * c + 1))),
+                                 sl2x2, negx2);
+          float2 e;
+          if ((c & 3) == 3) {
+            e.x = exp2_fma(x.x);
+            e.y = exp2_fma(x.y);
+          } else {
+            e.x = ex2(x.x);
+            e.y = ex2(x.y);
+          }
+          acc[c & 3] = fadd2(acc[c & 3], e);
+          pk[c] = pack_bf16(e.x, e.y);
         }
-        tmem_st32(tP + 32 * hh, pk);
+        // P overwrites the first 64 columns of S_i; the whole S row is
+        // already in registers.
+        tmem_st32(tS + 32 * hh, pk);
       }
 #undef S_
-      l += ls;
+      const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
+      const float2 at = fadd2(a01, a23);
+      l += at.x + at.y;
       tmem_st_wait();
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_p(i));
+      if ((warp & 3) == 0 && lane == 0) SA_TRACE(1 + i, j, 3);
     }
     ok = ok && __all_sync(0xffffffffu, mbar_wait(b_of, 0, ab));
     if (ok) {
