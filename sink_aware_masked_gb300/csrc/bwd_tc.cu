@@ -45,6 +45,8 @@
 #include "tc.cuh"
 #include "tmap.h"
 
+#include <algorithm>
+
 // Optional timeline instrumentation for performance work: compiled in only
 // when SA_BWD_TRACE is defined (never in the library build).
 #ifdef SA_BWD_TRACE
@@ -101,7 +103,26 @@ struct BwdTcK {
   int hq, hkv, group;
   MaskParams mask;
   float scale, scale_log2;
+  // Query-range splitting of key tiles that hold always-visible prefix keys
+  // (only with a finite window, where those tiles would otherwise visit every
+  // query tile while their neighbours visit a few): such a tile's query tiles
+  // are cut into chunks of `qchunk`, one CTA each, whose partial dK/dV are
+  // added into the fp32 accumulator dkv_acc ([num_seqs][pre_tiles * 128][Hkv]
+  // [2][64]: dV then unscaled dK).  blockIdx.z >= n_kt indexes the extra chunks.
+  int n_kt, pre_tiles, qchunk;
+  float* dkv_acc;
 };
+
+// Number of query-tile chunks of key tile kt in a sequence of length len.
+SA_DEV int tile_chunks(int kt, int len, const MaskParams& m, int pre_tiles, int qchunk) {
+  if (kt >= pre_tiles || m.window < 0) return 1;
+  const int k0 = kt * BN;
+  if (k0 >= len) return 0;
+  int qlo, qhi;
+  query_range(k0, min(k0 + BN, len) - 1, len, m, qlo, qhi);
+  const int nq = qhi / BM - qlo / BM + 1;
+  return (nq + qchunk - 1) / qchunk;
+}
 
 struct Bars {
   uint64_t kv_full, kv_tmem;
@@ -121,6 +142,12 @@ SA_DEV uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
   return v;
+}
+
+// Vector fp32 atomic add (no return value).
+SA_DEV void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
 }
 
 SA_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -173,12 +200,31 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x;
   const SeqSpan sp = seq_span(p.cu, p.seqlen, blockIdx.y);
-  const int k0 = static_cast<int>(blockIdx.z) * BN;
+  int kt = static_cast<int>(blockIdx.z), chunk = 0;
+  if (kt >= p.n_kt) {
+    // An extra chunk of a prefix key tile: find which one.
+    int e = kt - p.n_kt;
+    kt = 0;
+    while (kt < p.pre_tiles) {
+      const int extra = max(0, tile_chunks(kt, sp.len, p.mask, p.pre_tiles, p.qchunk) - 1);
+      if (e < extra) break;
+      e -= extra;
+      ++kt;
+    }
+    if (kt >= p.pre_tiles) return;
+    chunk = e + 1;
+  }
+  const int k0 = kt * BN;
   if (k0 >= sp.len) return;
   const int k1 = min(k0 + BN, sp.len) - 1;
+  const bool split = tile_chunks(kt, sp.len, p.mask, p.pre_tiles, p.qchunk) > 1;
   int qlo, qhi;
   query_range(k0, k1, sp.len, p.mask, qlo, qhi);
-  const int qt_lo = qlo / BM, nq = qhi / BM - qt_lo + 1;
+  int qt_lo = qlo / BM, nq = qhi / BM - qt_lo + 1;
+  if (split) {
+    qt_lo += chunk * p.qchunk;
+    nq = min(p.qchunk, nq - chunk * p.qchunk);
+  }
   const int nsteps = p.group * nq;
   auto step_head = [&](int t) { return g * p.group + t / nq; };
   auto step_q0 = [&](int t) { return (qt_lo + t % nq) * BM; };
@@ -418,7 +464,19 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
       reg_fence32(a);
       reg_fence32(b2);
       const float mul = half ? p.scale : 1.f;
-      if (key < sp.len) {
+      if (key < sp.len && split) {
+        // Partial sums of a split tile: add into the fp32 accumulator.
+        float* dst = p.dkv_acc + ((static_cast<size_t>(blockIdx.y) * p.pre_tiles * BN + key) * p.hkv + g) * 2 * D +
+                     half * D;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          red_add_v4(dst + 4 * c, __uint_as_float(a[4 * c]), __uint_as_float(a[4 * c + 1]),
+                     __uint_as_float(a[4 * c + 2]), __uint_as_float(a[4 * c + 3]));
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          red_add_v4(dst + 32 + 4 * c, __uint_as_float(b2[4 * c]), __uint_as_float(b2[4 * c + 1]),
+                     __uint_as_float(b2[4 * c + 2]), __uint_as_float(b2[4 * c + 3]));
+      } else if (key < sp.len) {
         __nv_bfloat16* dst = (half ? p.dk : p.dv) + (static_cast<size_t>(sp.start + key) * p.hkv + g) * D;
         uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
@@ -491,7 +549,77 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
   }
 }
 
+// dK, dV of split prefix tiles: fp32 accumulator -> bf16 (dK scaled).
+struct DkvConvK {
+  const float* acc;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  const int32_t* cu;
+  int seqlen, num_seqs, rows, hkv;  // rows = pre_tiles * 128
+  float scale;
+  MaskParams mask;
+  int pre_tiles, qchunk;
+};
+
+__global__ void __launch_bounds__(256) dkv_convert_kernel(const DkvConvK p) {
+  const long long total = static_cast<long long>(p.num_seqs) * p.rows * p.hkv * 2 * (D / 8);
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int c8 = static_cast<int>(i % (D / 8));
+    long long r = i / (D / 8);
+    const int which = static_cast<int>(r % 2);  // 0: dV, 1: dK
+    r /= 2;
+    const int g = static_cast<int>(r % p.hkv);
+    r /= p.hkv;
+    const int key = static_cast<int>(r % p.rows);
+    const int b = static_cast<int>(r / p.rows);
+    const SeqSpan sp = seq_span(p.cu, p.seqlen, b);
+    if (key >= sp.len) continue;
+    // Only tiles that were split accumulate here; the others wrote bf16 directly.
+    if (tile_chunks(key / BN, sp.len, p.mask, p.pre_tiles, p.qchunk) <= 1) continue;
+    const float* src = p.acc + (((static_cast<size_t>(b) * p.rows + key) * p.hkv + g) * 2 + which) * D + 8 * c8;
+    const float mul = which ? p.scale : 1.f;
+    const float4 x = reinterpret_cast<const float4*>(src)[0], y = reinterpret_cast<const float4*>(src)[1];
+    uint4 o;
+    o.x = pack_bf16(x.x * mul, x.y * mul);
+    o.y = pack_bf16(x.z * mul, x.w * mul);
+    o.z = pack_bf16(y.x * mul, y.y * mul);
+    o.w = pack_bf16(y.z * mul, y.w * mul);
+    __nv_bfloat16* dst = (which ? p.dk : p.dv) + (static_cast<size_t>(sp.start + key) * p.hkv + g) * D + 8 * c8;
+    *reinterpret_cast<uint4*>(dst) = o;
+  }
+}
+
 }  // namespace
+
+// Host view of the prefix-tile split (same rule as tile_chunks on the device).
+void bwd_split_plan(const Problem& pr, int& pre_tiles, int& qchunk, int& n_extra) {
+  pre_tiles = 0;
+  qchunk = 1;
+  n_extra = 0;
+  if (pr.window < 0 || pr.prefix <= 0 || pr.seqlen == 0) return;
+  pre_tiles = ceil_div(pr.prefix, BN);
+  // Chunk so a split CTA has about as many query tiles as a window-only tile.
+  qchunk = max(2, ceil_div(static_cast<long long>(pr.window) + BN, BM) + 1);
+  const int len = pr.seqlen;
+  for (int kt = 0; kt < pre_tiles; ++kt) {
+    const int k0 = kt * BN;
+    if (k0 >= len) break;
+    const int k1 = std::min(k0 + BN, len) - 1;
+    const int qlo = pr.causal ? k0 : 0;
+    const int qhi = len - 1;  // a prefix key is visible to every later query
+    (void)k1;
+    const int nq = qhi / BM - qlo / BM + 1;
+    n_extra += std::max(0, ceil_div(nq, qchunk) - 1);
+  }
+}
+
+size_t bwd_split_acc_bytes(const Problem& pr) {
+  int pre, qc, ne;
+  bwd_split_plan(pr, pre, qc, ne);
+  if (pre == 0) return 0;
+  return static_cast<size_t>(pr.num_seqs) * pre * BN * pr.hkv * 2 * D * sizeof(float);
+}
 
 cudaError_t launch_bwd_tc_main(const Problem& pr, const BwdArgs& a, int* status, cudaStream_t stream) {
   const int n_kt = ceil_div(pr.seqlen, BN);
@@ -517,13 +645,32 @@ cudaError_t launch_bwd_tc_main(const Problem& pr, const BwdArgs& a, int* status,
   k.mask = MaskParams{pr.window, pr.prefix, pr.causal};
   k.scale = pr.scale;
   k.scale_log2 = pr.scale * kLog2e;
-  cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_DYN);
-  if (e != cudaSuccess) return e;
-  dim3 grid(pr.hkv, pr.num_seqs, n_kt);
+  int n_extra = 0;
+  bwd_split_plan(pr, k.pre_tiles, k.qchunk, n_extra);
+  k.n_kt = n_kt;
+  k.dkv_acc = a.dkv_acc;
+  cudaError_t e;
+  const bool any_split = n_extra > 0;
+  if (any_split) {
+    if (a.dkv_acc == nullptr) return cudaErrorInvalidValue;
+    if ((e = cudaMemsetAsync(a.dkv_acc, 0, bwd_split_acc_bytes(pr), stream)) != cudaSuccess) return e;
+  }
+  if ((e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_DYN)) !=
+      cudaSuccess)
+    return e;
+  dim3 grid(pr.hkv, pr.num_seqs, n_kt + n_extra);
   if ((e = prof_begin(g_prof_bwd, stream)) != cudaSuccess) return e;
   bwd_tc_kernel<<<grid, NTHR, SMEM_DYN, stream>>>(k);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  return prof_end(g_prof_bwd, stream);
+  if ((e = prof_end(g_prof_bwd, stream)) != cudaSuccess) return e;
+  if (any_split) {
+    DkvConvK c{a.dkv_acc, static_cast<__nv_bfloat16*>(a.dk), static_cast<__nv_bfloat16*>(a.dv), pr.cu, pr.seqlen,
+               pr.num_seqs, k.pre_tiles * BN, pr.hkv, pr.scale, k.mask, k.pre_tiles, k.qchunk};
+    const long long total = static_cast<long long>(pr.num_seqs) * c.rows * pr.hkv * 2 * (D / 8);
+    dkv_convert_kernel<<<static_cast<int>(std::min<long long>((total + 255) / 256, 152 * 8)), 256, 0, stream>>>(c);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace sa

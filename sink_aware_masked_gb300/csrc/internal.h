@@ -49,6 +49,7 @@ struct BwdArgs {
   float* delta;       // [Hq, T]  D = <dO, O>
   float* lse_log2;    // [Hq, T]  (l + softplus(sink - l)) * log2(e)
   float* dsink_part;  // [preprocess blocks, Hq]
+  float* dkv_acc;     // fp32 dK/dV partial sums of split prefix key tiles (or nullptr)
   int preprocess_blocks;
 };
 
@@ -73,6 +74,7 @@ inline cudaError_t prof_end(const ProfileEvents& e, cudaStream_t s) {
 cudaError_t launch_fwd_tc(const Problem& p, const FwdArgs& a, int* status, cudaStream_t s);
 cudaError_t launch_bwd(const Problem& p, const BwdArgs& a, int* status, cudaStream_t s);
 cudaError_t launch_bwd_tc_main(const Problem& p, const BwdArgs& a, int* status, cudaStream_t s);
+size_t bwd_split_acc_bytes(const Problem& p);
 cudaError_t launch_varlen_plan(const int32_t* seqlens, int n, int32_t* cu, cudaStream_t s);
 cudaError_t launch_pack(const void* src, const int32_t* cu, int B, int Smax, int H, int D, void* dst, bool unpack,
                         cudaStream_t s);

@@ -85,7 +85,7 @@ sinkattn_status normalise(const sinkattn_problem* pr, sa::Problem& out) {
 }
 
 struct BwdLayout {
-  size_t dq_accum, delta, lse_log2, part, total;
+  size_t dq_accum, delta, lse_log2, part, dkv, total;
   int pre_blocks;
 };
 
@@ -97,7 +97,8 @@ BwdLayout bwd_layout(const sa::Problem& p) {
   l.delta = l.dq_accum + round_up(T * H * sa::kHeadDim * 4, 256);
   l.lse_log2 = l.delta + round_up(T * H * 4, 256);
   l.part = l.lse_log2 + round_up(T * H * 4, 256);
-  l.total = l.part + round_up(static_cast<size_t>(l.pre_blocks) * H * 4, 256) + 256;
+  l.dkv = l.part + round_up(static_cast<size_t>(l.pre_blocks) * H * 4, 256);
+  l.total = l.dkv + round_up(sa::bwd_split_acc_bytes(p), 256) + 256;
   return l;
 }
 
@@ -172,6 +173,7 @@ sinkattn_status sinkattn_bwd(const sinkattn_problem* prob, const void* q, const 
   a.delta = reinterpret_cast<float*>(ws + L.delta);
   a.lse_log2 = reinterpret_cast<float*>(ws + L.lse_log2);
   a.dsink_part = reinterpret_cast<float*>(ws + L.part);
+  a.dkv_acc = sa::bwd_split_acc_bytes(p) ? reinterpret_cast<float*>(ws + L.dkv) : nullptr;
   a.preprocess_blocks = L.pre_blocks;
   int* status = status_word();
   if (status == nullptr) return SINKATTN_ERR_CUDA;

@@ -79,6 +79,10 @@ SMALL = [
     W.custom((640,), 2, 1, window=127, seed=21, name="s640_w127"),
     W.custom((640,), 2, 1, window=129, prefix=1, seed=22, name="s640_w129_p1"),
     W.custom((777, 1025), 4, 2, seed=23, sink_dist="uniform2", name="varlen2_ragged"),
+    # long prefix with a short window: prefix key tiles are split over several CTAs
+    W.custom((1000,), 4, 2, window=10, prefix=150, seed=24, name="s1000_w10_p150_split"),
+    W.custom((700, 1300, 5), 4, 1, window=64, prefix=40, seed=25, name="varlen_w64_p40_split"),
+    W.custom((900,), 4, 2, window=20, prefix=3, causal=False, seed=26, name="s900_noncausal_w20_p3_split"),
 ]
 
 
