@@ -1,0 +1,176 @@
+// Backward helper kernels of sink-aware attention (the main kernel is
+// bwd_tc.cu).
+//
+// Math (explicit sink column with zero value; SinkFlex-RL section 5 and the
+// summary page's alpha = sigmoid(l - s_h); per-head sink gradient from the
+// "GPT-OSS agentic RL training" page):
+//   l'  = l + softplus(s_h - l)        log-normaliser including the sink
+//   D   = <dO, O>                      O is the final, alpha-scaled output
+//   dsink[h] = -sum_rows (1 - alpha) D,   1 - alpha = sigmoid(s_h - l)
+//
+//   bwd_pre   : one pass over O and dO: D, l' (log2 units), per-block partial
+//               dsink sums, zeroes the fp32 dQ accumulator.  HBM-bound; many
+//               small blocks and two tokens' loads in flight per iteration
+//               keep enough bytes in flight.
+//   dq_convert: dQ = scale * accumulator -> bf16; ceil(Hq / 8) extra blocks
+//               reduce the dsink partials in a fixed order (deterministic),
+//               one warp per head.
+#include "common.cuh"
+#include "internal.h"
+
+namespace sa {
+namespace {
+
+constexpr int D = kHeadDim;
+
+// ------------------------------------------------------------------ preprocess
+struct PreK {
+  const __nv_bfloat16* o;
+  const __nv_bfloat16* dout;
+  const float* lse;
+  const float* sink;
+  float* delta;
+  float* lse_log2;
+  float* dq_accum;
+  float* dsink_part;
+  long long T;
+  int hq;
+};
+
+__device__ __forceinline__ float dot8_bf16(const uint4& a, const uint4& b) {
+  const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(&a);
+  const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(&b);
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 fx = __bfloat1622float2(x[i]);
+    const float2 fy = __bfloat1622float2(y[i]);
+    s = fmaf(fx.x, fy.x, s);
+    s = fmaf(fx.y, fy.y, s);
+  }
+  return s;
+}
+
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const PreK p) {
+  const int sub = threadIdx.x & 7;   // 16-byte chunk of a 128-byte row
+  const int hs = threadIdx.x >> 3;   // 0..31
+  const long long t0 = static_cast<long long>(blockIdx.x) * kPreTokens;
+  const long long t1 = min(t0 + kPreTokens, p.T);
+  float acc[kMaxHeadsQ / 32];
+#pragma unroll
+  for (int i = 0; i < kMaxHeadsQ / 32; ++i) acc[i] = 0.f;
+#pragma unroll 2
+  for (long long t = t0; t < t1; ++t) {
+#pragma unroll
+    for (int hi = 0; hi < kMaxHeadsQ / 32; ++hi) {
+      if (hi * 32 >= p.hq) break;
+      const int h = hi * 32 + hs;
+      const bool ok = h < p.hq;
+      float dot = 0.f;
+      if (ok) {
+        const size_t base = (static_cast<size_t>(t) * p.hq + h) * D + sub * 8;
+        const uint4 ov = __ldg(reinterpret_cast<const uint4*>(p.o + base));
+        const uint4 gv = __ldg(reinterpret_cast<const uint4*>(p.dout + base));
+        dot = dot8_bf16(ov, gv);
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        reinterpret_cast<float4*>(p.dq_accum + base)[0] = z;
+        reinterpret_cast<float4*>(p.dq_accum + base)[1] = z;
+      }
+      dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+      dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+      dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+      if (ok && sub == 0) {
+        const size_t idx = static_cast<size_t>(h) * p.T + t;
+        const float l = p.lse[idx];
+        const float x = __ldg(p.sink + h) - l;
+        const float softplus = fmaxf(x, 0.f) + log1pf(__expf(-fabsf(x)));
+        p.lse_log2[idx] = (l + softplus) * kLog2e;
+        p.delta[idx] = dot;
+        const float one_minus_alpha = 1.f / (1.f + __expf(-x));
+        acc[hi] -= one_minus_alpha * dot;
+      }
+    }
+  }
+  if (sub == 0) {
+#pragma unroll
+    for (int hi = 0; hi < kMaxHeadsQ / 32; ++hi) {
+      const int h = hi * 32 + hs;
+      if (h < p.hq) p.dsink_part[static_cast<size_t>(blockIdx.x) * p.hq + h] = acc[hi];
+    }
+  }
+}
+
+// ------------------------------------------------------------------ convert
+struct ConvK {
+  const float* acc;
+  __nv_bfloat16* dq;
+  long long n8;  // number of 8-element groups
+  float scale;
+  const float* part;
+  int nparts;
+  int hq;
+  float* dsink;
+};
+
+__global__ void __launch_bounds__(256) dq_convert_kernel(const ConvK p) {
+  const int nred = (p.hq + 7) / 8;
+  const int conv_blocks = static_cast<int>(gridDim.x) - nred;
+  if (static_cast<int>(blockIdx.x) >= conv_blocks) {
+    // Fixed-order reduction of the dsink partials: one warp per head.
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = (static_cast<int>(blockIdx.x) - conv_blocks) * 8 + warp;
+    if (h >= p.hq) return;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    int i = lane;
+    for (; i + 7 * 32 < p.nparts; i += 8 * 32) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) acc[u] += p.part[static_cast<size_t>(i + 32 * u) * p.hq + h];
+    }
+    for (; i < p.nparts; i += 32) acc[0] += p.part[static_cast<size_t>(i) * p.hq + h];
+    float s = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) p.dsink[h] = s;
+    return;
+  }
+  const long long stride = static_cast<long long>(conv_blocks) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.n8; i += stride) {
+    const float4 a = reinterpret_cast<const float4*>(p.acc)[2 * i];
+    const float4 c = reinterpret_cast<const float4*>(p.acc)[2 * i + 1];
+    uint4 o;
+    o.x = pack_bf16(a.x * p.scale, a.y * p.scale);
+    o.y = pack_bf16(a.z * p.scale, a.w * p.scale);
+    o.z = pack_bf16(c.x * p.scale, c.y * p.scale);
+    o.w = pack_bf16(c.z * p.scale, c.w * p.scale);
+    reinterpret_cast<uint4*>(p.dq)[i] = o;
+  }
+}
+
+}  // namespace
+
+// Preprocess, main kernel (bwd_tc.cu), then dQ conversion and dsink reduction.
+cudaError_t launch_bwd(const Problem& pr, const BwdArgs& a, int* status, cudaStream_t stream) {
+  const long long T = pr.total_tokens;
+  {
+    PreK k{static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.sink,
+           a.delta, a.lse_log2, a.dq_accum, a.dsink_part, T, pr.hq};
+    if (a.preprocess_blocks > 0) bwd_pre_kernel<<<a.preprocess_blocks, 256, 0, stream>>>(k);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    cudaError_t e = launch_bwd_tc_main(pr, a, status, stream);
+    if (e != cudaSuccess) return e;
+  }
+  {
+    ConvK k{a.dq_accum, static_cast<__nv_bfloat16*>(a.dq), T * pr.hq * D / 8, pr.scale, a.dsink_part,
+            a.preprocess_blocks, pr.hq, a.dsink};
+    long long blocks = (k.n8 + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks < 1) blocks = 1;
+    dq_convert_kernel<<<static_cast<int>(blocks) + (pr.hq + 7) / 8, 256, 0, stream>>>(k);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace sa

@@ -103,26 +103,16 @@ struct BwdTcK {
   int hq, hkv, group;
   MaskParams mask;
   float scale, scale_log2;
-  // Query-range splitting of key tiles that hold always-visible prefix keys
-  // (only with a finite window, where those tiles would otherwise visit every
-  // query tile while their neighbours visit a few): such a tile's query tiles
-  // are cut into chunks of `qchunk`, one CTA each, whose partial dK/dV are
-  // added into the fp32 accumulator dkv_acc ([num_seqs][pre_tiles * 128][Hkv]
-  // [2][64]: dV then unscaled dK).  blockIdx.z >= n_kt indexes the extra chunks.
-  int n_kt, pre_tiles, qchunk;
+  // Work list slice (longest first).  A key tile whose query range is longer
+  // than `qchunk` query tiles is split into chunks, one item each; their
+  // partial dK/dV are added into the fp32 accumulator dkv_acc
+  // ([T][Hkv][2][64]: dV then unscaled dK) and converted afterwards.
+  int qchunk;
   float* dkv_acc;
+  int n_items;
+  BwdItem items[2048];
 };
-
-// Number of query-tile chunks of key tile kt in a sequence of length len.
-SA_DEV int tile_chunks(int kt, int len, const MaskParams& m, int pre_tiles, int qchunk) {
-  if (kt >= pre_tiles || m.window < 0) return 1;
-  const int k0 = kt * BN;
-  if (k0 >= len) return 0;
-  int qlo, qhi;
-  query_range(k0, min(k0 + BN, len) - 1, len, m, qlo, qhi);
-  const int nq = qhi / BM - qlo / BM + 1;
-  return (nq + qchunk - 1) / qchunk;
-}
+static_assert(sizeof(BwdTcK) < 32000, "kernel parameter block too large");
 
 struct Bars {
   uint64_t kv_full, kv_tmem;
@@ -199,31 +189,18 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x;
-  const SeqSpan sp = seq_span(p.cu, p.seqlen, blockIdx.y);
-  int kt = static_cast<int>(blockIdx.z), chunk = 0;
-  if (kt >= p.n_kt) {
-    // An extra chunk of a prefix key tile: find which one.
-    int e = kt - p.n_kt;
-    kt = 0;
-    while (kt < p.pre_tiles) {
-      const int extra = max(0, tile_chunks(kt, sp.len, p.mask, p.pre_tiles, p.qchunk) - 1);
-      if (e < extra) break;
-      e -= extra;
-      ++kt;
-    }
-    if (kt >= p.pre_tiles) return;
-    chunk = e + 1;
-  }
-  const int k0 = kt * BN;
+  const BwdItem item = p.items[blockIdx.y];  // longest first
+  const SeqSpan sp = seq_span(p.cu, p.seqlen, item.b);
+  const int k0 = static_cast<int>(item.kt) * BN;
   if (k0 >= sp.len) return;
   const int k1 = min(k0 + BN, sp.len) - 1;
-  const bool split = tile_chunks(kt, sp.len, p.mask, p.pre_tiles, p.qchunk) > 1;
+  const bool split = item.nchunks > 1;
   int qlo, qhi;
   query_range(k0, k1, sp.len, p.mask, qlo, qhi);
   int qt_lo = qlo / BM, nq = qhi / BM - qt_lo + 1;
   if (split) {
-    qt_lo += chunk * p.qchunk;
-    nq = min(p.qchunk, nq - chunk * p.qchunk);
+    qt_lo += item.chunk * p.qchunk;
+    nq = min(p.qchunk, nq - item.chunk * p.qchunk);
   }
   const int nsteps = p.group * nq;
   auto step_head = [&](int t) { return g * p.group + t / nq; };
@@ -466,8 +443,7 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
       const float mul = half ? p.scale : 1.f;
       if (key < sp.len && split) {
         // Partial sums of a split tile: add into the fp32 accumulator.
-        float* dst = p.dkv_acc + ((static_cast<size_t>(blockIdx.y) * p.pre_tiles * BN + key) * p.hkv + g) * 2 * D +
-                     half * D;
+        float* dst = p.dkv_acc + (static_cast<size_t>(sp.start + key) * p.hkv + g) * 2 * D + half * D;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           red_add_v4(dst + 4 * c, __uint_as_float(a[4 * c]), __uint_as_float(a[4 * c + 1]),
@@ -549,35 +525,29 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
   }
 }
 
-// dK, dV of split prefix tiles: fp32 accumulator -> bf16 (dK scaled).
+// dK, dV of split key tiles: fp32 accumulator -> bf16 (dK scaled).  One
+// block per work item; only the first chunk of a split tile converts it.
 struct DkvConvK {
   const float* acc;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   const int32_t* cu;
-  int seqlen, num_seqs, rows, hkv;  // rows = pre_tiles * 128
+  int seqlen, hkv;
   float scale;
-  MaskParams mask;
-  int pre_tiles, qchunk;
+  BwdItem items[2048];
 };
 
-__global__ void __launch_bounds__(256) dkv_convert_kernel(const DkvConvK p) {
-  const long long total = static_cast<long long>(p.num_seqs) * p.rows * p.hkv * 2 * (D / 8);
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int c8 = static_cast<int>(i % (D / 8));
-    long long r = i / (D / 8);
-    const int which = static_cast<int>(r % 2);  // 0: dV, 1: dK
-    r /= 2;
-    const int g = static_cast<int>(r % p.hkv);
-    r /= p.hkv;
-    const int key = static_cast<int>(r % p.rows);
-    const int b = static_cast<int>(r / p.rows);
-    const SeqSpan sp = seq_span(p.cu, p.seqlen, b);
-    if (key >= sp.len) continue;
-    // Only tiles that were split accumulate here; the others wrote bf16 directly.
-    if (tile_chunks(key / BN, sp.len, p.mask, p.pre_tiles, p.qchunk) <= 1) continue;
-    const float* src = p.acc + (((static_cast<size_t>(b) * p.rows + key) * p.hkv + g) * 2 + which) * D + 8 * c8;
+__global__ void __launch_bounds__(256) dkv_convert_kernel(const __grid_constant__ DkvConvK p) {
+  const BwdItem item = p.items[blockIdx.x];
+  if (item.nchunks <= 1 || item.chunk != 0) return;
+  const SeqSpan sp = seq_span(p.cu, p.seqlen, item.b);
+  const int k0 = item.kt * BN, rows = min(BN, sp.len - k0);
+  const int per_row = p.hkv * 2 * (D / 8);  // 8-element groups per key row
+  for (int i = threadIdx.x; i < rows * per_row; i += blockDim.x) {
+    const int r = i / per_row, rem = i - r * per_row;
+    const int g = rem / (2 * (D / 8)), which = (rem / (D / 8)) & 1, c8 = rem % (D / 8);
+    const size_t row = static_cast<size_t>(sp.start + k0 + r);
+    const float* src = p.acc + ((row * p.hkv + g) * 2 + which) * D + 8 * c8;
     const float mul = which ? p.scale : 1.f;
     const float4 x = reinterpret_cast<const float4*>(src)[0], y = reinterpret_cast<const float4*>(src)[1];
     uint4 o;
@@ -585,46 +555,21 @@ __global__ void __launch_bounds__(256) dkv_convert_kernel(const DkvConvK p) {
     o.y = pack_bf16(x.z * mul, x.w * mul);
     o.z = pack_bf16(y.x * mul, y.y * mul);
     o.w = pack_bf16(y.z * mul, y.w * mul);
-    __nv_bfloat16* dst = (which ? p.dk : p.dv) + (static_cast<size_t>(sp.start + key) * p.hkv + g) * D + 8 * c8;
-    *reinterpret_cast<uint4*>(dst) = o;
+    *reinterpret_cast<uint4*>((which ? p.dk : p.dv) + (row * p.hkv + g) * D + 8 * c8) = o;
   }
 }
 
 }  // namespace
 
-// Host view of the prefix-tile split (same rule as tile_chunks on the device).
-void bwd_split_plan(const Problem& pr, int& pre_tiles, int& qchunk, int& n_extra) {
-  pre_tiles = 0;
-  qchunk = 1;
-  n_extra = 0;
-  if (pr.window < 0 || pr.prefix <= 0 || pr.seqlen == 0) return;
-  pre_tiles = ceil_div(pr.prefix, BN);
-  // Chunk so a split CTA has about as many query tiles as a window-only tile.
-  qchunk = max(2, ceil_div(static_cast<long long>(pr.window) + BN, BM) + 1);
-  const int len = pr.seqlen;
-  for (int kt = 0; kt < pre_tiles; ++kt) {
-    const int k0 = kt * BN;
-    if (k0 >= len) break;
-    const int k1 = std::min(k0 + BN, len) - 1;
-    const int qlo = pr.causal ? k0 : 0;
-    const int qhi = len - 1;  // a prefix key is visible to every later query
-    (void)k1;
-    const int nq = qhi / BM - qlo / BM + 1;
-    n_extra += std::max(0, ceil_div(nq, qchunk) - 1);
-  }
-}
-
 size_t bwd_split_acc_bytes(const Problem& pr) {
-  int pre, qc, ne;
-  bwd_split_plan(pr, pre, qc, ne);
-  if (pre == 0) return 0;
-  return static_cast<size_t>(pr.num_seqs) * pre * BN * pr.hkv * 2 * D * sizeof(float);
+  if (pr.total_tokens == 0 || pr.num_seqs == 0) return 0;
+  if (!bwd_any_split(bwd_work_list(pr, bwd_qchunk(pr)))) return 0;
+  return static_cast<size_t>(pr.total_tokens) * pr.hkv * 2 * D * sizeof(float);
 }
 
 cudaError_t launch_bwd_tc_main(const Problem& pr, const BwdArgs& a, int* status, cudaStream_t stream) {
-  const int n_kt = ceil_div(pr.seqlen, BN);
-  if (n_kt == 0 || pr.num_seqs == 0 || pr.total_tokens == 0) return cudaSuccess;
-  BwdTcK k;
+  if (pr.num_seqs == 0 || pr.total_tokens == 0 || pr.seqlen == 0) return cudaSuccess;
+  thread_local BwdTcK k;  // 17 KB parameter block; host-side staging, one per host thread
   if (!make_rows_map(&k.tm_q, a.q, pr.total_tokens, pr.hq, BM) ||
       !make_rows_map(&k.tm_do, a.dout, pr.total_tokens, pr.hq, BM) ||
       !make_rows_map(&k.tm_k, a.k, pr.total_tokens, pr.hkv, BN) ||
@@ -645,12 +590,11 @@ cudaError_t launch_bwd_tc_main(const Problem& pr, const BwdArgs& a, int* status,
   k.mask = MaskParams{pr.window, pr.prefix, pr.causal};
   k.scale = pr.scale;
   k.scale_log2 = pr.scale * kLog2e;
-  int n_extra = 0;
-  bwd_split_plan(pr, k.pre_tiles, k.qchunk, n_extra);
-  k.n_kt = n_kt;
+  k.qchunk = bwd_qchunk(pr);
   k.dkv_acc = a.dkv_acc;
+  const std::vector<BwdItem> items = bwd_work_list(pr, k.qchunk);
+  const bool any_split = bwd_any_split(items);
   cudaError_t e;
-  const bool any_split = n_extra > 0;
   if (any_split) {
     if (a.dkv_acc == nullptr) return cudaErrorInvalidValue;
     if ((e = cudaMemsetAsync(a.dkv_acc, 0, bwd_split_acc_bytes(pr), stream)) != cudaSuccess) return e;
@@ -658,17 +602,31 @@ cudaError_t launch_bwd_tc_main(const Problem& pr, const BwdArgs& a, int* status,
   if ((e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_DYN)) !=
       cudaSuccess)
     return e;
-  dim3 grid(pr.hkv, pr.num_seqs, n_kt + n_extra);
+  constexpr int kMax = static_cast<int>(sizeof(k.items) / sizeof(k.items[0]));
   if ((e = prof_begin(g_prof_bwd, stream)) != cudaSuccess) return e;
-  bwd_tc_kernel<<<grid, NTHR, SMEM_DYN, stream>>>(k);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  for (size_t first = 0; first < items.size(); first += kMax) {
+    const int n = static_cast<int>(std::min<size_t>(kMax, items.size() - first));
+    std::copy(items.begin() + first, items.begin() + first + n, k.items);
+    k.n_items = n;
+    bwd_tc_kernel<<<dim3(pr.hkv, n), NTHR, SMEM_DYN, stream>>>(k);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   if ((e = prof_end(g_prof_bwd, stream)) != cudaSuccess) return e;
   if (any_split) {
-    DkvConvK c{a.dkv_acc, static_cast<__nv_bfloat16*>(a.dk), static_cast<__nv_bfloat16*>(a.dv), pr.cu, pr.seqlen,
-               pr.num_seqs, k.pre_tiles * BN, pr.hkv, pr.scale, k.mask, k.pre_tiles, k.qchunk};
-    const long long total = static_cast<long long>(pr.num_seqs) * c.rows * pr.hkv * 2 * (D / 8);
-    dkv_convert_kernel<<<static_cast<int>(std::min<long long>((total + 255) / 256, 152 * 8)), 256, 0, stream>>>(c);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    thread_local DkvConvK c;
+    c.acc = a.dkv_acc;
+    c.dk = static_cast<__nv_bfloat16*>(a.dk);
+    c.dv = static_cast<__nv_bfloat16*>(a.dv);
+    c.cu = pr.cu;
+    c.seqlen = pr.seqlen;
+    c.hkv = pr.hkv;
+    c.scale = pr.scale;
+    for (size_t first = 0; first < items.size(); first += kMax) {
+      const int n = static_cast<int>(std::min<size_t>(kMax, items.size() - first));
+      std::copy(items.begin() + first, items.begin() + first + n, c.items);
+      dkv_convert_kernel<<<n, 256, 0, stream>>>(c);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
   }
   return cudaSuccess;
 }

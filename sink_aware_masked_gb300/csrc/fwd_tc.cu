@@ -44,6 +44,8 @@
 #include "tc.cuh"
 #include "tmap.h"
 
+#include <algorithm>
+
 // Optional timeline instrumentation for performance work: compiled in only
 // when SA_FWD_TRACE is defined (never in the library build).
 #ifdef SA_FWD_TRACE
@@ -93,8 +95,10 @@ struct FwdTcK {
   int hq, hkv, group, nh;
   MaskParams mask;
   float scale_log2;
-  int n_qtiles;
+  int n_items;
+  uint32_t items[4096];  // this launch's slice of the work list: b | (query tile << 16)
 };
+static_assert(sizeof(FwdTcK) < 32000, "kernel parameter block too large");
 
 struct Bars {
   uint64_t q_full;
@@ -122,9 +126,9 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
   const int nh = p.nh;
   const int h0 = static_cast<int>(blockIdx.x) * nh;
   const int g = h0 / p.group;
-  const SeqSpan sp = seq_span(p.cu, p.seqlen, blockIdx.y);
-  const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.z);  // longest rows first
-  const int q0 = qt * BM;
+  const uint32_t item = p.items[blockIdx.y];  // longest first
+  const SeqSpan sp = seq_span(p.cu, p.seqlen, static_cast<int>(item & 0xFFFFu));
+  const int q0 = static_cast<int>(item >> 16) * BM;
   if (q0 >= sp.len) return;
   const int q1 = min(q0 + BM, sp.len) - 1;
   const KeyRange kr = key_range(q0, q1, sp.len, p.mask);
@@ -419,7 +423,7 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
 
 cudaError_t launch_fwd_tc(const Problem& pr, const FwdArgs& a, int* status, cudaStream_t stream) {
   if (pr.total_tokens == 0 || pr.num_seqs == 0 || pr.seqlen == 0) return cudaSuccess;
-  FwdTcK k;
+  thread_local FwdTcK k;  // 17 KB parameter block; host-side staging, one per host thread
   if (!make_rows_map(&k.tm_q, a.q, pr.total_tokens, pr.hq, BM) ||
       !make_rows_map(&k.tm_k, a.k, pr.total_tokens, pr.hkv, BN) ||
       !make_rows_map(&k.tm_v, a.v, pr.total_tokens, pr.hkv, BN))
@@ -437,13 +441,19 @@ cudaError_t launch_fwd_tc(const Problem& pr, const FwdArgs& a, int* status, cuda
   k.nh = (k.group % 2 == 0) ? 2 : 1;
   k.mask = MaskParams{pr.window, pr.prefix, pr.causal};
   k.scale_log2 = pr.scale * kLog2e;
-  k.n_qtiles = ceil_div(pr.seqlen, BM);
+  const std::vector<uint32_t> items = fwd_work_list(pr);
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_DYN);
   if (e != cudaSuccess) return e;
-  dim3 grid(pr.hq / k.nh, pr.num_seqs, k.n_qtiles);
   if ((e = prof_begin(g_prof_fwd, stream)) != cudaSuccess) return e;
-  fwd_tc_kernel<<<grid, NTHR, SMEM_DYN, stream>>>(k);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  constexpr int kMax = static_cast<int>(sizeof(k.items) / sizeof(k.items[0]));
+  for (size_t first = 0; first < items.size(); first += kMax) {
+    const int n = static_cast<int>(std::min<size_t>(kMax, items.size() - first));
+    std::copy(items.begin() + first, items.begin() + first + n, k.items);
+    k.n_items = n;
+    dim3 grid(pr.hq / k.nh, n);
+    fwd_tc_kernel<<<grid, NTHR, SMEM_DYN, stream>>>(k);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   return prof_end(g_prof_fwd, stream);
 }
 

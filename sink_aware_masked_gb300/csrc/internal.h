@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <vector>
+
 namespace sa {
 
 constexpr int kHeadDim = 64;
@@ -54,9 +56,21 @@ struct BwdArgs {
 };
 
 // Preprocess tokens per block (bounds the number of dsink partial rows).
-constexpr int kPreTokens = 32;
+constexpr int kPreTokens = 8;
 
 inline int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+// One backward work item: key tile `kt` of sequence `b`, query chunk `chunk`
+// of `nchunks` (nchunks > 1: partial dK/dV go to the fp32 accumulator).
+struct BwdItem {
+  uint16_t b, kt, chunk, nchunks;
+};
+
+// Work lists (schedule.cu), longest first.
+std::vector<uint32_t> fwd_work_list(const Problem& p);  // b | (query tile << 16)
+int bwd_qchunk(const Problem& p);
+std::vector<BwdItem> bwd_work_list(const Problem& p, int qchunk);
+bool bwd_any_split(const std::vector<BwdItem>& items);
 
 // Optional events recorded around the main kernels (measurement hook).
 struct ProfileEvents {
