@@ -157,6 +157,14 @@ sinkattn_status sinkattn_get_device_status(void* stream);
  * Returns INVALID_ARG for an unknown kind or a half-NULL pair. */
 sinkattn_status sinkattn_set_profile_events(int32_t kind, void* start, void* stop);
 
+/* Self-test of the bounded waits the kernels use: launches one CTA that
+ * waits on an mbarrier nothing ever arrives on, giving up after
+ * `limit_cycles` SM cycles (1 .. 2e9) exactly as a kernel's wait does on a
+ * timeout.  Afterwards sinkattn_get_device_status() reports
+ * SINKATTN_ERR_TIMEOUT once.  Nothing faults or hangs; the context stays
+ * usable.  INVALID_ARG for a limit out of range. */
+sinkattn_status sinkattn_selftest_wait_timeout(int64_t limit_cycles, void* stream);
+
 /* Static, human-readable name of a status. */
 const char* sinkattn_status_string(sinkattn_status s);
 

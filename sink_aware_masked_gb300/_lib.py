@@ -50,6 +50,7 @@ SIGNATURES = {
     "sinkattn_unpack": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp]),
     "sinkattn_get_device_status": (ctypes.c_int, [_vp]),
     "sinkattn_set_profile_events": (ctypes.c_int, [_i32, _vp, _vp]),
+    "sinkattn_selftest_wait_timeout": (ctypes.c_int, [_i64, _vp]),
     "sinkattn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "sinkattn_version": (_i32, []),
 }

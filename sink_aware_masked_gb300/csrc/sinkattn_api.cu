@@ -7,6 +7,7 @@
 
 #include "../../include/sinkattn.h"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace sa {
 ProfileEvents g_prof_fwd, g_prof_bwd;
@@ -82,6 +83,20 @@ sinkattn_status normalise(const sinkattn_problem* pr, sa::Problem& out) {
   out.causal = pr->causal;
   out.scale = pr->scale;
   return SINKATTN_OK;
+}
+
+// One CTA waits on an mbarrier that never completes, with a bounded wait.
+__global__ void selftest_wait_kernel(int* status, long long limit) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    sa::tc::mbar_init(sa::smem_u32(&bar), 1);
+    sa::tc::fence_mbar_init();
+  }
+  __syncthreads();
+  const sa::tc::Abort ab{&abort_flag, status};
+  sa::tc::mbar_wait(sa::smem_u32(&bar), 0, ab, limit);
 }
 
 struct BwdLayout {
@@ -231,6 +246,14 @@ sinkattn_status sinkattn_set_profile_events(int32_t kind, void* start, void* sto
   else
     return SINKATTN_ERR_INVALID_ARG;
   return SINKATTN_OK;
+}
+
+sinkattn_status sinkattn_selftest_wait_timeout(int64_t limit_cycles, void* stream) {
+  if (limit_cycles < 1 || limit_cycles > 2000000000LL) return SINKATTN_ERR_INVALID_ARG;
+  int* status = status_word();
+  if (status == nullptr) return SINKATTN_ERR_CUDA;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, limit_cycles);
+  return from_cuda(cudaGetLastError());
 }
 
 const char* sinkattn_status_string(sinkattn_status s) {

@@ -55,13 +55,13 @@ struct Abort {
   int* status;         // global device status word
 };
 
-SA_DEV bool mbar_wait(uint32_t bar, uint32_t parity, const Abort& ab) {
+SA_DEV bool mbar_wait(uint32_t bar, uint32_t parity, const Abort& ab, long long limit = kTimeoutCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*ab.flag) return false;
-    if (clock64() - t0 > kTimeoutCycles) {
+    if (clock64() - t0 > limit) {
       *ab.flag = 1;
       atomicExch(ab.status, kStatusTimeout);
       return false;
