@@ -8,7 +8,7 @@
 //   D   = <dO, O>                      O is the final, alpha-scaled output
 //   dsink[h] = -sum_rows (1 - alpha) D,   1 - alpha = sigmoid(s_h - l)
 //
-//   bwd_pre   : one pass over O and dO: D, l' (log2 units), per-block partial
+//   bwd_pre   : one pass over O and dO: -D, -l' (log2 units), per-block partial
 //               dsink sums, zeroes the fp32 dQ accumulator.  HBM-bound; many
 //               small blocks and two tokens' loads in flight per iteration
 //               keep enough bytes in flight.
@@ -84,8 +84,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreK p) {
         const float l = p.lse[idx];
         const float x = __ldg(p.sink + h) - l;
         const float softplus = fmaxf(x, 0.f) + log1pf(__expf(-fabsf(x)));
-        p.lse_log2[idx] = (l + softplus) * kLog2e;
-        p.delta[idx] = dot;
+        // Stored negated so the main kernel's element-wise pass is two packed
+        // f32x2 operations per pair: exp2(s * c + (-l')) and dP + (-D).
+        p.lse_log2[idx] = -(l + softplus) * kLog2e;
+        p.delta[idx] = -dot;
         const float one_minus_alpha = 1.f / (1.f + __expf(-x));
         acc[hi] -= one_minus_alpha * dot;
       }

@@ -146,38 +146,41 @@ SA_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint
 
 // One 32-column chunk of the element-wise step for this thread's key row:
 // P^T = exp2(S^T * scale * log2(e) - l'), dS^T = P^T (dP^T - D), packed to bf16
-// pairs.  FULL skips the mask predicate (every pair of the tile visible).
+// pairs.  The preprocess stored -l' (log2 units) and -D, so each pair of
+// columns costs one f32x2 FMA, one f32x2 add and one f32x2 multiply.  FULL
+// skips the mask predicate (every pair of the tile visible).
 template <bool FULL>
 SA_DEV void ew_chunk(uint32_t tS, uint32_t tDP, uint32_t sL, uint32_t sD, float sl2, int qb, int key, int len,
                      const MaskParams& mask, uint32_t (&pp)[16], uint32_t (&dd)[16]) {
   // tS, tDP: TMEM address of this chunk's 32 columns; sL, sD: shared address
-  // of its 32 l' and D values; qb: position of its first query.
+  // of its 32 -l' and -D values; qb: position of its first query.
   uint32_t sr[32], dr[32];
   tmem_ld32(tS, sr);
   tmem_ld32(tDP, dr);
   tmem_ld_wait();
   reg_fence32(sr);
   reg_fence32(dr);
+  const float2 sl2x2 = make_float2(sl2, sl2);
 #pragma unroll
   for (int e = 0; e < 32; e += 4) {
     const float4 l4 = ld_shared_f4(sL + e * 4);
     const float4 d4 = ld_shared_f4(sD + e * 4);
-    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-    const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-    float pe[4], de[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      pe[u] = ex2(fmaf(__uint_as_float(sr[e + u]), sl2, -lv[u]));
-      de[u] = pe[u] * (__uint_as_float(dr[e + u]) - dv[u]);
+    for (int u = 0; u < 4; u += 2) {
+      const float2 x = ffma2(make_float2(__uint_as_float(sr[e + u]), __uint_as_float(sr[e + u + 1])), sl2x2,
+                             u ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y));
+      float2 pe = make_float2(ex2(x.x), ex2(x.y));
+      const float2 t = fadd2(make_float2(__uint_as_float(dr[e + u]), __uint_as_float(dr[e + u + 1])),
+                             u ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y));
+      float2 de = fmul2(pe, t);
       if (!FULL) {
         const int q = qb + e + u;
-        if (!(q < len && visible(q, key, len, mask))) pe[u] = de[u] = 0.f;
+        if (!(q < len && visible(q, key, len, mask))) pe.x = de.x = 0.f;
+        if (!(q + 1 < len && visible(q + 1, key, len, mask))) pe.y = de.y = 0.f;
       }
+      pp[(e + u) >> 1] = pack_bf16(pe.x, pe.y);
+      dd[(e + u) >> 1] = pack_bf16(de.x, de.y);
     }
-    pp[e >> 1] = pack_bf16(pe[0], pe[1]);
-    pp[(e >> 1) + 1] = pack_bf16(pe[2], pe[3]);
-    dd[e >> 1] = pack_bf16(de[0], de[1]);
-    dd[(e >> 1) + 1] = pack_bf16(de[2], de[3]);
   }
 }
 

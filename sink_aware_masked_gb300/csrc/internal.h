@@ -48,8 +48,8 @@ struct BwdArgs {
   float* dsink;
   // workspace carve-up
   float* dq_accum;    // [T, Hq, 64] fp32
-  float* delta;       // [Hq, T]  D = <dO, O>
-  float* lse_log2;    // [Hq, T]  (l + softplus(sink - l)) * log2(e)
+  float* delta;       // [Hq, T]  -D = -<dO, O>
+  float* lse_log2;    // [Hq, T]  -(l + softplus(sink - l)) * log2(e)
   float* dsink_part;  // [preprocess blocks, Hq]
   float* dkv_acc;     // fp32 dK/dV partial sums of split prefix key tiles (or nullptr)
   int preprocess_blocks;
