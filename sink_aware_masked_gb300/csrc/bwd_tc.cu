@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
     int issued = 0;
     for (int t = 0; t < nsteps; ++t) {
       const int s = t % NS;
-      if (t >= NS && !__all_sync(0xffffffffu, mbar_wait(b_qe(s), ((t / NS) - 1) & 1, ab))) break;
+      if (t >= NS && !mbar_wait_warp(b_qe(s), ((t / NS) - 1) & 1, ab)) break;
       if (lane == 0) SA_TRACE(0, t, 0);
       const int h = step_head(t), q0 = step_q0(t);
       // l' and D of the 128 query rows: asynchronous 4-byte copies that
@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
           }
         }
       };
-      bool ok = __all_sync(0xffffffffu, mbar_wait(b_kvt, 0, ab)) && __all_sync(0xffffffffu, mbar_wait(b_qf(0), 0, ab));
+      bool ok = mbar_wait_warp(b_kvt, 0, ab) && mbar_wait_warp(b_qf(0), 0, ab);
       if (ok) {
         fence_after_sync();
         for (int h = 0; h < 2; ++h) {
@@ -324,11 +324,11 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
         const int s = t % NS, db = t & 1;
         if (lane == 0) SA_TRACE(1, t, 0);
         for (int h = 0; h < 2 && ok; ++h) {
-          if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_p(h), t & 1, ab)))) break;
+          if (!(ok = mbar_wait_warp(b_p(h), t & 1, ab))) break;
           if (lane == 0) SA_TRACE(1, t, 1 + 2 * h);
           fence_after_sync();
           if (h == 0 && t + 1 < nsteps) {
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_qf((t + 1) % NS), ((t + 1) / NS) & 1, ab)))) break;
+            if (!(ok = mbar_wait_warp(b_qf((t + 1) % NS), ((t + 1) / NS) & 1, ab))) break;
             fence_after_sync();
           }
           // dV += P_h^T dO_h and dK += dS_h^T Q_h, A operands in the S^T / dP^T columns of half h.
@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
         if (!ok) break;
         if (leader) mma_commit(b_qe(s));  // Q(t), dO(t), l'(t), D(t) have no later reader
         if (t > 0) {
-          if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_dqe, (t - 1) & 1, ab)))) break;
+          if (!(ok = mbar_wait_warp(b_dqe, (t - 1) & 1, ab))) break;
           fence_after_sync();
         }
         if (lane == 0) SA_TRACE(1, t, 5);
@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
     const uint32_t lb = lane_base(warp);
     const uint32_t tS = tmem + TM_S + HALF * half + lb, tDP = tmem + TM_DP + HALF * half + lb;
     const float sl2 = p.scale_log2;
-    bool ok = __all_sync(0xffffffffu, mbar_wait(b_kv, 0, ab));
+    bool ok = mbar_wait_warp(b_kv, 0, ab);
     if (ok) {
       // Copy this thread's row of K (first half) or V (second half) into TMEM,
       // where it is the A operand of S^T = K Q^T / dP^T = V dO^T.
@@ -397,8 +397,8 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
     for (int t = 0; ok && t < nsteps; ++t) {
       const int s = t % NS;
       if (tid == 128) SA_TRACE(2, t, 0);
-      ok = __all_sync(0xffffffffu, mbar_wait(b_s(half), t & 1, ab)) &&
-           __all_sync(0xffffffffu, mbar_wait(b_qf(s), (t / NS) & 1, ab));
+      ok = mbar_wait_warp(b_s(half), t & 1, ab) &&
+           mbar_wait_warp(b_qf(s), (t / NS) & 1, ab);
       if (!ok) break;
       if (tid == 128) SA_TRACE(2, t, 1);
       fence_after_sync();
@@ -432,7 +432,7 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
       if (lane == 0) mbar_arrive(b_p(half));
       if (tid == 128) SA_TRACE(2, t, 4);
     }
-    ok = ok && __all_sync(0xffffffffu, mbar_wait(b_done, 0, ab));
+    ok = ok && mbar_wait_warp(b_done, 0, ab);
     if (ok) {
       // First warpgroup writes dV, second writes dK (scaled).
       fence_after_sync();
@@ -482,7 +482,7 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
     bool ok = true;
     for (int t = 0; t < nsteps; ++t) {
       if (leader) SA_TRACE(3, t, 0);
-      ok = __all_sync(0xffffffffu, mbar_wait(b_dqf, t & 1, ab));
+      ok = mbar_wait_warp(b_dqf, t & 1, ab);
       if (!ok) break;
       if (leader) SA_TRACE(3, t, 1);
       fence_after_sync();

@@ -79,6 +79,19 @@ SA_DEV bool block_full(int q0, int nq, int k0, int nk, int len, const MaskParams
   return (m.window < 0) || (q1 - k0 <= m.window) || (k1 < m.prefix);
 }
 
+// Bit e set for e < n, n clamped to [0, 32].
+SA_DEV uint32_t bits_below(int n) { return n <= 0 ? 0u : (n >= 32 ? 0xFFFFFFFFu : (1u << n) - 1u); }
+
+// visible(q, kbase + e, len, m) for e = 0..31 as a bit mask: keys up to the
+// causal / sequence bound, and at or above the window's lower edge unless
+// they lie in the prefix.
+SA_DEV uint32_t visible_bits(int q, int kbase, int len, const MaskParams& m) {
+  const int hi = (m.causal ? min(q, len - 1) : len - 1) - kbase;
+  uint32_t r = bits_below(hi + 1);
+  if (m.window >= 0) r &= ~bits_below(q - m.window - kbase) | bits_below(m.prefix - kbase);
+  return r;
+}
+
 // ---------------------------------------------------------------- PTX helpers
 SA_DEV uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
@@ -170,6 +183,23 @@ SA_DEV float2 fmul2(float2 a, float2 b) {
       : "=l"(d)
       : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
   return *reinterpret_cast<float2*>(&d);
+}
+
+// exp2_fma on a pair: the same range reduction and polynomial, with the
+// additions and the Horner steps in packed f32x2 form (6 instructions per
+// element instead of 9).
+SA_DEV float2 exp2_fma2(float2 x) {
+  x.x = fmaxf(x.x, -125.f);
+  x.y = fmaxf(x.y, -125.f);
+  const float2 big = make_float2(12582912.f, 12582912.f);
+  const float2 t = fadd2(x, big);
+  const float2 j = fadd2(t, make_float2(-12582912.f, -12582912.f));
+  const float2 f = ffma2(j, make_float2(-1.f, -1.f), x);
+  float2 p = ffma2(make_float2(0.0551716648f, 0.0551716648f), f, make_float2(0.242611125f, 0.242611125f));
+  p = ffma2(p, f, make_float2(0.693260968f, 0.693260968f));
+  p = ffma2(p, f, make_float2(0.999928057f, 0.999928057f));
+  return make_float2(__int_as_float(__float_as_int(p.x) + (__float_as_int(t.x) << 23)),
+                     __int_as_float(__float_as_int(p.y) + (__float_as_int(t.y) << 23)));
 }
 
 // Offset in bytes of 16-byte chunk `c` (0..7) of row `r` in a tile whose rows

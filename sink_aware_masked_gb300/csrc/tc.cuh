@@ -69,6 +69,15 @@ SA_DEV bool mbar_wait(uint32_t bar, uint32_t parity, const Abort& ab, long long 
   }
 }
 
+// Wait by a whole warp (every lane passes the same barrier and parity).  The
+// common case, a phase that has already completed, is a single try_wait and
+// a vote with no divergent branch; only a pending phase enters the polling
+// loop.
+SA_DEV bool mbar_wait_warp(uint32_t bar, uint32_t parity, const Abort& ab) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab));
+}
+
 // ------------------------------------------------------------------ TMA
 SA_DEV void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

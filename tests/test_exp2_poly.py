@@ -56,3 +56,13 @@ def test_masked_scores_vanish():
     c = kernel_coefficients()
     got = emulate(np.array([-np.inf, -1e30, -200.0], dtype=np.float32), c)
     assert np.all(got > 0) and np.all(got < 3e-38)
+
+
+def test_packed_variant_uses_same_polynomial():
+    """exp2_fma2 (the f32x2 form) must carry exactly the scalar coefficients."""
+    with open(HDR) as f:
+        src = f.read()
+    body = src[src.index("SA_DEV float2 exp2_fma2"):]
+    body = body[:body.index("\n}")]
+    nums = {float(x) for x in re.findall(r"(\d+\.\d+)f", body) if float(x) < 2.0}
+    assert nums == set(kernel_coefficients())

@@ -129,18 +129,28 @@ def test_full_size_workload_group(name):
     pu.assert_within(pu.errors(gpu, ref, heads, [g]), name)
 
 
+# Outputs reduced in a fixed order are bitwise reproducible; dQ (TMA
+# reduce-add of every key tile's contribution) and the dK/dV of key tiles
+# split over several CTAs (fp32 reductions) are summed in arrival order, so
+# repeated runs agree to fp32 rounding, not bit for bit.
+EXACT = ("o", "lse", "dsink")
+REDUCED = ("dq", "dk", "dv")
+
+
+def assert_same_run(a, b, label):
+    for key in EXACT:
+        assert torch.equal(a[key], b[key]), (label, key)
+    for key in REDUCED:
+        assert pu.rel_l2(a[key].double().cpu().numpy(), b[key].double().cpu().numpy()) < 1e-3, (label, key)
+
+
 def test_determinism_and_window_fold():
     wl = W.custom((1500,), 8, 2, seed=40, sink_dist="uniform2", name="det")
     inp = W.make_inputs(wl)
     a = gpu_run(inp, wl)
-    b = gpu_run(inp, wl)
-    for key in ("o", "lse", "dk", "dv", "dsink"):
-        assert torch.equal(a[key], b[key]), key
-    assert pu.rel_l2(a["dq"].double().cpu().numpy(), b["dq"].double().cpu().numpy()) < 1e-3
+    assert_same_run(a, gpu_run(inp, wl), "repeat")
     for w in (1499, 1500, 10**9):
-        c = gpu_run(inp, wl, window=w)
-        for key in ("o", "lse", "dk", "dv", "dsink"):
-            assert torch.equal(a[key], c[key]), (w, key)
+        assert_same_run(a, gpu_run(inp, wl, window=w), w)
 
 
 def test_packed_equals_per_sequence():
@@ -156,10 +166,10 @@ def test_packed_equals_per_sequence():
         one = W.Inputs(one_wl, inp.q_bf16[t0:t1].clone(), inp.k_bf16[t0:t1].clone(), inp.v_bf16[t0:t1].clone(),
                        inp.do_bf16[t0:t1].clone(), inp.sink.clone())
         r = gpu_run(one, one_wl)
-        for key in ("o", "dk", "dv"):
-            assert torch.equal(packed[key][t0:t1], r[key]), (i, key)
+        assert torch.equal(packed["o"][t0:t1], r["o"]), i
         assert torch.equal(packed["lse"][:, t0:t1], r["lse"]), i
-        assert pu.rel_l2(packed["dq"][t0:t1].double().cpu().numpy(), r["dq"].double().cpu().numpy()) < 1e-3
+        for key in REDUCED:
+            assert pu.rel_l2(packed[key][t0:t1].double().cpu().numpy(), r[key].double().cpu().numpy()) < 1e-3, (i, key)
         dsink += r["dsink"].double().cpu()
     assert pu.rel_l2(packed["dsink"].double().cpu().numpy(), dsink.numpy()) < 1e-5
 
