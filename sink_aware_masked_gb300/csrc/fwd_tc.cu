@@ -295,8 +295,8 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
           const int s = nt % NS;
           // Both tests are issued before either result is needed, so their
           // latencies overlap; a phase still pending falls back to a wait.
-          const bool kv_ready = mbar_try_wait(b_kv(s), (nt / NS) & 1);
-          const bool s_ready = nt == 0 || mbar_try_wait(b_sf, (nt - 1) & 1);
+          const bool kv_ready = mbar_test_wait(b_kv(s), (nt / NS) & 1);
+          const bool s_ready = nt == 0 || mbar_test_wait(b_sf, (nt - 1) & 1);
           if (!__all_sync(0xffffffffu, kv_ready) && !(ok = wait_all(b_kv(s), (nt / NS) & 1))) break;
           if (!__all_sync(0xffffffffu, s_ready) && !(ok = wait_all(b_sf, (nt - 1) & 1))) break;
           fence_after_sync();
@@ -353,8 +353,8 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
           // Early tests of the two halves of the previous step's P.V; the
           // results are used only when P is stored, so their latency hides
           // behind the arithmetic below.
-          const bool pv_ready0 = nt == 0 || mbar_try_wait(b_pv(0), (nt - 1) & 1);
-          const bool pv_ready1 = nt == 0 || mbar_try_wait(b_pv(1), (nt - 1) & 1);
+          const bool pv_ready0 = nt == 0 || mbar_test_wait(b_pv(0), (nt - 1) & 1);
+          const bool pv_ready1 = nt == 0 || mbar_test_wait(b_pv(1), (nt - 1) & 1);
 #define S_(c) r_[(c) >> 5][(c) & 31]
           const int k0 = u.tile_k0(j);
           if (!block_full(u.q0, BM, k0, BN, u.sp.len, p.mask)) {
