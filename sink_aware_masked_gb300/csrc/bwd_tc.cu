@@ -53,8 +53,7 @@
 __device__ long long* g_bwd_trace;
 #define SA_TRACE(role, step, ev)                                                                       \
   do {                                                                                                \
-    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && g_bwd_trace != nullptr && (step) < 1024) \
-      g_bwd_trace[((role) * 1024 + (step)) * 8 + (ev)] = clock64();                                   \
+    if (trace_p != nullptr && (step) < 1024) trace_p[((role) * 1024 + (step)) * 8 + (ev)] = clock64(); \
   } while (0)
 #else
 #define SA_TRACE(role, step, ev) \
@@ -144,25 +143,19 @@ SA_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-// One 32-column chunk of the element-wise step for this thread's key row:
+// One 16-column chunk of the element-wise step for this thread's key row:
 // P^T = exp2(S^T * scale * log2(e) - l'), dS^T = P^T (dP^T - D), packed to bf16
 // pairs.  The preprocess stored -l' (log2 units) and -D, so each pair of
 // columns costs one f32x2 FMA, one f32x2 add and one f32x2 multiply.  FULL
 // skips the mask predicate (every pair of the tile visible).
 template <bool FULL>
-SA_DEV void ew_chunk(uint32_t tS, uint32_t tDP, uint32_t sL, uint32_t sD, float sl2, int qb, int key, int len,
-                     const MaskParams& mask, uint32_t (&pp)[16], uint32_t (&dd)[16]) {
-  // tS, tDP: TMEM address of this chunk's 32 columns; sL, sD: shared address
-  // of its 32 -l' and -D values; qb: position of its first query.
-  uint32_t sr[32], dr[32];
-  tmem_ld32(tS, sr);
-  tmem_ld32(tDP, dr);
-  tmem_ld_wait();
-  reg_fence32(sr);
-  reg_fence32(dr);
+SA_DEV void ew_chunk(const uint32_t (&sr)[16], const uint32_t (&dr)[16], uint32_t sL, uint32_t sD, float sl2, int qb,
+                     int key, int len, const MaskParams& mask, uint32_t (&pp)[8], uint32_t (&dd)[8]) {
+  // sr, dr: S^T and dP^T of 16 queries; sL, sD: shared address of their -l'
+  // and -D values; qb: position of the first query.
   const float2 sl2x2 = make_float2(sl2, sl2);
 #pragma unroll
-  for (int e = 0; e < 32; e += 4) {
+  for (int e = 0; e < 16; e += 4) {
     const float4 l4 = ld_shared_f4(sL + e * 4);
     const float4 d4 = ld_shared_f4(sD + e * 4);
 #pragma unroll
@@ -184,6 +177,38 @@ SA_DEV void ew_chunk(uint32_t tS, uint32_t tDP, uint32_t sL, uint32_t sD, float 
   }
 }
 
+// The element-wise pass over one half step (64 queries) in four 16-column
+// chunks; the Tensor Memory loads of the next chunk are issued before the
+// current one is computed, so their latency overlaps the arithmetic.
+template <bool FULL>
+SA_DEV void ew_half(uint32_t tS, uint32_t tDP, uint32_t sL, uint32_t sD, uint32_t rowb, int kr, float sl2, int qh,
+                    int key, int len, const MaskParams& mask) {
+  uint32_t sa[16], da[16];
+  tmem_ld16(tS, sa);
+  tmem_ld16(tDP, da);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    tmem_ld_wait();
+    reg_fence16(sa);
+    reg_fence16(da);
+    uint32_t sc[16], dc[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) sc[e] = sa[e], dc[e] = da[e];
+    if (c + 1 < 4) {
+      tmem_ld16(tS + 16 * (c + 1), sa);
+      tmem_ld16(tDP + 16 * (c + 1), da);
+    }
+    uint32_t pp[8], dd[8];
+    ew_chunk<FULL>(sc, dc, sL + 64 * c, sD + 64 * c, sl2, qh + 16 * c, key, len, mask, pp, dd);
+    // Packed P^T / dS^T of these 16 queries go to 8 columns of this half's
+    // S^T / dP^T columns that this thread has already read.
+    tmem_st8(tS + 8 * c, pp);
+    tmem_st8(tDP + 8 * c, dd);
+    st_shared_v4(rowb + (((2 * c) ^ (kr & 7)) << 4), dd[0], dd[1], dd[2], dd[3]);
+    st_shared_v4(rowb + (((2 * c + 1) ^ (kr & 7)) << 4), dd[4], dd[5], dd[6], dd[7]);
+  }
+}
+
 __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__ BwdTcK p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ Bars bars;
@@ -192,6 +217,9 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x;
+#ifdef SA_BWD_TRACE
+  long long* const trace_p = (blockIdx.x == 0 && blockIdx.y == 0) ? g_bwd_trace : nullptr;
+#endif
   const BwdItem item = p.items[blockIdx.y];  // longest first
   const SeqSpan sp = seq_span(p.cu, p.seqlen, item.b);
   const int k0 = static_cast<int>(item.kt) * BN;
@@ -330,6 +358,7 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
           if (h == 0 && t + 1 < nsteps) {
             if (!(ok = mbar_wait_warp(b_qf((t + 1) % NS), ((t + 1) / NS) & 1, ab))) break;
             fence_after_sync();
+            if (lane == 0) SA_TRACE(1, t, 6);
           }
           // dV += P_h^T dO_h and dK += dS_h^T Q_h, A operands in the S^T / dP^T columns of half h.
           const uint64_t q = sdesc_add(d_q, s * TILE + h * HALF * 128), o = sdesc_add(d_o, s * TILE + h * HALF * 128);
@@ -396,41 +425,29 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
     }
     for (int t = 0; ok && t < nsteps; ++t) {
       const int s = t % NS;
-      if (tid == 128) SA_TRACE(2, t, 0);
+      if (tid == 128 || tid == 256) SA_TRACE(2 + (tid == 256 ? 2 : 0), t, 0);
+      // l' and D of this step (stage s) have almost always landed: test that
+      // first, without blocking, so its latency overlaps the wait for S.
+      const bool q_ready = mbar_test_wait(b_qf(s), (t / NS) & 1);
       ok = mbar_wait_warp(b_s(half), t & 1, ab) &&
-           mbar_wait_warp(b_qf(s), (t / NS) & 1, ab);
+           (__all_sync(0xffffffffu, q_ready) || mbar_wait_warp(b_qf(s), (t / NS) & 1, ab));
       if (!ok) break;
-      if (tid == 128) SA_TRACE(2, t, 1);
+      if (tid == 128 || tid == 256) SA_TRACE(2 + (tid == 256 ? 2 : 0), t, 1);
       fence_after_sync();
       const int qh = step_q0(t) + HALF * half;
       const bool full = block_full(qh, HALF, k0, BN, sp.len, p.mask);
       const uint32_t rowb = sb + OFF_DS + (t & 1) * 2 * TILE + half * TILE + kr * 128;
       const uint32_t sL = sb + OFF_L + (s * BM + HALF * half) * 4, sD = sb + OFF_DL + (s * BM + HALF * half) * 4;
-#pragma unroll 1
-      for (int c = 0; c < HALF / 32; ++c) {
-        uint32_t pp[16], dd[16];
-        if (full)
-          ew_chunk<true>(tS + 32 * c, tDP + 32 * c, sL + 128 * c, sD + 128 * c, sl2, qh + 32 * c, key, sp.len, p.mask,
-                         pp, dd);
-        else
-          ew_chunk<false>(tS + 32 * c, tDP + 32 * c, sL + 128 * c, sD + 128 * c, sl2, qh + 32 * c, key, sp.len,
-                          p.mask, pp, dd);
-        // Packed P^T / dS^T of these 32 queries go to the first 16 columns of
-        // this half's S^T / dP^T columns, which this thread has already read.
-        tmem_st16(tS + 16 * c, pp);
-        tmem_st16(tDP + 16 * c, dd);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int cc = c * 4 + i;
-          st_shared_v4(rowb + ((cc ^ (kr & 7)) << 4), dd[4 * i], dd[4 * i + 1], dd[4 * i + 2], dd[4 * i + 3]);
-        }
-      }
+      if (full)
+        ew_half<true>(tS, tDP, sL, sD, rowb, kr, sl2, qh, key, sp.len, p.mask);
+      else
+        ew_half<false>(tS, tDP, sL, sD, rowb, kr, sl2, qh, key, sp.len, p.mask);
       tmem_st_wait();
       fence_before_sync();
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_p(half));
-      if (tid == 128) SA_TRACE(2, t, 4);
+      if (tid == 128 || tid == 256) SA_TRACE(2 + (tid == 256 ? 2 : 0), t, 4);
     }
     ok = ok && mbar_wait_warp(b_done, 0, ab);
     if (ok) {

@@ -68,11 +68,14 @@ struct Abort {
   int* status;         // global device status word
 };
 
+// The abort word and the clock are checked on every 16th poll only: the
+// shared-memory pipe they use is the one the waiting kernels are short of.
 SA_DEV bool mbar_wait(uint32_t bar, uint32_t parity, const Abort& ab, long long limit = kTimeoutCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  while (true) {
+  for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15) != 0) continue;
     if (*ab.flag) return false;
     if (clock64() - t0 > limit) {
       *ab.flag = 1;
@@ -225,6 +228,16 @@ SA_DEV void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
       : "memory");
 }
 // 16 consecutive 32-bit columns.
+SA_DEV void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      : SA_R8(0), SA_R8(8)
+      : "r"(taddr));
+}
+SA_DEV void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr), SA_W8(0)
+               : "memory");
+}
 SA_DEV void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
@@ -236,6 +249,7 @@ SA_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" :::
 SA_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 // Makes the registers filled by tmem_ld32 depend on the preceding wait, so the
 // compiler cannot move their first use above tcgen05.wait::ld.
+SA_DEV void reg_fence16(uint32_t (&r)[16]) { asm volatile("" : SA_F8(0), SA_F8(8)); }
 SA_DEV void reg_fence32(uint32_t (&r)[32]) {
   asm volatile("" : SA_F8(0), SA_F8(8), SA_F8(16), SA_F8(24));
 }
