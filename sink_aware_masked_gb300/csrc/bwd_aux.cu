@@ -9,9 +9,8 @@
 //   dsink[h] = -sum_rows (1 - alpha) D,   1 - alpha = sigmoid(s_h - l)
 //
 //   bwd_pre   : one pass over O and dO: -D, -l' (log2 units), per-block partial
-//               dsink sums, zeroes the fp32 dQ accumulator.  HBM-bound; many
-//               small blocks and two tokens' loads in flight per iteration
-//               keep enough bytes in flight.
+//               dsink sums, zeroes the fp32 dQ accumulator.  HBM-bound; every
+//               thread issues the loads of four tokens before using them.
 //   dq_convert: dQ = scale * accumulator -> bf16; ceil(Hq / 8) extra blocks
 //               reduce the dsink partials in a fixed order (deterministic),
 //               one warp per head.
@@ -51,54 +50,65 @@ __device__ __forceinline__ float dot8_bf16(const uint4& a, const uint4& b) {
   return s;
 }
 
+// Block = kPreTokens tokens x all heads; thread = (head slot, 16-byte chunk
+// of a 128-byte row).  For each head slot the block walks its tokens in
+// batches of kPreBatch, issuing every load of a batch (O, dO, l) before any
+// arithmetic so that enough bytes are in flight to reach HBM bandwidth.
+constexpr int kPreBatch = 4;
+
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreK p) {
   const int sub = threadIdx.x & 7;   // 16-byte chunk of a 128-byte row
   const int hs = threadIdx.x >> 3;   // 0..31
   const long long t0 = static_cast<long long>(blockIdx.x) * kPreTokens;
   const long long t1 = min(t0 + kPreTokens, p.T);
-  float acc[kMaxHeadsQ / 32];
+  for (int h = hs; h < ((p.hq + 31) & ~31); h += 32) {
+    const bool ok = h < p.hq;
+    const float sk = ok ? __ldg(p.sink + h) : 0.f;
+    float part = 0.f;
+    for (long long tt = t0; tt < t1; tt += kPreBatch) {
+      uint4 ov[kPreBatch], gv[kPreBatch];
+      float lv[kPreBatch];
 #pragma unroll
-  for (int i = 0; i < kMaxHeadsQ / 32; ++i) acc[i] = 0.f;
-#pragma unroll 2
-  for (long long t = t0; t < t1; ++t) {
-#pragma unroll
-    for (int hi = 0; hi < kMaxHeadsQ / 32; ++hi) {
-      if (hi * 32 >= p.hq) break;
-      const int h = hi * 32 + hs;
-      const bool ok = h < p.hq;
-      float dot = 0.f;
-      if (ok) {
-        const size_t base = (static_cast<size_t>(t) * p.hq + h) * D + sub * 8;
-        const uint4 ov = __ldg(reinterpret_cast<const uint4*>(p.o + base));
-        const uint4 gv = __ldg(reinterpret_cast<const uint4*>(p.dout + base));
-        dot = dot8_bf16(ov, gv);
-        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-        reinterpret_cast<float4*>(p.dq_accum + base)[0] = z;
-        reinterpret_cast<float4*>(p.dq_accum + base)[1] = z;
+      for (int u = 0; u < kPreBatch; ++u) {
+        const long long t = tt + u;
+        const bool v = ok && t < t1;
+        const size_t base = (static_cast<size_t>(v ? t : t0) * p.hq + (ok ? h : 0)) * D + sub * 8;
+        ov[u] = v ? __ldg(reinterpret_cast<const uint4*>(p.o + base)) : make_uint4(0, 0, 0, 0);
+        gv[u] = v ? __ldg(reinterpret_cast<const uint4*>(p.dout + base)) : make_uint4(0, 0, 0, 0);
+        lv[u] = (v && sub == 0) ? __ldg(p.lse + static_cast<size_t>(h) * p.T + t) : 0.f;
       }
-      dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-      dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-      dot += __shfl_xor_sync(0xffffffffu, dot, 4);
-      if (ok && sub == 0) {
-        const size_t idx = static_cast<size_t>(h) * p.T + t;
-        const float l = p.lse[idx];
-        const float x = __ldg(p.sink + h) - l;
-        const float softplus = fmaxf(x, 0.f) + log1pf(__expf(-fabsf(x)));
-        // Stored negated so the main kernel's element-wise pass is two packed
-        // f32x2 operations per pair: exp2(s * c + (-l')) and dP + (-D).
-        p.lse_log2[idx] = -(l + softplus) * kLog2e;
-        p.delta[idx] = -dot;
-        const float one_minus_alpha = 1.f / (1.f + __expf(-x));
-        acc[hi] -= one_minus_alpha * dot;
+#pragma unroll
+      for (int u = 0; u < kPreBatch; ++u) {
+        const long long t = tt + u;
+        if (ok && t < t1) {
+          const size_t base = (static_cast<size_t>(t) * p.hq + h) * D + sub * 8;
+          const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+          reinterpret_cast<float4*>(p.dq_accum + base)[0] = z;
+          reinterpret_cast<float4*>(p.dq_accum + base)[1] = z;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kPreBatch; ++u) {
+        const long long t = tt + u;
+        float dot = dot8_bf16(ov[u], gv[u]);
+        dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+        dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+        dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+        if (ok && sub == 0 && t < t1) {
+          const size_t idx = static_cast<size_t>(h) * p.T + t;
+          const float l = lv[u];
+          const float x = sk - l;
+          const float softplus = fmaxf(x, 0.f) + log1pf(__expf(-fabsf(x)));
+          // Stored negated so the main kernel's element-wise pass is two
+          // packed f32x2 operations per pair: exp2(s * c + (-l')) and dP + (-D).
+          p.lse_log2[idx] = -(l + softplus) * kLog2e;
+          p.delta[idx] = -dot;
+          const float one_minus_alpha = 1.f / (1.f + __expf(-x));
+          part -= one_minus_alpha * dot;
+        }
       }
     }
-  }
-  if (sub == 0) {
-#pragma unroll
-    for (int hi = 0; hi < kMaxHeadsQ / 32; ++hi) {
-      const int h = hi * 32 + hs;
-      if (h < p.hq) p.dsink_part[static_cast<size_t>(blockIdx.x) * p.hq + h] = acc[hi];
-    }
+    if (ok && sub == 0) p.dsink_part[static_cast<size_t>(blockIdx.x) * p.hq + h] = part;
   }
 }
 
@@ -135,17 +145,26 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const ConvK p) {
     if (lane == 0) p.dsink[h] = s;
     return;
   }
+  // Two groups of 8 accumulator values per thread in flight, read with
+  // streaming loads (the accumulator is dead after this pass).
   const long long stride = static_cast<long long>(conv_blocks) * blockDim.x;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.n8; i += stride) {
-    const float4 a = reinterpret_cast<const float4*>(p.acc)[2 * i];
-    const float4 c = reinterpret_cast<const float4*>(p.acc)[2 * i + 1];
+  auto emit = [&](long long i, const float4& a, const float4& c) {
     uint4 o;
     o.x = pack_bf16(a.x * p.scale, a.y * p.scale);
     o.y = pack_bf16(a.z * p.scale, a.w * p.scale);
     o.z = pack_bf16(c.x * p.scale, c.y * p.scale);
     o.w = pack_bf16(c.z * p.scale, c.w * p.scale);
     reinterpret_cast<uint4*>(p.dq)[i] = o;
+  };
+  const float4* acc4 = reinterpret_cast<const float4*>(p.acc);
+  long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + stride < p.n8; i += 2 * stride) {
+    const float4 a0 = __ldcs(acc4 + 2 * i), c0 = __ldcs(acc4 + 2 * i + 1);
+    const float4 a1 = __ldcs(acc4 + 2 * (i + stride)), c1 = __ldcs(acc4 + 2 * (i + stride) + 1);
+    emit(i, a0, c0);
+    emit(i + stride, a1, c1);
   }
+  if (i < p.n8) emit(i, __ldcs(acc4 + 2 * i), __ldcs(acc4 + 2 * i + 1));
 }
 
 }  // namespace
