@@ -138,22 +138,6 @@ SA_DEV float ex2(float x) {
   return y;
 }
 
-// 2^x on the FMA pipe (frees the MUFU unit for the other exponentials).
-// x = j + f with j = round(x) taken from the low mantissa bits of x + 1.5*2^23
-// and f in [-0.5, 0.5]; 2^f is a degree-3 polynomial fitted for relative
-// error 7.5e-5 on that interval (fit_exp2_poly.py); 2^j is added to the
-// exponent field.  x is clamped to >= -125 so the result stays a normal
-// number (masked scores, x = -inf, give 2^-125, which is zero to every
-// bf16/fp32 sum they enter).  Valid for x <= 127.
-SA_DEV float exp2_fma(float x) {
-  x = fmaxf(x, -125.f);
-  const float t = x + 12582912.f;
-  const float j = t - 12582912.f;
-  const float f = x - j;
-  const float p = fmaf(fmaf(fmaf(0.0551716648f, f, 0.242611125f), f, 0.693260968f), f, 0.999928057f);
-  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
-}
-
 // Three-input maximum (sm_100 family).
 SA_DEV float fmax3(float a, float b, float c) {
   float r;
@@ -183,23 +167,6 @@ SA_DEV float2 fmul2(float2 a, float2 b) {
       : "=l"(d)
       : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
   return *reinterpret_cast<float2*>(&d);
-}
-
-// exp2_fma on a pair: the same range reduction and polynomial, with the
-// additions and the Horner steps in packed f32x2 form (6 instructions per
-// element instead of 9).
-SA_DEV float2 exp2_fma2(float2 x) {
-  x.x = fmaxf(x.x, -125.f);
-  x.y = fmaxf(x.y, -125.f);
-  const float2 big = make_float2(12582912.f, 12582912.f);
-  const float2 t = fadd2(x, big);
-  const float2 j = fadd2(t, make_float2(-12582912.f, -12582912.f));
-  const float2 f = ffma2(j, make_float2(-1.f, -1.f), x);
-  float2 p = ffma2(make_float2(0.0551716648f, 0.0551716648f), f, make_float2(0.242611125f, 0.242611125f));
-  p = ffma2(p, f, make_float2(0.693260968f, 0.693260968f));
-  p = ffma2(p, f, make_float2(0.999928057f, 0.999928057f));
-  return make_float2(__int_as_float(__float_as_int(p.x) + (__float_as_int(t.x) << 23)),
-                     __int_as_float(__float_as_int(p.y) + (__float_as_int(t.y) << 23)));
 }
 
 // Offset in bytes of 16-byte chunk `c` (0..7) of row `r` in a tile whose rows
