@@ -69,7 +69,7 @@ using namespace tc;
 constexpr int D = kHeadDim;
 constexpr int BN = 128;  // keys per CTA (TMEM lanes)
 constexpr int BM = 128;  // query rows per step
-constexpr int NS = 2;    // Q/dO stages
+constexpr int NS = 3;    // Q/dO (and l', D) stages
 constexpr int NTHR = 512;
 // setmaxnreg split of the 512 x 128 launch registers: 128 x 56 (loader/MMA
 // warpgroup) + 256 x 168 (two element-wise warpgroups) + 128 x 96 (dQ drain)
@@ -81,8 +81,8 @@ constexpr int OFF_V = OFF_K + TILE;
 constexpr int OFF_Q = OFF_V + TILE;
 constexpr int OFF_DO = OFF_Q + NS * TILE;
 constexpr int OFF_DS = OFF_DO + NS * TILE;     // 2 buffers x 32 KB
-constexpr int OFF_STG = OFF_DS + 2 * 2 * TILE;  // 32 KB fp32 dQ staging
-constexpr int OFF_L = OFF_STG + 2 * TILE;
+constexpr int OFF_STG = OFF_DS + 2 * 2 * TILE;  // 16 KB fp32 dQ staging (32 of the 64 columns at a time)
+constexpr int OFF_L = OFF_STG + TILE;
 constexpr int OFF_DL = OFF_L + NS * BM * 4;
 constexpr int SMEM_DYN = OFF_DL + NS * BM * 4 + 1024;
 
@@ -116,7 +116,8 @@ static_assert(sizeof(BwdTcK) < 32000, "kernel parameter block too large");
 struct Bars {
   uint64_t kv_full, kv_tmem;
   uint64_t q_full[NS], q_empty[NS];
-  uint64_t s_full[2], p_full[2];
+  uint64_t s_full[2], dp_full[2];   // per half: S^T / dP^T of the step ready
+  uint64_t pt_full[2], ds_full[2];  // per half: packed P^T / dS^T written by the element-wise warps
   uint64_t dq_full, dq_free, kv_done, drain;
 };
 
@@ -143,66 +144,78 @@ SA_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-// One 16-column chunk of the element-wise step for this thread's key row:
-// P^T = exp2(S^T * scale * log2(e) - l'), dS^T = P^T (dP^T - D), packed to bf16
-// pairs.  The preprocess stored -l' (log2 units) and -D, so each pair of
-// columns costs one f32x2 FMA, one f32x2 add and one f32x2 multiply.  FULL
-// skips the mask predicate (every pair of the tile visible).
+// The element-wise pass over one half step (64 queries) for this thread's
+// key row, in four 16-column chunks; the Tensor Memory loads of the next
+// chunk are issued before the current one is computed.  The preprocess
+// stored -l' (log2 units) and -D, so each pair of columns costs one f32x2
+// FMA (phase 1) and one f32x2 add and multiply (phase 2).
+//
+// Phase 1: P^T = exp2(S^T * scale * log2(e) - l'), masked on partial tiles
+// (FULL skips the predicate); packed P^T overwrites the S^T columns already
+// read; fp32 P stays in registers for phase 2.
 template <bool FULL>
-SA_DEV void ew_chunk(const uint32_t (&sr)[16], const uint32_t (&dr)[16], uint32_t sL, uint32_t sD, float sl2, int qb,
-                     int key, int len, const MaskParams& mask, uint32_t (&pp)[8], uint32_t (&dd)[8]) {
-  // sr, dr: S^T and dP^T of 16 queries; sL, sD: shared address of their -l'
-  // and -D values; qb: position of the first query.
+SA_DEV void ew_phase1(uint32_t tS, uint32_t sL, float sl2, int qh, int key, int len, const MaskParams& mask,
+                      float (&pv)[4][16]) {
   const float2 sl2x2 = make_float2(sl2, sl2);
-#pragma unroll
-  for (int e = 0; e < 16; e += 4) {
-    const float4 l4 = ld_shared_f4(sL + e * 4);
-    const float4 d4 = ld_shared_f4(sD + e * 4);
-#pragma unroll
-    for (int u = 0; u < 4; u += 2) {
-      const float2 x = ffma2(make_float2(__uint_as_float(sr[e + u]), __uint_as_float(sr[e + u + 1])), sl2x2,
-                             u ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y));
-      float2 pe = make_float2(ex2(x.x), ex2(x.y));
-      const float2 t = fadd2(make_float2(__uint_as_float(dr[e + u]), __uint_as_float(dr[e + u + 1])),
-                             u ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y));
-      float2 de = fmul2(pe, t);
-      if (!FULL) {
-        const int q = qb + e + u;
-        if (!(q < len && visible(q, key, len, mask))) pe.x = de.x = 0.f;
-        if (!(q + 1 < len && visible(q + 1, key, len, mask))) pe.y = de.y = 0.f;
-      }
-      pp[(e + u) >> 1] = pack_bf16(pe.x, pe.y);
-      dd[(e + u) >> 1] = pack_bf16(de.x, de.y);
-    }
-  }
-}
-
-// The element-wise pass over one half step (64 queries) in four 16-column
-// chunks; the Tensor Memory loads of the next chunk are issued before the
-// current one is computed, so their latency overlaps the arithmetic.
-template <bool FULL>
-SA_DEV void ew_half(uint32_t tS, uint32_t tDP, uint32_t sL, uint32_t sD, uint32_t rowb, int kr, float sl2, int qh,
-                    int key, int len, const MaskParams& mask) {
-  uint32_t sa[16], da[16];
+  uint32_t sa[16];
   tmem_ld16(tS, sa);
-  tmem_ld16(tDP, da);
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     tmem_ld_wait();
     reg_fence16(sa);
-    reg_fence16(da);
-    uint32_t sc[16], dc[16];
+    uint32_t sc[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) sc[e] = sa[e], dc[e] = da[e];
-    if (c + 1 < 4) {
-      tmem_ld16(tS + 16 * (c + 1), sa);
-      tmem_ld16(tDP + 16 * (c + 1), da);
+    for (int e = 0; e < 16; ++e) sc[e] = sa[e];
+    if (c + 1 < 4) tmem_ld16(tS + 16 * (c + 1), sa);
+    uint32_t pp[8];
+#pragma unroll
+    for (int e = 0; e < 16; e += 4) {
+      const float4 l4 = ld_shared_f4(sL + 64 * c + e * 4);
+#pragma unroll
+      for (int u = 0; u < 4; u += 2) {
+        const float2 x = ffma2(make_float2(__uint_as_float(sc[e + u]), __uint_as_float(sc[e + u + 1])), sl2x2,
+                               u ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y));
+        float2 pe = make_float2(ex2(x.x), ex2(x.y));
+        if (!FULL) {
+          const int q = qh + 16 * c + e + u;
+          if (!(q < len && visible(q, key, len, mask))) pe.x = 0.f;
+          if (!(q + 1 < len && visible(q + 1, key, len, mask))) pe.y = 0.f;
+        }
+        pv[c][e + u] = pe.x;
+        pv[c][e + u + 1] = pe.y;
+        pp[(e + u) >> 1] = pack_bf16(pe.x, pe.y);
+      }
     }
-    uint32_t pp[8], dd[8];
-    ew_chunk<FULL>(sc, dc, sL + 64 * c, sD + 64 * c, sl2, qh + 16 * c, key, len, mask, pp, dd);
-    // Packed P^T / dS^T of these 16 queries go to 8 columns of this half's
-    // S^T / dP^T columns that this thread has already read.
     tmem_st8(tS + 8 * c, pp);
+  }
+}
+
+// Phase 2: dS^T = P^T (dP^T - D), packed over the dP^T columns already
+// read and into this key row of the shared dS^T tile (128-byte swizzle) for
+// the dQ product.  Masked entries have P = 0 and so dS = 0.
+SA_DEV void ew_phase2(uint32_t tDP, uint32_t sD, uint32_t rowb, int kr, const float (&pv)[4][16]) {
+  uint32_t da[16];
+  tmem_ld16(tDP, da);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    tmem_ld_wait();
+    reg_fence16(da);
+    uint32_t dc[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) dc[e] = da[e];
+    if (c + 1 < 4) tmem_ld16(tDP + 16 * (c + 1), da);
+    uint32_t dd[8];
+#pragma unroll
+    for (int e = 0; e < 16; e += 4) {
+      const float4 d4 = ld_shared_f4(sD + 64 * c + e * 4);
+#pragma unroll
+      for (int u = 0; u < 4; u += 2) {
+        const float2 t = fadd2(make_float2(__uint_as_float(dc[e + u]), __uint_as_float(dc[e + u + 1])),
+                               u ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y));
+        const float2 de = fmul2(make_float2(pv[c][e + u], pv[c][e + u + 1]), t);
+        dd[(e + u) >> 1] = pack_bf16(de.x, de.y);
+      }
+    }
     tmem_st8(tDP + 8 * c, dd);
     st_shared_v4(rowb + (((2 * c) ^ (kr & 7)) << 4), dd[0], dd[1], dd[2], dd[3]);
     st_shared_v4(rowb + (((2 * c + 1) ^ (kr & 7)) << 4), dd[4], dd[5], dd[6], dd[7]);
@@ -242,7 +255,9 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
   const uint32_t b_kv = smem_u32(&bars.kv_full), b_kvt = smem_u32(&bars.kv_tmem);
   const uint32_t b_dqf = smem_u32(&bars.dq_full), b_dqe = smem_u32(&bars.dq_free);
   auto b_s = [&](int h) { return smem_u32(&bars.s_full[h]); };
-  auto b_p = [&](int h) { return smem_u32(&bars.p_full[h]); };
+  auto b_dp = [&](int h) { return smem_u32(&bars.dp_full[h]); };
+  auto b_pt = [&](int h) { return smem_u32(&bars.pt_full[h]); };
+  auto b_ds = [&](int h) { return smem_u32(&bars.ds_full[h]); };
   const uint32_t b_done = smem_u32(&bars.kv_done), b_dr = smem_u32(&bars.drain);
   auto b_qf = [&](int s) { return smem_u32(&bars.q_full[s]); };
   auto b_qe = [&](int s) { return smem_u32(&bars.q_empty[s]); };
@@ -257,7 +272,9 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
     mbar_init(b_kvt, 8);
     for (int h = 0; h < 2; ++h) {
       mbar_init(b_s(h), 1);
-      mbar_init(b_p(h), 4);
+      mbar_init(b_dp(h), 1);
+      mbar_init(b_pt(h), 4);
+      mbar_init(b_ds(h), 4);
     }
     mbar_init(b_dqf, 1);
     mbar_init(b_dqe, 4);
@@ -330,53 +347,75 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
       const uint64_t d_q = sdesc_sw128(sb + OFF_Q, 16, 1024);    // stage s: + s * TILE, half h: + h * 8 KB
       const uint64_t d_o = sdesc_sw128(sb + OFF_DO, 16, 1024);
       const uint64_t d_dsm = sdesc_sw128(sb + OFF_DS, TILE, 1024);  // MN-major A of dQ (two 64-query blocks)
-      auto issue_s_dp = [&](int h, int s) {
-        const uint64_t q = sdesc_add(d_q, s * TILE + h * HALF * 128), o = sdesc_add(d_o, s * TILE + h * HALF * 128);
+      // S_h^T = K Q_h^T and dP_h^T = V dO_h^T of the step held in stage s
+      // (A = K or V in Tensor Memory, B = the half's 64 query rows, K-major).
+      auto issue_s = [&](int h, int s) {
+        const uint64_t q = sdesc_add(d_q, s * TILE + h * HALF * 128);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          if (leader) {
-            mma_ts(tmem + TM_S + HALF * h, tmem + TM_K + kk * 8, sdesc_add(q, kk * 32), id_s, kk > 0);
-            mma_ts(tmem + TM_DP + HALF * h, tmem + TM_V + kk * 8, sdesc_add(o, kk * 32), id_s, kk > 0);
-          }
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          if (leader) mma_ts(tmem + TM_S + HALF * h, tmem + TM_K + kk * 8, sdesc_add(q, kk * 32), id_s, kk > 0);
+      };
+      auto issue_dp = [&](int h, int s) {
+        const uint64_t o = sdesc_add(d_o, s * TILE + h * HALF * 128);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          if (leader) mma_ts(tmem + TM_DP + HALF * h, tmem + TM_V + kk * 8, sdesc_add(o, kk * 32), id_s, kk > 0);
       };
       bool ok = mbar_wait_warp(b_kvt, 0, ab) && mbar_wait_warp(b_qf(0), 0, ab);
       if (ok) {
         fence_after_sync();
         for (int h = 0; h < 2; ++h) {
-          issue_s_dp(h, 0);
+          issue_s(h, 0);
           if (leader) mma_commit(b_s(h));
+        }
+        for (int h = 0; h < 2; ++h) {
+          issue_dp(h, 0);
+          if (leader) mma_commit(b_dp(h));
         }
       }
       for (int t = 0; ok && t < nsteps; ++t) {
         const int s = t % NS, db = t & 1;
+        const bool more = t + 1 < nsteps;
         if (lane == 0) SA_TRACE(1, t, 0);
+        // Phase 1 of each half is done (packed P^T in the S^T columns):
+        // dV += P_h^T dO_h, then the next step's S_h^T over those columns
+        // (the tensor core runs MMAs in issue order).
         for (int h = 0; h < 2 && ok; ++h) {
-          if (!(ok = mbar_wait_warp(b_p(h), t & 1, ab))) break;
-          if (lane == 0) SA_TRACE(1, t, 1 + 2 * h);
+          if (!(ok = mbar_wait_warp(b_pt(h), t & 1, ab))) break;
+          if (lane == 0) SA_TRACE(1, t, 1 + h);
           fence_after_sync();
-          if (h == 0 && t + 1 < nsteps) {
-            if (!(ok = mbar_wait_warp(b_qf((t + 1) % NS), ((t + 1) / NS) & 1, ab))) break;
-            fence_after_sync();
-            if (lane == 0) SA_TRACE(1, t, 6);
-          }
-          // dV += P_h^T dO_h and dK += dS_h^T Q_h, A operands in the S^T / dP^T columns of half h.
-          const uint64_t q = sdesc_add(d_q, s * TILE + h * HALF * 128), o = sdesc_add(d_o, s * TILE + h * HALF * 128);
+          const uint64_t o = sdesc_add(d_o, s * TILE + h * HALF * 128);
 #pragma unroll
-          for (int kk = 0; kk < HALF / 16; ++kk) {
-            const uint32_t acc = (t > 0 || h > 0 || kk > 0) ? 1u : 0u;
-            if (leader) {
-              mma_ts(tmem + TM_DV, tmem + TM_S + HALF * h + kk * 8, sdesc_add(o, kk * 2048), id_kv, acc);
-              mma_ts(tmem + TM_DK, tmem + TM_DP + HALF * h + kk * 8, sdesc_add(q, kk * 2048), id_kv, acc);
+          for (int kk = 0; kk < HALF / 16; ++kk)
+            if (leader)
+              mma_ts(tmem + TM_DV, tmem + TM_S + HALF * h + kk * 8, sdesc_add(o, kk * 2048), id_kv,
+                     (t > 0 || h > 0 || kk > 0) ? 1u : 0u);
+          if (more) {
+            if (h == 0) {
+              if (!(ok = mbar_wait_warp(b_qf((t + 1) % NS), ((t + 1) / NS) & 1, ab))) break;
+              fence_after_sync();
             }
-          }
-          // The next step's S^T and dP^T of this half overwrite those columns;
-          // the tensor core runs MMAs in issue order.
-          if (t + 1 < nsteps) {
-            issue_s_dp(h, (t + 1) % NS);
+            issue_s(h, (t + 1) % NS);
             if (leader) mma_commit(b_s(h));
           }
-          if (lane == 0) SA_TRACE(1, t, 2 + 2 * h);
+        }
+        if (!ok) break;
+        // Phase 2 of each half is done (packed dS^T in the dP^T columns):
+        // dK += dS_h^T Q_h, then the next step's dP_h^T over those columns.
+        for (int h = 0; h < 2 && ok; ++h) {
+          if (!(ok = mbar_wait_warp(b_ds(h), t & 1, ab))) break;
+          if (lane == 0) SA_TRACE(1, t, 3 + h);
+          fence_after_sync();
+          const uint64_t q = sdesc_add(d_q, s * TILE + h * HALF * 128);
+#pragma unroll
+          for (int kk = 0; kk < HALF / 16; ++kk)
+            if (leader)
+              mma_ts(tmem + TM_DK, tmem + TM_DP + HALF * h + kk * 8, sdesc_add(q, kk * 2048), id_kv,
+                     (t > 0 || h > 0 || kk > 0) ? 1u : 0u);
+          if (more) {
+            issue_dp(h, (t + 1) % NS);
+            if (leader) mma_commit(b_dp(h));
+          }
         }
         if (!ok) break;
         if (leader) mma_commit(b_qe(s));  // Q(t), dO(t), l'(t), D(t) have no later reader
@@ -438,15 +477,24 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
       const bool full = block_full(qh, HALF, k0, BN, sp.len, p.mask);
       const uint32_t rowb = sb + OFF_DS + (t & 1) * 2 * TILE + half * TILE + kr * 128;
       const uint32_t sL = sb + OFF_L + (s * BM + HALF * half) * 4, sD = sb + OFF_DL + (s * BM + HALF * half) * 4;
+      float pv[4][16];
       if (full)
-        ew_half<true>(tS, tDP, sL, sD, rowb, kr, sl2, qh, key, sp.len, p.mask);
+        ew_phase1<true>(tS, sL, sl2, qh, key, sp.len, p.mask, pv);
       else
-        ew_half<false>(tS, tDP, sL, sD, rowb, kr, sl2, qh, key, sp.len, p.mask);
+        ew_phase1<false>(tS, sL, sl2, qh, key, sp.len, p.mask, pv);
+      tmem_st_wait();
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_pt(half));
+      if (tid == 128 || tid == 256) SA_TRACE(2 + (tid == 256 ? 2 : 0), t, 2);
+      if (!(ok = mbar_wait_warp(b_dp(half), t & 1, ab))) break;
+      fence_after_sync();
+      ew_phase2(tDP, sD, rowb, kr, pv);
       tmem_st_wait();
       fence_before_sync();
       fence_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(b_p(half));
+      if (lane == 0) mbar_arrive(b_ds(half));
       if (tid == 128 || tid == 256) SA_TRACE(2 + (tid == 256 ? 2 : 0), t, 4);
     }
     ok = ok && mbar_wait_warp(b_done, 0, ab);
@@ -517,19 +565,31 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
       if (leader) bulk_wait_read0();
       if (leader) SA_TRACE(3, t, 2);
       named_sync(1, 128);
+      // Columns 0-31, then 32-63, through the one 16 KB staging tile.
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const uint32_t sw = ((i ^ (qr & 7)) << 4) + qr * 128;
         st_shared_v4(stg + sw, valid ? a[4 * i] : 0u, valid ? a[4 * i + 1] : 0u, valid ? a[4 * i + 2] : 0u,
                      valid ? a[4 * i + 3] : 0u);
-        st_shared_v4(stg + TILE + sw, valid ? b2[4 * i] : 0u, valid ? b2[4 * i + 1] : 0u,
-                     valid ? b2[4 * i + 2] : 0u, valid ? b2[4 * i + 3] : 0u);
       }
       fence_async_smem();
       named_sync(1, 128);
       if (leader) {
         tma_reduce_add_2d(&p.tm_dq, h * D, sp.start + q0, stg);
-        tma_reduce_add_2d(&p.tm_dq, h * D + 32, sp.start + q0, stg + TILE);
+        bulk_commit();
+        bulk_wait_read0();
+      }
+      named_sync(1, 128);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t sw = ((i ^ (qr & 7)) << 4) + qr * 128;
+        st_shared_v4(stg + sw, valid ? b2[4 * i] : 0u, valid ? b2[4 * i + 1] : 0u, valid ? b2[4 * i + 2] : 0u,
+                     valid ? b2[4 * i + 3] : 0u);
+      }
+      fence_async_smem();
+      named_sync(1, 128);
+      if (leader) {
+        tma_reduce_add_2d(&p.tm_dq, h * D + 32, sp.start + q0, stg);
         bulk_commit();
         SA_TRACE(3, t, 3);
       }
