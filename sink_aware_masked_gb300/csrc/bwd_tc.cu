@@ -18,24 +18,31 @@
 // element-wise warpgroup, so the tensor core works on one half while the
 // other half's element-wise pass runs.
 // Warp roles (16 warps, four warpgroups):
-//   warp 0      loader: K, V once; per step Q and dO tiles by TMA (2-stage
+//   warp 0      loader: K, V once; per step Q and dO tiles by TMA (3-stage
 //               ring) and the 128 l' and D values of the query tile by
 //               cp.async, all completing on the stage's full barrier.
 //   warp 1      MMA issuer and TMEM owner (whole warp, one elected lane
-//               issues).  Per half h of step t:
-//                 dV += P_h^T dO_h, dK += dS_h^T Q_h   (A in TMEM, B MN-major)
-//                 S_h^T(t+1) = K Q_h^T, dP_h^T(t+1) = V dO_h^T   (A = K, V in TMEM)
-//               then for the whole step dQ(t) = dS(t) K (A = dS^T tile in
+//               issues).  Per half h of step t, as the element-wise warps
+//               hand their results over:
+//                 P_h^T ready : dV += P_h^T dO_h, then S_h^T(t+1) = K Q_h^T
+//                 dS_h^T ready: dK += dS_h^T Q_h, then dP_h^T(t+1) = V dO_h^T
+//               (A = P^T / dS^T / K / V in TMEM, B from shared memory; the
+//               next step's S^T and dP^T overwrite the columns the
+//               preceding MMA read, which the tensor core runs first), then
+//               for the whole step dQ(t) = dS(t) K (A = the dS^T tile in
 //               shared memory read MN-major, B = K MN-major).
 //   warps 4-7   element-wise for half A, warps 8-11 for half B; thread = key
-//               row.  P^T and dS^T (packed bf16) overwrite the S^T and dP^T
-//               columns they were computed from; dS^T also goes to a
-//               double-buffered 128 x 128 bf16 shared tile (128-byte
-//               swizzle) for the dQ product.  At start they copy K and V
-//               into TMEM; at the end one warpgroup writes dV, the other dK.
-//               Fully visible tiles take a path without the mask predicate.
+//               row.  Phase 1: P^T = exp(S^T - l'), packed over the S^T
+//               columns just read, then signalled, so dV and the next S^T
+//               run while phase 2 computes dS^T = P^T (dP^T - D), packed
+//               over the dP^T columns and into a double-buffered 128 x 128
+//               bf16 shared tile (128-byte swizzle) for the dQ product.
+//               At start they copy K and V into TMEM; at the end one
+//               warpgroup writes dV, the other dK.  Fully visible tiles
+//               take a path without the mask predicate.
 //   warps 12-15 dQ drain: thread = query row; TMEM -> swizzled fp32 staging
-//               tile -> TMA reduce-add into the fp32 dQ accumulator.
+//               tile (32 columns at a time) -> TMA reduce-add into the fp32
+//               dQ accumulator.
 // Tensor Memory (512 columns): S^T A|B (64 each) | dP^T A|B (64 each) |
 // dV 64 | dK 64 | dQ 64 | K 32 | V 32 (bf16 pairs).
 // Every mbarrier wait is bounded; a timeout raises the status word and all
@@ -145,8 +152,9 @@ SA_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint
 }
 
 // The element-wise pass over one half step (64 queries) for this thread's
-// key row, in four 16-column chunks; the Tensor Memory loads of the next
-// chunk are issued before the current one is computed.  The preprocess
+// key row, in four 16-column chunks whose Tensor Memory loads are all issued
+// before the first wait (the whole phase's arithmetic is then independent
+// work for the scheduler).  The preprocess
 // stored -l' (log2 units) and -D, so each pair of columns costs one f32x2
 // FMA (phase 1) and one f32x2 add and multiply (phase 2).
 //
@@ -157,16 +165,15 @@ template <bool FULL>
 SA_DEV void ew_phase1(uint32_t tS, uint32_t sL, float sl2, int qh, int key, int len, const MaskParams& mask,
                       float (&pv)[4][16]) {
   const float2 sl2x2 = make_float2(sl2, sl2);
-  uint32_t sa[16];
-  tmem_ld16(tS, sa);
+  uint32_t sr[4][16];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) tmem_ld16(tS + 16 * c, sr[c]);
+  tmem_ld_wait();
+#pragma unroll
+  for (int c = 0; c < 4; ++c) reg_fence16(sr[c]);
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    tmem_ld_wait();
-    reg_fence16(sa);
-    uint32_t sc[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) sc[e] = sa[e];
-    if (c + 1 < 4) tmem_ld16(tS + 16 * (c + 1), sa);
+    const uint32_t (&sc)[16] = sr[c];
     uint32_t pp[8];
 #pragma unroll
     for (int e = 0; e < 16; e += 4) {
@@ -194,16 +201,15 @@ SA_DEV void ew_phase1(uint32_t tS, uint32_t sL, float sl2, int qh, int key, int 
 // read and into this key row of the shared dS^T tile (128-byte swizzle) for
 // the dQ product.  Masked entries have P = 0 and so dS = 0.
 SA_DEV void ew_phase2(uint32_t tDP, uint32_t sD, uint32_t rowb, int kr, const float (&pv)[4][16]) {
-  uint32_t da[16];
-  tmem_ld16(tDP, da);
+  uint32_t dr[4][16];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) tmem_ld16(tDP + 16 * c, dr[c]);
+  tmem_ld_wait();
+#pragma unroll
+  for (int c = 0; c < 4; ++c) reg_fence16(dr[c]);
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    tmem_ld_wait();
-    reg_fence16(da);
-    uint32_t dc[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) dc[e] = da[e];
-    if (c + 1 < 4) tmem_ld16(tDP + 16 * (c + 1), da);
+    const uint32_t (&dc)[16] = dr[c];
     uint32_t dd[8];
 #pragma unroll
     for (int e = 0; e < 16; e += 4) {
