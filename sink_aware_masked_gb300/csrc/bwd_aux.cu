@@ -8,9 +8,11 @@
 //   D   = <dO, O>                      O is the final, alpha-scaled output
 //   dsink[h] = -sum_rows (1 - alpha) D,   1 - alpha = sigmoid(s_h - l)
 //
-//   bwd_pre   : one pass over O and dO: -D, -l' (log2 units), per-block partial
-//               dsink sums, zeroes the fp32 dQ accumulator.  HBM-bound; every
-//               thread issues the loads of four tokens before using them.
+//   bwd_pre   : one pass over O and dO: the bias rows (-l'/scale and -D as
+//               bf16 hi/mid/lo triples) the main kernel folds into its S^T and
+//               dP^T MMAs, per-block partial dsink sums, zeroes the fp32 dQ
+//               accumulator.  HBM-bound; every thread issues the loads of four
+//               tokens before using them.
 //   dq_convert: dQ = scale * accumulator -> bf16; ceil(Hq / 8) extra blocks
 //               reduce the dsink partials in a fixed order (deterministic),
 //               one warp per head.
@@ -28,12 +30,12 @@ struct PreK {
   const __nv_bfloat16* dout;
   const float* lse;
   const float* sink;
-  float* delta;
-  float* lse_log2;
+  uint4* bias;
   float* dq_accum;
   float* dsink_part;
   long long T;
   int hq;
+  float scale;
 };
 
 __device__ __forceinline__ float dot8_bf16(const uint4& a, const uint4& b) {
@@ -55,6 +57,17 @@ __device__ __forceinline__ float dot8_bf16(const uint4& a, const uint4& b) {
 // batches of kPreBatch, issuing every load of a batch (O, dO, l) before any
 // arithmetic so that enough bytes are in flight to reach HBM bandwidth.
 constexpr int kPreBatch = 4;
+
+// v as hi + mid + lo, three round-to-nearest bf16 values (the remainder of
+// each step is exact in fp32): about 24 significant bits in total.
+__device__ __forceinline__ void split3_bf16(float v, uint16_t (&out)[3]) {
+#pragma unroll
+  for (int i = 0; i < 3; ++i) {
+    const __nv_bfloat16 b = __float2bfloat16_rn(v);
+    out[i] = __bfloat16_as_ushort(b);
+    v -= __bfloat162float(b);
+  }
+}
 
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreK p) {
   const int sub = threadIdx.x & 7;   // 16-byte chunk of a 128-byte row
@@ -99,10 +112,20 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreK p) {
           const float l = lv[u];
           const float x = sk - l;
           const float softplus = fmaxf(x, 0.f) + log1pf(__expf(-fabsf(x)));
-          // Stored negated so the main kernel's element-wise pass is two
-          // packed f32x2 operations per pair: exp2(s * c + (-l')) and dP + (-D).
-          p.lse_log2[idx] = -(l + softplus) * kLog2e;
-          p.delta[idx] = -dot;
+          // -l'/scale and -D as three bf16 summands each: the main kernel
+          // adds them to S^T and dP^T with one K=16 MMA (a 0/1 selector times
+          // these rows), so its element-wise pass reads neither from shared
+          // memory; three terms keep about 24 bits of each value.
+          // Clamped finite (sink = +inf gives l' = +inf): exp2 of the biased
+          // score still underflows to exactly 0, and the selector's zeros
+          // times these entries stay 0 instead of NaN.
+          uint16_t lb[3], db[3];
+          split3_bf16(fminf(fmaxf(-(l + softplus) / p.scale, -1e30f), 1e30f), lb);
+          split3_bf16(fminf(fmaxf(-dot, -1e30f), 1e30f), db);
+          // Row [l_hi, l_mid, l_lo, d_hi, d_mid, d_lo, 0, 0].
+          p.bias[idx] = make_uint4(lb[0] | (static_cast<uint32_t>(lb[1]) << 16),
+                                   lb[2] | (static_cast<uint32_t>(db[0]) << 16),
+                                   db[1] | (static_cast<uint32_t>(db[2]) << 16), 0u);
           const float one_minus_alpha = 1.f / (1.f + __expf(-x));
           part -= one_minus_alpha * dot;
         }
@@ -174,7 +197,7 @@ cudaError_t launch_bwd(const Problem& pr, const BwdArgs& a, int* status, cudaStr
   const long long T = pr.total_tokens;
   {
     PreK k{static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.sink,
-           a.delta, a.lse_log2, a.dq_accum, a.dsink_part, T, pr.hq};
+           static_cast<uint4*>(a.bias), a.dq_accum, a.dsink_part, T, pr.hq, pr.scale};
     if (a.preprocess_blocks > 0) bwd_pre_kernel<<<a.preprocess_blocks, 256, 0, stream>>>(k);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -89,17 +89,21 @@ constexpr int OFF_Q = OFF_V + TILE;
 constexpr int OFF_DO = OFF_Q + NS * TILE;
 constexpr int OFF_DS = OFF_DO + NS * TILE;     // 2 buffers x 32 KB
 constexpr int OFF_STG = OFF_DS + 2 * 2 * TILE;  // 16 KB fp32 dQ staging (32 of the 64 columns at a time)
-constexpr int OFF_L = OFF_STG + TILE;
-constexpr int OFF_DL = OFF_L + NS * BM * 4;
-constexpr int SMEM_DYN = OFF_DL + NS * BM * 4 + 1024;
+// Bias rows of the stage's 128 queries (16 bytes each: -l'/scale and -D as
+// bf16 hi/mid/lo, two zeros), the two 0/1 selector tiles that pick one triple
+// or the other (128 keys x 16 bytes), and a zero block that serves as the
+// upper K half (elements 8-15) of all of them.  All K-major, no swizzle.
+constexpr int OFF_BIAS = OFF_STG + TILE;           // NS x 2 KB
+constexpr int OFF_SEL = OFF_BIAS + NS * BM * 16;   // 2 x 2 KB
+constexpr int OFF_ZERO = OFF_SEL + 2 * BN * 16;    // 2 KB
+constexpr int SMEM_DYN = OFF_ZERO + BN * 16 + 1024;
 
 constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 320, TM_DQ = 384, TM_K = 448, TM_V = 480;
 constexpr int HALF = BM / 2;
 
 struct BwdTcK {
   CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dq;
-  const float* lse_log2;
-  const float* delta;
+  const uint4* bias;  // [Hq, T] rows of 8 bf16
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   const int32_t* cu;
@@ -154,16 +158,15 @@ SA_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint
 // The element-wise pass over one half step (64 queries) for this thread's
 // key row, in four 16-column chunks whose Tensor Memory loads are all issued
 // before the first wait (the whole phase's arithmetic is then independent
-// work for the scheduler).  The preprocess
-// stored -l' (log2 units) and -D, so each pair of columns costs one f32x2
-// FMA (phase 1) and one f32x2 add and multiply (phase 2).
+// work for the scheduler).  The MMAs already added -l'/scale to S^T and -D
+// to dP^T (a K=16 bias product), so each pair of columns costs one f32x2
+// multiply per phase and nothing is read from shared memory.
 //
-// Phase 1: P^T = exp2(S^T * scale * log2(e) - l'), masked on partial tiles
-// (FULL skips the predicate); packed P^T overwrites the S^T columns already
-// read; fp32 P stays in registers for phase 2.
+// Phase 1: P^T = exp2((S^T - l'/scale) * scale * log2(e)), masked on partial
+// tiles (FULL skips the predicate); packed P^T overwrites the S^T columns
+// already read; fp32 P stays in registers for phase 2.
 template <bool FULL>
-SA_DEV void ew_phase1(uint32_t tS, uint32_t sL, float sl2, int qh, int key, int len, const MaskParams& mask,
-                      float (&pv)[4][16]) {
+SA_DEV void ew_phase1(uint32_t tS, float sl2, int qh, int key, int len, const MaskParams& mask, float (&pv)[4][16]) {
   const float2 sl2x2 = make_float2(sl2, sl2);
   uint32_t sr[4][16];
 #pragma unroll
@@ -176,22 +179,17 @@ SA_DEV void ew_phase1(uint32_t tS, uint32_t sL, float sl2, int qh, int key, int 
     const uint32_t (&sc)[16] = sr[c];
     uint32_t pp[8];
 #pragma unroll
-    for (int e = 0; e < 16; e += 4) {
-      const float4 l4 = ld_shared_f4(sL + 64 * c + e * 4);
-#pragma unroll
-      for (int u = 0; u < 4; u += 2) {
-        const float2 x = ffma2(make_float2(__uint_as_float(sc[e + u]), __uint_as_float(sc[e + u + 1])), sl2x2,
-                               u ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y));
-        float2 pe = make_float2(ex2(x.x), ex2(x.y));
-        if (!FULL) {
-          const int q = qh + 16 * c + e + u;
-          if (!(q < len && visible(q, key, len, mask))) pe.x = 0.f;
-          if (!(q + 1 < len && visible(q + 1, key, len, mask))) pe.y = 0.f;
-        }
-        pv[c][e + u] = pe.x;
-        pv[c][e + u + 1] = pe.y;
-        pp[(e + u) >> 1] = pack_bf16(pe.x, pe.y);
+    for (int e = 0; e < 16; e += 2) {
+      const float2 x = fmul2(make_float2(__uint_as_float(sc[e]), __uint_as_float(sc[e + 1])), sl2x2);
+      float2 pe = make_float2(ex2(x.x), ex2(x.y));
+      if (!FULL) {
+        const int q = qh + 16 * c + e;
+        if (!(q < len && visible(q, key, len, mask))) pe.x = 0.f;
+        if (!(q + 1 < len && visible(q + 1, key, len, mask))) pe.y = 0.f;
       }
+      pv[c][e] = pe.x;
+      pv[c][e + 1] = pe.y;
+      pp[e >> 1] = pack_bf16(pe.x, pe.y);
     }
     tmem_st8(tS + 8 * c, pp);
   }
@@ -200,7 +198,7 @@ SA_DEV void ew_phase1(uint32_t tS, uint32_t sL, float sl2, int qh, int key, int 
 // Phase 2: dS^T = P^T (dP^T - D), packed over the dP^T columns already
 // read and into this key row of the shared dS^T tile (128-byte swizzle) for
 // the dQ product.  Masked entries have P = 0 and so dS = 0.
-SA_DEV void ew_phase2(uint32_t tDP, uint32_t sD, uint32_t rowb, int kr, const float (&pv)[4][16]) {
+SA_DEV void ew_phase2(uint32_t tDP, uint32_t rowb, int kr, const float (&pv)[4][16]) {
   uint32_t dr[4][16];
 #pragma unroll
   for (int c = 0; c < 4; ++c) tmem_ld16(tDP + 16 * c, dr[c]);
@@ -212,15 +210,10 @@ SA_DEV void ew_phase2(uint32_t tDP, uint32_t sD, uint32_t rowb, int kr, const fl
     const uint32_t (&dc)[16] = dr[c];
     uint32_t dd[8];
 #pragma unroll
-    for (int e = 0; e < 16; e += 4) {
-      const float4 d4 = ld_shared_f4(sD + 64 * c + e * 4);
-#pragma unroll
-      for (int u = 0; u < 4; u += 2) {
-        const float2 t = fadd2(make_float2(__uint_as_float(dc[e + u]), __uint_as_float(dc[e + u + 1])),
-                               u ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y));
-        const float2 de = fmul2(make_float2(pv[c][e + u], pv[c][e + u + 1]), t);
-        dd[(e + u) >> 1] = pack_bf16(de.x, de.y);
-      }
+    for (int e = 0; e < 16; e += 2) {
+      const float2 de = fmul2(make_float2(pv[c][e], pv[c][e + 1]),
+                              make_float2(__uint_as_float(dc[e]), __uint_as_float(dc[e + 1])));
+      dd[e >> 1] = pack_bf16(de.x, de.y);
     }
     tmem_st8(tDP + 8 * c, dd);
     st_shared_v4(rowb + (((2 * c) ^ (kr & 7)) << 4), dd[0], dd[1], dd[2], dd[3]);
@@ -292,6 +285,15 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
     tmem_alloc(smem_u32(&tmem_base_sh), 512);
     tmem_relinquish();
   }
+  if (tid < BN) {
+    // Selector rows [1,1,1,0,...] (picks -l'/scale) and [0,0,0,1,1,1,0,0]
+    // (picks -D) in bf16, and the zero block.
+    constexpr uint32_t one = 0x3F80u;
+    st_shared_v4(sb + OFF_SEL + tid * 16, one | (one << 16), one, 0u, 0u);
+    st_shared_v4(sb + OFF_SEL + BN * 16 + tid * 16, 0u, one << 16, one | (one << 16), 0u);
+    st_shared_v4(sb + OFF_ZERO + tid * 16, 0u, 0u, 0u, 0u);
+    fence_async_smem();  // generic-proxy writes, read by the tensor core
+  }
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
@@ -317,15 +319,14 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
       if (t >= NS && !mbar_wait_warp(b_qe(s), ((t / NS) - 1) & 1, ab)) break;
       if (lane == 0) SA_TRACE(0, t, 0);
       const int h = step_head(t), q0 = step_q0(t);
-      // l' and D of the 128 query rows: asynchronous 4-byte copies that
+      // Bias rows of the 128 query rows: asynchronous 16-byte copies that
       // complete on the stage's full barrier (rows past the sequence end read
       // row 0 and are masked by the element-wise warps).
 #pragma unroll
       for (int r = lane; r < BM; r += 32) {
         const int qq = q0 + r;
         const size_t idx = static_cast<size_t>(h) * p.T + sp.start + (qq < sp.len ? qq : 0);
-        cp_async4(sb + OFF_L + (s * BM + r) * 4, p.lse_log2 + idx);
-        cp_async4(sb + OFF_DL + (s * BM + r) * 4, p.delta + idx);
+        cp_async16(sb + OFF_BIAS + (s * BM + r) * 16, p.bias + idx, true);
       }
       cp_async_arrive_noinc(b_qf(s));
       if (lane == 0) {
@@ -355,17 +356,27 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
       const uint64_t d_dsm = sdesc_sw128(sb + OFF_DS, TILE, 1024);  // MN-major A of dQ (two 64-query blocks)
       // S_h^T = K Q_h^T and dP_h^T = V dO_h^T of the step held in stage s
       // (A = K or V in Tensor Memory, B = the half's 64 query rows, K-major).
+      // Bias product first (overwrites): a selector tile times the stage's
+      // bias rows of the half adds -l'/scale to S^T and -D to dP^T.
+      auto bias_desc = [&](int h, int s) {
+        const uint32_t off = OFF_BIAS + (s * BM + h * HALF) * 16;
+        return sdesc_nosw(sb + off, OFF_ZERO - off, 128);
+      };
+      const uint64_t d_sel_s = sdesc_nosw(sb + OFF_SEL, OFF_ZERO - OFF_SEL, 128);
+      const uint64_t d_sel_dp = sdesc_nosw(sb + OFF_SEL + BN * 16, OFF_ZERO - (OFF_SEL + BN * 16), 128);
       auto issue_s = [&](int h, int s) {
         const uint64_t q = sdesc_add(d_q, s * TILE + h * HALF * 128);
+        if (leader) mma_ss(tmem + TM_S + HALF * h, d_sel_s, bias_desc(h, s), id_s, 0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          if (leader) mma_ts(tmem + TM_S + HALF * h, tmem + TM_K + kk * 8, sdesc_add(q, kk * 32), id_s, kk > 0);
+          if (leader) mma_ts(tmem + TM_S + HALF * h, tmem + TM_K + kk * 8, sdesc_add(q, kk * 32), id_s, 1);
       };
       auto issue_dp = [&](int h, int s) {
         const uint64_t o = sdesc_add(d_o, s * TILE + h * HALF * 128);
+        if (leader) mma_ss(tmem + TM_DP + HALF * h, d_sel_dp, bias_desc(h, s), id_s, 0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          if (leader) mma_ts(tmem + TM_DP + HALF * h, tmem + TM_V + kk * 8, sdesc_add(o, kk * 32), id_s, kk > 0);
+          if (leader) mma_ts(tmem + TM_DP + HALF * h, tmem + TM_V + kk * 8, sdesc_add(o, kk * 32), id_s, 1);
       };
       bool ok = mbar_wait_warp(b_kvt, 0, ab) && mbar_wait_warp(b_qf(0), 0, ab);
       if (ok) {
@@ -469,25 +480,19 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
       if (lane == 0) mbar_arrive(b_kvt);
     }
     for (int t = 0; ok && t < nsteps; ++t) {
-      const int s = t % NS;
       if (tid == 128 || tid == 256) SA_TRACE(2 + (tid == 256 ? 2 : 0), t, 0);
-      // l' and D of this step (stage s) have almost always landed: test that
-      // first, without blocking, so its latency overlaps the wait for S.
-      const bool q_ready = mbar_test_wait(b_qf(s), (t / NS) & 1);
-      ok = mbar_wait_warp(b_s(half), t & 1, ab) &&
-           (__all_sync(0xffffffffu, q_ready) || mbar_wait_warp(b_qf(s), (t / NS) & 1, ab));
+      ok = mbar_wait_warp(b_s(half), t & 1, ab);
       if (!ok) break;
       if (tid == 128 || tid == 256) SA_TRACE(2 + (tid == 256 ? 2 : 0), t, 1);
       fence_after_sync();
       const int qh = step_q0(t) + HALF * half;
       const bool full = block_full(qh, HALF, k0, BN, sp.len, p.mask);
       const uint32_t rowb = sb + OFF_DS + (t & 1) * 2 * TILE + half * TILE + kr * 128;
-      const uint32_t sL = sb + OFF_L + (s * BM + HALF * half) * 4, sD = sb + OFF_DL + (s * BM + HALF * half) * 4;
       float pv[4][16];
       if (full)
-        ew_phase1<true>(tS, sL, sl2, qh, key, sp.len, p.mask, pv);
+        ew_phase1<true>(tS, sl2, qh, key, sp.len, p.mask, pv);
       else
-        ew_phase1<false>(tS, sL, sl2, qh, key, sp.len, p.mask, pv);
+        ew_phase1<false>(tS, sl2, qh, key, sp.len, p.mask, pv);
       tmem_st_wait();
       fence_before_sync();
       __syncwarp();
@@ -495,7 +500,7 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
       if (tid == 128 || tid == 256) SA_TRACE(2 + (tid == 256 ? 2 : 0), t, 2);
       if (!(ok = mbar_wait_warp(b_dp(half), t & 1, ab))) break;
       fence_after_sync();
-      ew_phase2(tDP, sD, rowb, kr, pv);
+      ew_phase2(tDP, rowb, kr, pv);
       tmem_st_wait();
       fence_before_sync();
       fence_async_smem();
@@ -662,8 +667,7 @@ cudaError_t launch_bwd_tc_main(const Problem& pr, const BwdArgs& a, int* status,
       !make_rows_map(&k.tm_v, a.v, pr.total_tokens, pr.hkv, BN) ||
       !make_f32_rows_map(&k.tm_dq, a.dq_accum, pr.total_tokens, pr.hq, BM))
     return cudaErrorInvalidValue;
-  k.lse_log2 = a.lse_log2;
-  k.delta = a.delta;
+  k.bias = static_cast<const uint4*>(a.bias);
   k.dk = static_cast<__nv_bfloat16*>(a.dk);
   k.dv = static_cast<__nv_bfloat16*>(a.dv);
   k.cu = pr.cu;

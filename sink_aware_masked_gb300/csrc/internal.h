@@ -48,8 +48,10 @@ struct BwdArgs {
   float* dsink;
   // workspace carve-up
   float* dq_accum;    // [T, Hq, 64] fp32
-  float* delta;       // [Hq, T]  -D = -<dO, O>
-  float* lse_log2;    // [Hq, T]  -(l + softplus(sink - l)) * log2(e)
+  // [Hq, T, 8] bf16 per (head, token): -l'/scale and -D (l' = l + softplus(sink - l),
+  // D = <dO, O>), each as three bf16 summands (hi, mid, lo), then two zeros;
+  // the main kernel adds them to S^T and dP^T through one K=16 MMA.
+  void* bias;
   float* dsink_part;  // [preprocess blocks, Hq]
   float* dkv_acc;     // fp32 dK/dV partial sums of split prefix key tiles (or nullptr)
   int preprocess_blocks;

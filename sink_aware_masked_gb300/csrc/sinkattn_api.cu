@@ -100,7 +100,7 @@ __global__ void selftest_wait_kernel(int* status, long long limit) {
 }
 
 struct BwdLayout {
-  size_t dq_accum, delta, lse_log2, part, dkv, total;
+  size_t dq_accum, bias, part, dkv, total;
   int pre_blocks;
 };
 
@@ -109,9 +109,8 @@ BwdLayout bwd_layout(const sa::Problem& p) {
   const size_t T = static_cast<size_t>(p.total_tokens), H = static_cast<size_t>(p.hq);
   l.pre_blocks = sa::ceil_div(p.total_tokens, sa::kPreTokens);
   l.dq_accum = 0;
-  l.delta = l.dq_accum + round_up(T * H * sa::kHeadDim * 4, 256);
-  l.lse_log2 = l.delta + round_up(T * H * 4, 256);
-  l.part = l.lse_log2 + round_up(T * H * 4, 256);
+  l.bias = l.dq_accum + round_up(T * H * sa::kHeadDim * 4, 256);
+  l.part = l.bias + round_up(T * H * 16, 256);
   l.dkv = l.part + round_up(static_cast<size_t>(l.pre_blocks) * H * 4, 256);
   l.total = l.dkv + round_up(sa::bwd_split_acc_bytes(p), 256) + 256;
   return l;
@@ -185,8 +184,7 @@ sinkattn_status sinkattn_bwd(const sinkattn_problem* prob, const void* q, const 
   a.dv = dv;
   a.dsink = dsink;
   a.dq_accum = reinterpret_cast<float*>(ws + L.dq_accum);
-  a.delta = reinterpret_cast<float*>(ws + L.delta);
-  a.lse_log2 = reinterpret_cast<float*>(ws + L.lse_log2);
+  a.bias = ws + L.bias;
   a.dsink_part = reinterpret_cast<float*>(ws + L.part);
   a.dkv_acc = sa::bwd_split_acc_bytes(p) ? reinterpret_cast<float*>(ws + L.dkv) : nullptr;
   a.preprocess_blocks = L.pre_blocks;

@@ -167,6 +167,17 @@ SA_DEV uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
 // Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A
 // and B (bits 7-9 = 1, 10-12 = 1), operand majorness (bit 15 A, bit 16 B;
 // 0 = K-major, 1 = MN-major), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+// Shared-memory matrix descriptor, K-major, no swizzle: 8-row x 16-byte
+// core matrices; lbo = byte offset from a core matrix to the next one along
+// K, sbo = byte offset between consecutive 8-row groups.
+SA_DEV uint64_t sdesc_nosw(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;  // descriptor version; layout type 0 (no swizzle) in bits 61-63
+  return d;
+}
+
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);

@@ -239,5 +239,8 @@ def test_peak_memory_linear_in_sequence_length():
         torch.cuda.synchronize()
         peaks.append(torch.cuda.max_memory_allocated() - base)
     d = np.diff(peaks) / np.diff([2048, 4096, 8192, 16384])
-    # bytes per extra token stay constant (no S^2 term)
-    assert np.max(d) / np.min(d) < 1.05, peaks
+    # Bytes per extra token stay constant (no S^2 term).  torch's caching
+    # allocator rounds large blocks up to 2 MiB, which moves the smallest case
+    # by a few percent; an S x S buffer of even one head would double the
+    # slope between the last two sizes.
+    assert np.max(d) / np.min(d) < 1.15, peaks
