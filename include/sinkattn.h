@@ -96,9 +96,10 @@ sinkattn_status sinkattn_fwd(const sinkattn_problem* prob,
 /* Backward.  Reads the forward's inputs, its outputs o and lse, and dout;
  * writes dq, dk, dv (bf16) and dsink (fp32 [Hq]), where
  * dsink[h] = -sum over all rows of (1 - alpha_q) * <dout_q, o_q>.
- * The workspace holds an fp32 dQ accumulator [T, Hq, 64], the per-row
- * terms D and l' = l + softplus(sink - l) ([Hq, T] each) and per-block
- * partial sums of dsink. */
+ * The workspace holds an fp32 dQ accumulator [T, Hq, 64], one 16-byte row
+ * per (head, token) with the per-row terms -D and -l'/scale, where
+ * l' = l + softplus(sink - l), as three bf16 summands each ([Hq, T]), and
+ * per-block partial sums of dsink. */
 sinkattn_status sinkattn_bwd(const sinkattn_problem* prob,
                              const void* q, const void* k, const void* v, const void* o,
                              const float* lse, const void* dout, const float* sink,
