@@ -8,22 +8,25 @@
 // (round r gives unit r*G + c to CTA c on even rounds, r*G + G-1-c on odd
 // ones).  Warp roles (12 warps, three warpgroups):
 //   warp 0      TMA producer: Q of both heads into one of two Q buffers,
-//               then K and V tiles of 128 keys through an NS-stage ring
-//               (separate K and V barriers so S = QK^T can start before V
-//               lands).  It runs ahead across unit boundaries.
-//   warp 1      MMA issuer (one elected lane) and TMEM owner:
+//               then K and V tiles of 128 keys through an NS-stage ring (one
+//               barrier per stage).  It runs ahead across unit boundaries.
+//   warp 1      S issuer (one elected lane) and TMEM owner:
 //               S_i = Q_i K_j^T   (M=128, N=128, K=64; A = Q_i, B = K_j, both
 //                                   K-major in smem)
+//               for both heads of step t as soon as both softmax warpgroups
+//               hold S of step t-1 in registers.
+//   warp 2      P.V issuer (one elected lane):
 //               O_i += P_i V_j    (M=128, N=64,  K=128; A = P_i in TMEM,
 //                                   B = V_j MN-major in smem)
-//               in the order S_0(t), S_1(t), then P.V of step t-1 by key
-//               halves (first half of both heads, then the second) over the
-//               flat sequence t of (unit, key tile) steps.  Barriers that
-//               both heads pass together are shared (K/V stage, S release,
-//               P halves), which keeps this warp's serial chain of barrier
-//               round trips short: it, not the tensor core, bounds the step.
-//   warps 2-3   idle (they only complete the first warpgroup, which hands
-//               its registers to the softmax warpgroups: 64 vs 216 each)
+//               by key halves (first half of both heads, then the second) as
+//               the softmax hands them over.  The tensor core queues only a
+//               few MMAs, so an issuing thread blocks while earlier ones run;
+//               with S and P.V in separate warps neither chain of waits
+//               stalls the other.  t is the flat sequence of (unit, key tile)
+//               steps; barriers both heads pass together (K/V stage, S
+//               release, P halves) are shared.
+//   warp 3      idle (it only completes the first warpgroup, which hands its
+//               registers to the softmax warpgroups: 64 vs 216 each)
 //   warps 4-7   softmax of head 0, warps 8-11 softmax of head 1: the thread
 //               in lane l of warp w owns query row 32 * (w % 4) + l (its TMEM
 //               lane), so row max and row sum need no shuffles.
@@ -84,8 +87,8 @@ constexpr int BN = 128;
 constexpr int NS = 4;   // K/V ring stages
 constexpr int NQB = 2;  // Q buffers (the next unit's Q lands while this one runs)
 constexpr int NTHR = 384;
-// Register split after setmaxnreg: 128 x 64 + 256 x 216 = 63,488 <= 384 x 168.
-constexpr int REGS_LOW = 64, REGS_HIGH = 216;
+// Register split after setmaxnreg: 128 x 72 + 256 x 216 = 64,512 <= 384 x 168.
+constexpr int REGS_LOW = 72, REGS_HIGH = 216;
 constexpr int TILE = BM * D * 2;  // 16 KB: 128 rows x 128 bytes
 constexpr int OFF_Q = 0;                      // buffer b, head i: + (2 b + i) * TILE
 constexpr int OFF_K = OFF_Q + NQB * 2 * TILE;
@@ -189,7 +192,7 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
     }
     for (int s = 0; s < NS; ++s) {
       mbar_init(b_kv(s), 1);
-      mbar_init(b_e(s), 1);
+      mbar_init(b_e(s), 2);  // one commit from each MMA issuer
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_s(i), 1);
@@ -197,7 +200,7 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
       mbar_init(b_pv(i), 1);
     }
     mbar_init(b_sf, 4 * nh);
-    mbar_init(b_dr, 1);
+    mbar_init(b_dr, 2);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -242,77 +245,75 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
           for (int t = max(0, nt - NS); t < nt; ++t) wait_drain(b_kv(t % NS), (t / NS) & 1);
         }
       }
-    } else if (warp == 1) {
-      // ---------------------------------------------------------- MMA issuer
+    } else if (warp == 1 || warp == 2) {
+      // ---------------------------------------------------------- MMA issuers
       // Whole warp: descriptors are warp-uniform; one elected lane issues.
       const bool leader = elect_one();
-      const uint32_t id_s = idesc_bf16(BM, BN, false, false);
-      const uint32_t id_o = idesc_bf16(BM, D, false, true);
-      const uint64_t d_q = sdesc_sw128(sb + OFF_Q, 16, 1024);  // buffer b, head i: + (2 b + i) * TILE
-      const uint64_t d_k = sdesc_sw128(sb + OFF_K, 16, 1024);  // stage s: + s * TILE
-      const uint64_t d_v = sdesc_sw128(sb + OFF_V, 16, 1024);
-      auto issue_s = [&](int i, int qb, int s) {
-        const uint64_t qd = sdesc_add(d_q, (2 * qb + i) * TILE), kd = sdesc_add(d_k, s * TILE);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          if (leader) mma_ss(tmem + TM_S + 128 * i, sdesc_add(qd, kk * 32), sdesc_add(kd, kk * 32), id_s, kk > 0);
-      };
-      // O_i += P_i V over keys [64 hf, 64 hf + 64) of the tile.
-      auto issue_pv = [&](int i, int s, int hf, bool first) {
-        const uint64_t vb = sdesc_add(d_v, s * TILE);
-#pragma unroll
-        for (int k4 = 0; k4 < BN / 32; ++k4) {
-          const int kk = 4 * hf + k4;
-          if (leader)
-            mma_ts(tmem + TM_O + 64 * i, tmem + TM_P + 64 * i + kk * 8, sdesc_add(vb, kk * 2048), id_o,
-                   (!first || kk > 0) ? 1u : 0u);
-        }
-      };
       auto wait_all = [&](uint32_t bar, uint32_t parity) { return mbar_wait_warp(bar, parity, ab); };
-      int nt = 0;            // flat step index
-      int pend_s = 0;        // K/V stage of step nt - 1
-      bool pend_first = false;
-      // P.V of step nt - 1 for both heads, one key half at a time as the
-      // softmax hands the halves of P over, then release its K/V stage.
-      auto flush_pv = [&]() -> bool {
-        const int t = nt - 1;
-        for (int hf = 0; hf < 2; ++hf) {
-          if (!wait_all(b_p(hf), t & 1)) return false;
-          fence_after_sync();
-          for (int i = 0; i < nh; ++i) issue_pv(i, pend_s, hf, pend_first);
-          if (leader) mma_commit(b_pv(hf));
-          if (lane == 0) SA_TRACE(0, t, 3 + hf);
-        }
-        if (leader) mma_commit(b_e(pend_s));
-        return true;
-      };
       bool ok = true;
+      int nt = 0;  // flat step index
       Unit u;
-      for (int r = 0; ok && get_unit(p, r, u); ++r) {
-        const int qb = r % NQB;
-        if (!(ok = wait_all(b_qf(qb), (r / NQB) & 1))) break;
-        for (int j = 0; j < u.n_tiles; ++j, ++nt) {
-          const int s = nt % NS;
-          // Both tests are issued before either result is needed, so their
-          // latencies overlap; a phase still pending falls back to a wait.
-          const bool kv_ready = mbar_test_wait(b_kv(s), (nt / NS) & 1);
-          const bool s_ready = nt == 0 || mbar_test_wait(b_sf, (nt - 1) & 1);
-          if (!__all_sync(0xffffffffu, kv_ready) && !(ok = wait_all(b_kv(s), (nt / NS) & 1))) break;
-          if (!__all_sync(0xffffffffu, s_ready) && !(ok = wait_all(b_sf, (nt - 1) & 1))) break;
-          fence_after_sync();
-          for (int i = 0; i < nh; ++i) {
-            issue_s(i, qb, s);
-            if (leader) mma_commit(b_s(i));
-            if (lane == 0) SA_TRACE(0, nt, 1 + i);
+      if (warp == 1) {
+        // S_i(t) = Q_i K(t)^T for both heads.
+        const uint32_t id_s = idesc_bf16(BM, BN, false, false);
+        const uint64_t d_q = sdesc_sw128(sb + OFF_Q, 16, 1024);  // buffer b, head i: + (2 b + i) * TILE
+        const uint64_t d_k = sdesc_sw128(sb + OFF_K, 16, 1024);  // stage s: + s * TILE
+        for (int r = 0; ok && get_unit(p, r, u); ++r) {
+          const int qb = r % NQB;
+          if (!(ok = wait_all(b_qf(qb), (r / NQB) & 1))) break;
+          for (int j = 0; j < u.n_tiles; ++j, ++nt) {
+            const int s = nt % NS;
+            // Both tests are issued before either result is needed, so their
+            // latencies overlap; a phase still pending falls back to a wait.
+            const bool kv_ready = mbar_test_wait(b_kv(s), (nt / NS) & 1);
+            const bool s_ready = nt == 0 || mbar_test_wait(b_sf, (nt - 1) & 1);
+            if (!__all_sync(0xffffffffu, kv_ready) && !(ok = wait_all(b_kv(s), (nt / NS) & 1))) break;
+            if (!__all_sync(0xffffffffu, s_ready) && !(ok = wait_all(b_sf, (nt - 1) & 1))) break;
+            fence_after_sync();
+            for (int i = 0; i < nh; ++i) {
+              const uint64_t qd = sdesc_add(d_q, (2 * qb + i) * TILE), kd = sdesc_add(d_k, s * TILE);
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk)
+                if (leader) mma_ss(tmem + TM_S + 128 * i, sdesc_add(qd, kk * 32), sdesc_add(kd, kk * 32), id_s, kk > 0);
+              if (leader) mma_commit(b_s(i));
+              if (lane == 0) SA_TRACE(0, nt, 1 + i);
+            }
+            if (leader) {
+              if (j == u.n_tiles - 1) mma_commit(b_qe(qb));
+              mma_commit(b_e(s));
+            }
           }
-          if (j == u.n_tiles - 1 && leader) mma_commit(b_qe(qb));
-          if (nt > 0 && !(ok = flush_pv())) break;
-          pend_s = s;
-          pend_first = (j == 0);
-          if (lane == 0) SA_TRACE(0, nt, 0);
+        }
+      } else {
+        // O_i += P_i(t) V(t) for both heads, one key half at a time.
+        const uint32_t id_o = idesc_bf16(BM, D, false, true);
+        const uint64_t d_v = sdesc_sw128(sb + OFF_V, 16, 1024);  // stage s: + s * TILE
+        for (int r = 0; ok && get_unit(p, r, u); ++r) {
+          for (int j = 0; ok && j < u.n_tiles; ++j, ++nt) {
+            const int s = nt % NS;
+            const uint64_t vb = sdesc_add(d_v, s * TILE);
+            // The V tile landed before S of this step was issued; this
+            // acquires the TMA writes for this warp's own MMAs.
+            if (!(ok = wait_all(b_kv(s), (nt / NS) & 1))) break;
+            for (int hf = 0; hf < 2; ++hf) {
+              if (!(ok = wait_all(b_p(hf), nt & 1))) break;
+              fence_after_sync();
+              for (int i = 0; i < nh; ++i) {
+#pragma unroll
+                for (int k4 = 0; k4 < BN / 32; ++k4) {
+                  const int kk = 4 * hf + k4;
+                  if (leader)
+                    mma_ts(tmem + TM_O + 64 * i, tmem + TM_P + 64 * i + kk * 8, sdesc_add(vb, kk * 2048), id_o,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+                }
+              }
+              if (leader) mma_commit(b_pv(hf));
+              if (lane == 0) SA_TRACE(0, nt, 3 + hf);
+            }
+            if (ok && leader) mma_commit(b_e(s));
+          }
         }
       }
-      if (ok && nt > 0) flush_pv();
       if (leader) mma_commit(b_dr);
       __syncwarp();
       wait_drain(b_dr, 0);
