@@ -41,6 +41,8 @@ dK = scale dS^T Q, dV = P^T dO, and dsink[h] = sum over rows of dS_sink.
 
 Arrays: q, dout [T, Hq, D]; k, v [T, Hkv, D]; sink [Hq]; cu_seqlens [B + 1]
 (token offsets of the packed sequences).  All float64 NumPy arrays.
+``decode_forward`` evaluates the last few rows of each sequence against its
+whole key/value history (the rollout-side forward).
 Rows are handled in blocks of at most ``row_block`` queries to bound memory;
 each row's softmax is independent, so blocking changes no arithmetic.
 """
@@ -179,6 +181,43 @@ def forward_backward(q, k, v, sink, dout, cu_seqlens, window=WINDOW_INF, prefix=
     if with_bwd:
         res.update(dq=dq, dk=dk, dv=dv, dsink=dsink)
     return res
+
+
+def decode_forward(q, k, v, sink, cu_kv, q_per_seq, window=WINDOW_INF, prefix=0, causal=True, scale=None):
+    """Forward for the last ``q_per_seq`` positions of each packed sequence.
+
+    The rollout-side (decode) forward of the same attention: sequence b keeps
+    its L_b cached keys and values in k, v [T_kv, Hkv, D] at offsets cu_kv
+    [B + 1], and q [B * n, Hq, D] (n = q_per_seq) holds the queries of its
+    positions L_b - n ... L_b - 1 in that order.  Every row is the same row
+    of ``forward`` over the whole sequence (rows are independent): same mask,
+    explicit sink column and lse.  Returns (o [B * n, Hq, D], lse [Hq, B * n]).
+    """
+    T_kv, hkv, d = k.shape
+    hq = q.shape[1]
+    n = int(q_per_seq)
+    cu = np.asarray(cu_kv, dtype=np.int64)
+    B = len(cu) - 1
+    assert n >= 1 and q.shape == (B * n, hq, d) and v.shape == k.shape and sink.shape == (hq,)
+    assert hq % hkv == 0 and cu[0] == 0 and cu[-1] == T_kv and np.all(np.diff(cu) >= n)
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    group = hq // hkv
+    o = np.zeros((B * n, hq, d))
+    lse = np.zeros((hq, B * n))
+    for b in range(B):
+        t0, t1 = int(cu[b]), int(cu[b + 1])
+        L = t1 - t0
+        m = visible(np.arange(L - n, L), np.arange(L), window, prefix, causal)
+        rows = slice(b * n, (b + 1) * n)
+        for h in range(hq):
+            g = h // group
+            s = scale * (q[rows, h, :] @ k[t0:t1, g, :].T)
+            s = np.where(m, s, -np.inf)
+            p, _, l = _extended_softmax(s, float(sink[h]))
+            o[rows, h, :] = p @ v[t0:t1, g, :]
+            lse[h, rows] = l
+    return o, lse
 
 
 def unmasked_pairs(seqlens, num_heads_q, window=WINDOW_INF, prefix=0, causal=True) -> int:

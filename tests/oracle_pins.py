@@ -333,9 +333,24 @@ def check_invariants(mod):
     return None if e < 1e-12 else f"dsink identity err {e:.3g}"
 
 
+def check_decode_sdpa(mod):
+    """Decode rows equal the last rows of SDPA over the whole sequence."""
+    for (lens, n, window, prefix, hq, hkv, seed) in [((40, 17, 9), 3, 11, 3, 4, 2, 81), ((33, 5), 1, -1, 0, 6, 3, 82),
+                                                     ((20,), 4, 2, 0, 2, 1, 83)]:
+        q, k, v, do, sink, cu = rand_problem(lens, hq, hkv, 8, seed)
+        want = sdpa_with_sink(q, k, v, sink, do, cu, window, prefix, True, 0.35)
+        last = np.concatenate([np.arange(int(cu[b + 1]) - n, int(cu[b + 1])) for b in range(len(lens))])
+        o, lse = mod.decode_forward(q[last], k, v, sink, cu, n, window, prefix, True, 0.35)
+        msg = _cmp({"o": o, "lse": lse}, {"o": want["o"][last], "lse": want["lse"][:, last]}, ["o", "lse"], 1e-12,
+                   f"decode lens={lens} n={n}")
+        if msg:
+            return msg
+    return None
+
+
 ALL_CHECKS = [check_hand_example, check_sdpa, check_alpha_closed_form, check_window0, check_single_token,
               check_finite_differences, check_pair_counts, check_sink_limits, check_mask_equivalences,
-              check_gqa_vs_mha, check_invariants]
+              check_gqa_vs_mha, check_invariants, check_decode_sdpa]
 
 
 def run_all(mod):

@@ -32,8 +32,12 @@ MUTATIONS = {
     "dq_no_scale": ("dq[t0 + r0:t0 + r1, h, :] = scale * (ds @ K)", "dq[t0 + r0:t0 + r1, h, :] = (ds @ K)"),
     "dk_uses_p": ("dk[t0:t1, g, :] += scale * (ds.T @ Q[r0:r1])", "dk[t0:t1, g, :] += scale * (p.T @ Q[r0:r1])"),
     "dv_uses_ds": ("dv[t0:t1, g, :] += p.T @ dO", "dv[t0:t1, g, :] += ds.T @ dO"),
-    "gqa_modulo": ("g = h // group", "g = h % hkv"),
+    "gqa_modulo": ("        g = h // group\n        if with_bwd:", "        g = h % hkv\n        if with_bwd:"),
     "ds_sign": ("ds = p * (dp - D[:, None])", "ds = p * (D[:, None] - dp)"),
+    "decode_position_shift": ("m = visible(np.arange(L - n, L), np.arange(L), window, prefix, causal)",
+                              "m = visible(np.arange(L - n + 1, L + 1), np.arange(L), window, prefix, causal)"),
+    "decode_head_map": ("            g = h // group\n            s = scale * (q[rows, h, :]",
+                        "            g = h % hkv\n            s = scale * (q[rows, h, :]"),
 }
 
 
