@@ -10,6 +10,11 @@ at 14 * 64 FLOP per pair (forward 4 * 64, backward 10 * 64).  Inputs are
 resident in HBM; L2 is flushed (256 MiB write) before every timed step, and
 each step is timed alone with CUDA events on the stream the kernels run on.
 
+Decode workloads (``--workload decode_*``): one step = one decode forward
+(key-chunk kernel + merge kernel) of the workload's query rows against the
+key/value cache of every sequence, reported in GB/s of algorithmic HBM
+traffic (the visible keys and values once, the queries, O and lse).
+
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
        python bench.py --impl reference ...   (times the CPU float64 oracle)
 Under torchrun each rank runs its own batch (weak scaling, no collective on
@@ -42,6 +47,8 @@ FLOP_FWD_PER_PAIR = 4 * 64
 FLOP_BWD_PER_PAIR = 10 * 64
 L2_FLUSH_BYTES = 256 << 20
 LAUNCHES_PER_STEP = 4  # forward, backward preprocess, backward main, dQ convert
+DECODE_METRIC = "sink-attn decode GB/s (bf16 KV-cache stream) and % of measured HBM copy bandwidth"
+DECODE_LAUNCHES_PER_STEP = 2  # key-chunk kernel, merge kernel
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -69,6 +76,25 @@ def algorithmic_bytes(wl):
     fwd = q + 2 * kv + q + lse
     bwd = q + 2 * kv + q + q + lse + q + 2 * kv
     return fwd, bwd
+
+
+def decode_visible_keys(wl, n):
+    """Keys that at least one of the last n query rows of a sequence sees, summed over sequences."""
+    total = 0
+    for L in wl.seqlens:
+        L = int(L)
+        lo = 0 if wl.window < 0 else max(0, L - n - wl.window)
+        total += (L - lo) + min(wl.prefix, lo)
+    return total
+
+
+def decode_bytes(wl, n):
+    """Algorithmic HBM bytes of one decode step: visible K and V once per kv
+    head, the query rows, O and lse."""
+    rows = wl.num_seqs * n
+    kv = decode_visible_keys(wl, n) * wl.num_heads_kv * wl.head_dim * 2 * 2
+    q = rows * wl.num_heads_q * wl.head_dim * 2
+    return kv + 2 * q + rows * wl.num_heads_q * 4
 
 
 def load_peaks():
@@ -202,8 +228,82 @@ def cpu_baseline(wl, pool=None):
                       f"{wl.name}, fwd+bwd, one single-threaded worker per head, {sec:.2f} s wall"}
 
 
+def _oracle_decode_job(args):
+    import oracle
+
+    q, k, v, sink, cu, n, window, prefix, causal, scale = args
+    t = time.perf_counter()
+    oracle.decode_forward(q, k, v, sink, cu, n, window, prefix, causal, scale)
+    return time.perf_counter() - t
+
+
+def decode_oracle_jobs(wl, n, cores):
+    """One job per sequence of a bounded sample (the first min(B, cores)
+    sequences, float64), and the algorithmic bytes the sample covers."""
+    nseq = max(1, min(wl.num_seqs, cores))
+    sub_wl = wl.with_(seqlens=tuple(wl.seqlens[:nseq]))
+    inp = W.make_decode_inputs(sub_wl, n)
+    q, k, v, sink = (inp.f64(x) for x in ("q", "k", "v", "sink"))
+    cu = sub_wl.cu_seqlens()
+    jobs = []
+    for b in range(nseq):
+        t0, t1 = int(cu[b]), int(cu[b + 1])
+        jobs.append((np.ascontiguousarray(q[b * n:(b + 1) * n]), np.ascontiguousarray(k[t0:t1]),
+                     np.ascontiguousarray(v[t0:t1]), sink, np.array([0, t1 - t0]), n, wl.window, wl.prefix,
+                     wl.causal, wl.scale))
+    return jobs, decode_bytes(sub_wl, n), nseq
+
+
+def decode_cpu_baseline(wl, n, steps=3):
+    pool = OraclePool()
+    try:
+        jobs, nbytes, nseq = decode_oracle_jobs(wl, n, pool.cores)
+        t = time.perf_counter()
+        for _ in range(steps):
+            pool.pool.map(_oracle_decode_job, jobs, chunksize=1)
+        sec = time.perf_counter() - t
+    finally:
+        pool.close()
+    return {"value": steps * nbytes / sec / 1e9, "unit": "GB/s", "cores": pool.cores, "kind": "oracle",
+            "sample": f"{steps} rounds of {nseq} sequences of {wl.name} (all heads, {n} query rows each), "
+                      f"one single-threaded worker per sequence, {sec:.2f} s wall"}
+
+
+def run_reference_decode(args, rank):
+    if rank != 0:
+        return 0
+    wl, n = W.DECODE_WORKLOADS[args.workload]
+    pool = OraclePool()
+    try:
+        jobs, nbytes, nseq = decode_oracle_jobs(wl, n, pool.cores)
+        for _ in range(args.warmup):
+            pool.pool.map(_oracle_decode_job, jobs[:1], chunksize=1)
+        secs = []
+        for _ in range(args.steps):
+            t = time.perf_counter()
+            pool.pool.map(_oracle_decode_job, jobs, chunksize=1)
+            secs.append(time.perf_counter() - t)
+    finally:
+        pool.close()
+    total = sum(secs)
+    value = nbytes * len(secs) / total / 1e9
+    line = {
+        "impl": "reference", "metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(secs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "sample_per_step": f"{nseq} sequences, all heads"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": pool.cores, "kind": "oracle",
+                         "sample": f"each step: {nseq} sequences of {wl.name}, {n} query rows each"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_reference(args, rank):
     """The oracle as the reference arm, on the host cores of rank 0."""
+    if args.workload in W.DECODE_WORKLOADS:
+        return run_reference_decode(args, rank)
     if rank != 0:
         return 0
     wl = W.WORKLOADS[args.workload]
@@ -412,6 +512,131 @@ def run_gpu(args, world, rank, local):
     return 0
 
 
+def run_gpu_decode(args, world, rank, local):
+    """Decode steps of a DECODE_WORKLOADS entry; the key/value cache stays
+    resident (it is the decoder's state), the query rows are the step's input."""
+    import torch
+
+    import sink_aware_masked_gb300 as sa
+    from sink_aware_masked_gb300 import build as sa_build
+
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    sa_build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    base, n = W.DECODE_WORKLOADS[args.workload]
+    wl = base.with_(seed=base.seed + 1000 * rank)
+    inp = W.make_decode_inputs(wl, n)
+    q, k, v, sink = (t.to(dev) for t in (inp.q_bf16, inp.k_bf16, inp.v_bf16, inp.sink))
+    if wl.uniform:
+        prob = dict(num_seqs=wl.num_seqs)
+    else:
+        cu = wl.cu_seqlens()
+        prob = dict(cu_seqlens=torch.tensor(cu, dtype=torch.int32, device=dev),
+                    cu_seqlens_host=[int(x) for x in cu], max_seqlen=wl.max_seqlen)
+    prob.update(window=wl.window, prefix=wl.prefix, causal=wl.causal, scale=wl.scale)
+    o = torch.empty_like(q)
+    lse = torch.empty((wl.num_heads_q, q.shape[0]), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(16, sa.decode_workspace_bytes(q, k, q_per_seq=n, **prob)), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        sa.sinkattn_decode_fwd(q, k, v, sink, q_per_seq=n, o=o, lse=lse, workspace=ws, **prob)
+
+    for _ in range(max(args.warmup, 0)):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    if sa.sinkattn_get_device_status() != 0:
+        raise RuntimeError("device status reported a timed-out wait during warm-up")
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for e in ev:
+        for x in e:
+            x.record()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    for i in range(K):
+        flush.fill_(float(i))
+        e = ev[i]
+        sa.sinkattn_set_profile_events(sa.PROFILE_DECODE, e[2], e[3])
+        e[0].record()
+        step()
+        e[1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clock_info = clocks.stop()
+    sa.sinkattn_set_profile_events(sa.PROFILE_DECODE)
+    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    split_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    if sa.sinkattn_get_device_status() != 0:
+        raise RuntimeError("device status reported a timed-out wait")
+
+    # end to end: the step's query rows from pinned host memory, O and lse back
+    host_q = q.cpu().pin_memory()
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse)]
+    h2d = host_q.numel() * host_q.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    Ke = max(1, min(K, 20))
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ke)]
+    barrier(world)
+    for i in range(Ke):
+        flush.fill_(float(i))
+        e2e_ev[i][0].record()
+        q.copy_(host_q, non_blocking=True)
+        step()
+        for h_, d_ in zip(host_out, (o, lse)):
+            h_.copy_(d_, non_blocking=True)
+        e2e_ev[i][1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = [a.elapsed_time(b) for a, b in e2e_ev]
+
+    tot, e2e_tot = reduce_max([sum(step_ms), sum(e2e_ms)], world, dev)
+    nbytes = decode_bytes(wl, n)
+    value = world * nbytes * K / (tot / 1e3) / 1e9
+    e2e_value = world * nbytes * Ke / (e2e_tot / 1e3) / 1e9
+    peaks, peak_src = load_peaks()
+    avg_split = statistics.mean(split_ms)
+    achieved = nbytes / (avg_split / 1e3) / 1e9
+    line = {
+        "metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": tot / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "sequences": wl.num_seqs * world, "cached_tokens": wl.total_tokens,
+                   "query_rows_per_seq": n, "heads_q": wl.num_heads_q, "heads_kv": wl.num_heads_kv,
+                   "head_dim": wl.head_dim, "window": wl.window, "prefix": wl.prefix, "causal": wl.causal,
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "flushed before every step (256 MiB write, outside the step events)",
+                   "algorithmic_bytes_per_step": nbytes,
+                   "decode_rows_per_s": world * wl.num_seqs * n * K / (tot / 1e3)},
+        "pct_of_peak": 100.0 * value / world / peaks["hbm_gbs"],
+        "breakdown_ms": {"split_kernel": avg_split, "rest": statistics.mean(step_ms) - avg_split},
+        "roofline": {"bound": "hbm", "kernel": "decode_split", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "peak_source": f"{peak_src} HBM copy", "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": _committed_traffic(args.workload, "decode_split"), "algorithmic_bytes": nbytes},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "the key/value cache is the decoder's resident state; the step's query rows cross PCIe"},
+        "gpu_launches": K * DECODE_LAUNCHES_PER_STEP,
+        "clocks": clock_info,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = decode_cpu_baseline(wl, n)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
 def _committed_traffic(workload, kernel):
     """DRAM bytes per launch from the committed ncu summary, if one matches."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -438,13 +663,15 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS) + sorted(W.DECODE_WORKLOADS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU baseline leg")
     args = ap.parse_args(argv)
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, rank)
+    if args.workload in W.DECODE_WORKLOADS:
+        return run_gpu_decode(args, world, rank, local)
     return run_gpu(args, world, rank, local)
 
 

@@ -125,6 +125,27 @@ sinkattn_status sinkattn_bwd_noalloc(const sinkattn_problem* prob,
                                      const float* lse, const void* dout, const float* sink,
                                      void* dq, void* dk, void* dv, float* dsink, void* stream);
 
+/* Decode forward: the rollout side of the same attention (SinkFlex-RL,
+ * rollout worker: the policy samples turn by turn; GPT-OSS agentic RL page:
+ * the sink-aware forward of an inference FlashAttention fork).  `kv`
+ * describes the cached sequences exactly as `prob` does for sinkattn_fwd:
+ * k, v bf16 [kv->total_tokens, Hkv, 64] hold every position of each
+ * sequence.  q bf16 [num_seqs * q_per_seq, Hq, 64] holds, for sequence b,
+ * the queries of its last q_per_seq positions L_b - q_per_seq ... L_b - 1
+ * in that order (rows b * q_per_seq ...).  Writes o bf16 [num_seqs *
+ * q_per_seq, Hq, 64] and lse fp32 [Hq, num_seqs * q_per_seq], each row equal
+ * to the same row of sinkattn_fwd over the whole sequence (same mask, sink
+ * and lse).  Limits: 1 <= q_per_seq <= every sequence length,
+ * (Hq / Hkv) * q_per_seq <= 128 and num_seqs <= 4096, else
+ * SINKATTN_ERR_INVALID_ARG / SINKATTN_ERR_UNSUPPORTED.  The workspace
+ * (sinkattn_decode_workspace_size bytes, 16-byte aligned) holds the partial
+ * results of the key chunks; its size depends on the device's SM count. */
+size_t sinkattn_decode_workspace_size(const sinkattn_problem* kv, int32_t q_per_seq);
+sinkattn_status sinkattn_decode_fwd(const sinkattn_problem* kv, int32_t q_per_seq,
+                                    const void* q, const void* k, const void* v, const float* sink,
+                                    void* o, float* lse,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+
 /* Packed-sequence front end (multi-turn trajectories of different lengths,
  * SinkFlex-RL section 3).  seqlens: device int32 [num_seqs];
  * cu_seqlens_out: device int32 [num_seqs + 1] receives the exclusive prefix
@@ -149,8 +170,9 @@ sinkattn_status sinkattn_unpack(const void* packed, const int32_t* cu_seqlens, i
 sinkattn_status sinkattn_get_device_status(void* stream);
 
 /* Measurement hook.  kind 1 selects the forward attention kernel, kind 2
- * the backward main kernel.  With non-NULL `start` and `stop` (cudaEvent_t
- * handles passed as void*), every later sinkattn_fwd / sinkattn_bwd call
+ * the backward main kernel, kind 3 the key-chunk kernel of the decode
+ * forward.  With non-NULL `start` and `stop` (cudaEvent_t handles passed as
+ * void*), every later sinkattn_fwd / sinkattn_bwd / sinkattn_decode_fwd call
  * records `start` on its stream immediately before that kernel's launch and
  * `stop` immediately after it, so the caller can time the kernel alone with
  * cudaEventElapsedTime.  NULL for both clears the hook.  The setting is

@@ -9,12 +9,15 @@ from .api import (  # noqa: F401
     WINDOW_INF,
     SinkAttention,
     bwd_workspace_bytes,
+    decode_workspace_bytes,
     make_problem,
     sink_attention,
     sinkattn_bwd,
+    sinkattn_decode_fwd,
     sinkattn_fwd,
     sinkattn_get_device_status,
     PROFILE_BWD_MAIN,
+    PROFILE_DECODE,
     PROFILE_FWD,
     sinkattn_pack,
     sinkattn_set_profile_events,

@@ -45,6 +45,8 @@ SIGNATURES = {
     "sinkattn_fwd": (ctypes.c_int, [_PP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "sinkattn_bwd": (ctypes.c_int, [_PP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "sinkattn_bwd_noalloc": (ctypes.c_int, [_PP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "sinkattn_decode_workspace_size": (_sz, [_PP, _i32]),
+    "sinkattn_decode_fwd": (ctypes.c_int, [_PP, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "sinkattn_varlen_plan": (ctypes.c_int, [_vp, _i32, _vp, _vp]),
     "sinkattn_pack": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp]),
     "sinkattn_unpack": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp]),

@@ -35,9 +35,13 @@ def make_problem(q: torch.Tensor, k: torch.Tensor, *, num_seqs: Optional[int] = 
                  cu_seqlens: Optional[torch.Tensor] = None,
                  cu_seqlens_host: Optional[Sequence[int]] = None, max_seqlen: Optional[int] = None,
                  window: int = WINDOW_INF, prefix: int = 0, causal: bool = True,
-                 scale: Optional[float] = None):
-    """Build the C problem struct; returns (struct, keep-alive objects)."""
-    T, hq, d = q.shape
+                 scale: Optional[float] = None, total_tokens: Optional[int] = None):
+    """Build the C problem struct; returns (struct, keep-alive objects).
+
+    The sequences are those of q (T = q.shape[0]) unless ``total_tokens``
+    says otherwise (decode: the key/value cache holds the sequences)."""
+    _, hq, d = q.shape
+    T = q.shape[0] if total_tokens is None else int(total_tokens)
     hkv = k.shape[1]
     keep = []
     if cu_seqlens is None:
@@ -104,6 +108,37 @@ def sinkattn_bwd(q, k, v, o, lse, dout, sink, *, dq=None, dk=None, dv=None, dsin
     return dq, dk, dv, dsink
 
 
+def decode_workspace_bytes(q, k, *, q_per_seq: int, **problem) -> int:
+    lib = _lib.load()
+    pr, keep = make_problem(q, k, total_tokens=k.shape[0], **problem)
+    return int(lib.sinkattn_decode_workspace_size(ctypes.byref(pr), int(q_per_seq)))
+
+
+def sinkattn_decode_fwd(q, k, v, sink, *, q_per_seq: int, o=None, lse=None, workspace=None, **problem):
+    """Decode forward: returns (o, lse) for the last ``q_per_seq`` positions.
+
+    k, v [T_kv, Hkv, 64] hold every cached position of each sequence
+    (``num_seqs`` uniform sequences, or ``cu_seqlens``/``cu_seqlens_host``
+    offsets into k and v); q [num_seqs * q_per_seq, Hq, 64] holds the queries
+    of the last q_per_seq positions of each sequence in order.  Each output
+    row equals the same row of sinkattn_fwd over the whole sequence.
+    """
+    lib = _lib.load()
+    pr, keep = make_problem(q, k, total_tokens=k.shape[0], **problem)
+    R, hq, d = q.shape
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((hq, R), dtype=torch.float32, device=q.device)
+    ws_bytes = int(lib.sinkattn_decode_workspace_size(ctypes.byref(pr), int(q_per_seq)))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    st = lib.sinkattn_decode_fwd(ctypes.byref(pr), int(q_per_seq), _ptr(q), _ptr(k), _ptr(v), _ptr(sink), _ptr(o),
+                                 _ptr(lse), _ptr(workspace), workspace.numel(), _stream())
+    _lib.check("sinkattn_decode_fwd", st)
+    return o, lse
+
+
 def sinkattn_varlen_plan(seqlens: torch.Tensor) -> torch.Tensor:
     """Device int32 lengths [B] -> device int32 offsets [B + 1]."""
     lib = _lib.load()
@@ -138,12 +173,12 @@ def sinkattn_get_device_status() -> int:
     return int(_lib.load().sinkattn_get_device_status(_stream()))
 
 
-PROFILE_FWD, PROFILE_BWD_MAIN = 1, 2
+PROFILE_FWD, PROFILE_BWD_MAIN, PROFILE_DECODE = 1, 2, 3
 
 
 def sinkattn_set_profile_events(kind: int, start=None, stop=None) -> None:
     """Record torch.cuda.Event ``start``/``stop`` around the selected kernel
-    (PROFILE_FWD or PROFILE_BWD_MAIN) of every later call; None clears."""
+    (PROFILE_FWD, PROFILE_BWD_MAIN or PROFILE_DECODE) of every later call; None clears."""
     lib = _lib.load()
     ps = None if start is None else start.cuda_event
     pe = None if stop is None else stop.cuda_event

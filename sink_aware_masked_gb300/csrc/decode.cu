@@ -1,0 +1,497 @@
+// Decode (rollout-side) forward of sink-aware attention: the last n query
+// positions of each sequence against the sequence's whole key/value history.
+//
+// The pages' policy rollouts sample from the current policy turn by turn
+// (SinkFlex-RL, zh page, "Rollout worker"), and the GPT-OSS RL page takes the
+// sink-aware forward from an inference-engine FlashAttention fork ("GPT-OSS
+// agentic RL training", FlashAttention v3 implementation).  Same mask, sink
+// and lse as the full forward: every decode row equals the same row of the
+// full-sequence forward.
+//
+// Few query rows meet a long key history, so the work is a stream over K and
+// V bounded by HBM bandwidth (the 8 query heads of a GQA group share every
+// key: about 8 FLOP per byte at n = 1).  The key range of each (sequence, kv
+// head) is split into chunks of whole 128-key tiles (split-KV); one CTA per
+// (chunk, kv head) streams its tiles by TMA through a 3-stage mbarrier ring
+// and computes, for the group x n query rows, a partial online softmax
+// (running max m in log2 units, row sum l, unnormalised O) with warp-level
+// bf16 MMAs.  A second kernel merges the partials of each row,
+//     m = max m_i,  l = sum 2^{m_i - m} l_i,  O = sum 2^{m_i - m} O_i / l,
+// and only then applies the sink: lse = ln2 (m + log2 l), alpha =
+// sigmoid(lse - s_h), O <- alpha O (summary page, sink scaling of the output
+// by sigma(l - s_h)).
+//
+// Rows r of one (sequence, kv head): r = i * group + j is query position
+// L - n + i of query head g * group + j.  Warps split the rows into groups of
+// at most two 16-row blocks and the keys of each tile among the rest; the
+// warps that share rows are merged inside the CTA before the partial is
+// written.  Every mbarrier wait is bounded.
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+#include "tmap.h"
+
+#include <algorithm>
+#include <vector>
+
+namespace sa {
+namespace {
+
+using namespace tc;
+
+constexpr int D = kHeadDim;
+constexpr int BN = 128;           // keys per tile
+constexpr int NS = 3;             // K/V stages
+constexpr int NTHR = 128;
+constexpr int TILE = BN * D * 2;  // 16 KB
+constexpr int SMEM_DYN = NS * 2 * TILE + 1024;
+
+struct DecK {
+  CUtensorMap tm_k, tm_v;
+  const __nv_bfloat16* q;  // [B * n, Hq, 64]
+  float* ws_acc;           // [items * Hkv, R, 64] unnormalised O of each partial
+  float2* ws_ml;           // [items * Hkv, R]: (m in log2 units of the scaled score, l)
+  const int32_t* cu;       // key/value offsets or nullptr (uniform length kv_len)
+  int* status;
+  int kv_len;
+  int n, hq, hkv, group, R;
+  MaskParams mask;
+  float scale_log2;
+  int tiles_per_split;
+  int n_items;
+  uint32_t items[kDecodeMaxItems];  // sequence | (chunk << 16)
+};
+static_assert(sizeof(DecK) < 32000, "kernel parameter block too large");
+
+struct MergeK {
+  const float* ws_acc;
+  const float2* ws_ml;
+  const float* sink;
+  __nv_bfloat16* o;  // [B * n, Hq, 64]
+  float* lse;        // [Hq, B * n]
+  int num_seqs, n, hq, hkv, group, R;
+  uint16_t first[kDecodeMaxItems + 1];  // items of sequence b: [first[b], first[b + 1])
+};
+static_assert(sizeof(MergeK) < 32000, "kernel parameter block too large");
+
+// Key tiles that the query rows [L - n, L - 1] see: the prefix tiles below the
+// window, then the window/causal band (same arithmetic as the full forward).
+struct KeyTiles {
+  int lo_t, n_pre, n_tiles;
+  SA_DEV int k0(int j) const { return (j < n_pre ? j : lo_t + (j - n_pre)) * BN; }
+};
+
+SA_DEV KeyTiles key_tiles(int L, int n, const MaskParams& m) {
+  const KeyRange kr = key_range(L - n, L - 1, L, m);
+  KeyTiles t;
+  t.lo_t = kr.lo / BN;
+  t.n_pre = min((kr.pre_end + BN - 1) / BN, t.lo_t);
+  t.n_tiles = t.n_pre + (kr.hi / BN - t.lo_t + 1);
+  return t;
+}
+
+SA_DEV float quad_max(float x) {
+  x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
+  return fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
+}
+SA_DEV float quad_sum(float x) {
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+  return x + __shfl_xor_sync(0xffffffffu, x, 2);
+}
+
+// MB: 16-row blocks covering the R rows (1, 2, 4 or 8).
+template <int MB>
+__global__ void __launch_bounds__(NTHR) decode_split_kernel(const __grid_constant__ DecK p) {
+  constexpr int MBW = MB < 2 ? MB : 2;  // row blocks per warp
+  constexpr int WR = MB / MBW;          // warps splitting the rows
+  constexpr int WK = 4 / WR;            // warps splitting the keys of a tile
+  constexpr int KW = BN / WK;           // keys per warp per tile: 32, 64 or 128
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full[NS];
+  __shared__ int abort_flag;
+  __shared__ float red_m[4][32];  // per warp: running max of its (up to) 32 rows
+  __shared__ float red_l[4][32];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int wr = warp / WK, wk = warp % WK;
+  const int item_idx = blockIdx.x, g = blockIdx.y;
+  const uint32_t item = p.items[item_idx];
+  const int b = static_cast<int>(item & 0xFFFFu), split = static_cast<int>(item >> 16);
+  const SeqSpan sp = seq_span(p.cu, p.kv_len, b);
+  const int L = sp.len, n = p.n;
+  const KeyTiles kt = key_tiles(L, n, p.mask);
+  const int j0 = split * p.tiles_per_split, j1 = min(j0 + p.tiles_per_split, kt.n_tiles);
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  if (tid == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < NS; ++s) mbar_init(smem_u32(&full[s]), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const Abort ab{&abort_flag, p.status};
+  auto issue = [&](int j) {
+    const int s = (j - j0) % NS;
+    const uint32_t bar = smem_u32(&full[s]);
+    const int row = sp.start + kt.k0(j);
+    mbar_expect_tx(bar, 2 * TILE);
+    tma_load_2d(sb + s * 2 * TILE, &p.tm_k, g * D, row, bar);
+    tma_load_2d(sb + s * 2 * TILE + TILE, &p.tm_v, g * D, row, bar);
+  };
+  int issued = j0;  // tiles [j0, issued) have been requested
+  if (tid == 0) {
+    tma_prefetch_map(&p.tm_k);
+    tma_prefetch_map(&p.tm_v);
+    for (; issued < min(j0 + NS, j1); ++issued) issue(issued);
+  }
+
+  // Q fragments (A operand, row-major 16 x 16) of this warp's row blocks.
+  const int row0 = wr * MBW * 16;
+  uint32_t qa[MBW][4][4];
+#pragma unroll
+  for (int mb = 0; mb < MBW; ++mb)
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int r = row0 + mb * 16 + (lane >> 2) + 8 * hr;
+      const uint32_t* src = nullptr;
+      if (r < p.R) {
+        const int i = r / p.group, jh = r - i * p.group;
+        src = reinterpret_cast<const uint32_t*>(p.q + (static_cast<size_t>(b * n + i) * p.hq + g * p.group + jh) * D);
+      }
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        const int c = ks * 8 + (lane & 3);  // 32-bit word index of dims 2c, 2c + 1
+        qa[mb][ks][hr] = src ? __ldg(src + c) : 0u;
+        qa[mb][ks][2 + hr] = src ? __ldg(src + c + 4) : 0u;
+      }
+    }
+
+  float o_acc[MBW][8][4];
+  float m_run[MBW][2], l_run[MBW][2];
+#pragma unroll
+  for (int mb = 0; mb < MBW; ++mb) {
+#pragma unroll
+    for (int dn = 0; dn < 8; ++dn)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o_acc[mb][dn][e] = 0.f;
+    m_run[mb][0] = m_run[mb][1] = -INFINITY;
+    l_run[mb][0] = l_run[mb][1] = 0.f;
+  }
+  // Query position of each of this thread's rows (rows past R are padding).
+  int qpos[MBW][2];
+#pragma unroll
+  for (int mb = 0; mb < MBW; ++mb)
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) qpos[mb][hr] = L - n + (row0 + mb * 16 + (lane >> 2) + 8 * hr) / p.group;
+  const float sl2 = p.scale_log2;
+
+  bool failed = false;
+  int consumed = j0;
+  for (int j = j0; j < j1; ++j) {
+    const int s = (j - j0) % NS;
+    const bool ok = mbar_wait(smem_u32(&full[s]), ((j - j0) / NS) & 1, ab);
+    if (__syncthreads_or(!ok)) {
+      failed = true;
+      break;
+    }
+    const int k0 = kt.k0(j);
+    const uint32_t kb = sb + s * 2 * TILE, vb = kb + TILE;
+    const bool all_visible = block_full(L - n, n, k0, BN, L, p.mask);
+#pragma unroll 1
+    for (int sub = 0; sub < KW / 32; ++sub) {
+      const int kbase = wk * KW + sub * 32;  // first key of this 32-key block within the tile
+      float sacc[MBW][4][4];
+#pragma unroll
+      for (int mb = 0; mb < MBW; ++mb)
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sacc[mb][nt][e] = 0.f;
+      // S = Q K^T: B fragments from the key rows (ldmatrix, 8 keys x 8 dims per matrix).
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+        for (int np = 0; np < 2; ++np) {
+          const int m = lane >> 3;
+          const int key = kbase + (2 * np + (m >> 1)) * 8 + (lane & 7);
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4(kb + swz(key, 2 * ks + (m & 1)), r0, r1, r2, r3);
+#pragma unroll
+          for (int mb = 0; mb < MBW; ++mb) {
+            mma16816(sacc[mb][2 * np], qa[mb][ks], r0, r1);
+            mma16816(sacc[mb][2 * np + 1], qa[mb][ks], r2, r3);
+          }
+        }
+      // Online softmax in log2 units; element e of n-tile nt is key
+      // kbase + 8 nt + 2 (lane % 4) + (e & 1) of row half e >> 1.
+      uint32_t pa[MBW][2][4];
+#pragma unroll
+      for (int mb = 0; mb < MBW; ++mb) {
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          float x[8];
+#pragma unroll
+          for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              float v = sacc[mb][nt][2 * hr + e] * sl2;
+              if (!all_visible) {
+                const int key = k0 + kbase + 8 * nt + 2 * (lane & 3) + e;
+                if (!visible(qpos[mb][hr], key, L, p.mask)) v = -INFINITY;
+              }
+              x[2 * nt + e] = v;
+            }
+          float mx = x[0];
+#pragma unroll
+          for (int e = 1; e < 8; ++e) mx = fmaxf(mx, x[e]);
+          mx = quad_max(mx);
+          const float m_new = fmaxf(m_run[mb][hr], mx);
+          const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+          const float factor = ex2(m_run[mb][hr] - m_use);  // 0 while nothing was visible
+          m_run[mb][hr] = m_new;
+          float sum = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            x[e] = ex2(x[e] - m_use);
+            sum += x[e];
+          }
+          l_run[mb][hr] = l_run[mb][hr] * factor + sum;
+#pragma unroll
+          for (int dn = 0; dn < 8; ++dn) {
+            o_acc[mb][dn][2 * hr] *= factor;
+            o_acc[mb][dn][2 * hr + 1] *= factor;
+          }
+          // P as the A operand of P V: keys 16 kk + [0, 16) of this block.
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            pa[mb][kk][hr] = pack_bf16(x[4 * kk], x[4 * kk + 1]);
+            pa[mb][kk][2 + hr] = pack_bf16(x[4 * kk + 2], x[4 * kk + 3]);
+          }
+        }
+      }
+      // O += P V: B fragments from the value rows, transposed (ldmatrix.trans).
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+        for (int dp = 0; dp < 4; ++dp) {
+          const int m = lane >> 3;
+          const int key = kbase + 16 * kk + (m & 1) * 8 + (lane & 7);
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4_t(vb + swz(key, 2 * dp + (m >> 1)), r0, r1, r2, r3);
+#pragma unroll
+          for (int mb = 0; mb < MBW; ++mb) {
+            mma16816(o_acc[mb][2 * dp], pa[mb][kk], r0, r1);
+            mma16816(o_acc[mb][2 * dp + 1], pa[mb][kk], r2, r3);
+          }
+        }
+    }
+    consumed = j + 1;
+    __syncthreads();  // every warp is done with stage s
+    if (tid == 0 && issued < j1) {
+      issue(issued);
+      ++issued;
+    }
+  }
+  if (failed) {
+    // Let the copies still in flight land before the CTA leaves.
+    if (tid == 0)
+      for (int j = consumed; j < issued; ++j) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(smem_u32(&full[(j - j0) % NS]), ((j - j0) / NS) & 1))
+          if (clock64() - t0 > kTimeoutCycles) break;
+      }
+    return;
+  }
+
+  // Merge the warps that share rows: common maximum, then sums of l and O.
+#pragma unroll
+  for (int mb = 0; mb < MBW; ++mb)
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      l_run[mb][hr] = quad_sum(l_run[mb][hr]);
+      if ((lane & 3) == 0) red_m[warp][mb * 16 + (lane >> 2) + 8 * hr] = m_run[mb][hr];
+    }
+  __syncthreads();
+  float* acc_s = reinterpret_cast<float*>(smem);  // [WK][MB * 16][64]; the stages are no longer in use
+  constexpr int RP = MB * 16;
+#pragma unroll
+  for (int mb = 0; mb < MBW; ++mb)
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int rl = mb * 16 + (lane >> 2) + 8 * hr;  // row within the warp's block
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < WK; ++w) M = fmaxf(M, red_m[wr * WK + w][rl]);
+      const float sc = (m_run[mb][hr] == -INFINITY) ? 0.f : ex2(m_run[mb][hr] - M);
+      float* dst = acc_s + (static_cast<size_t>(wk) * RP + row0 + rl) * D + 2 * (lane & 3);
+#pragma unroll
+      for (int dn = 0; dn < 8; ++dn)
+        *reinterpret_cast<float2*>(dst + 8 * dn) =
+            make_float2(o_acc[mb][dn][2 * hr] * sc, o_acc[mb][dn][2 * hr + 1] * sc);
+      if ((lane & 3) == 0) red_l[warp][rl] = l_run[mb][hr] * sc;
+    }
+  __syncthreads();
+  const size_t part = static_cast<size_t>(item_idx) * p.hkv + g;
+  for (int idx = tid; idx < p.R * D; idx += NTHR) {
+    float a = 0.f;
+#pragma unroll
+    for (int w = 0; w < WK; ++w) a += acc_s[static_cast<size_t>(w) * RP * D + idx];
+    p.ws_acc[part * p.R * D + idx] = a;
+  }
+  for (int r = tid; r < p.R; r += NTHR) {
+    const int wr2 = r / (MBW * 16), rl = r - wr2 * MBW * 16;
+    float M = -INFINITY, l = 0.f;
+#pragma unroll
+    for (int w = 0; w < WK; ++w) {
+      M = fmaxf(M, red_m[wr2 * WK + w][rl]);
+      l += red_l[wr2 * WK + w][rl];
+    }
+    p.ws_ml[part * p.R + r] = make_float2(M, l);
+  }
+}
+
+// One warp per output row (sequence b, query i, head h): merge the partials,
+// apply the sink, write O (bf16) and lse.
+__global__ void __launch_bounds__(128) decode_merge_kernel(const __grid_constant__ MergeK p) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  const int rows = p.num_seqs * p.n * p.hq;
+  if (warp >= rows) return;
+  const int bn = warp / p.hq, h = warp - bn * p.hq;
+  const int b = bn / p.n, i = bn - b * p.n;
+  const int g = h / p.group, r = i * p.group + (h - g * p.group);
+  const int f0 = p.first[b], f1 = p.first[b + 1];
+  float M = -INFINITY;
+  for (int it = f0; it < f1; ++it) M = fmaxf(M, p.ws_ml[(static_cast<size_t>(it) * p.hkv + g) * p.R + r].x);
+  float l = 0.f;
+  float2 acc = make_float2(0.f, 0.f);
+  for (int it = f0; it < f1; ++it) {
+    const size_t part = static_cast<size_t>(it) * p.hkv + g;
+    const float2 ml = p.ws_ml[part * p.R + r];
+    const float w = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - M);
+    const float2 a = *reinterpret_cast<const float2*>(p.ws_acc + (part * p.R + r) * D + 2 * lane);
+    l += w * ml.y;
+    acc.x += w * a.x;
+    acc.y += w * a.y;
+  }
+  const float lse = (l > 0.f) ? (M + __log2f(l)) * kLn2 : -INFINITY;
+  const float alpha = 1.f / (1.f + ex2((__ldg(p.sink + h) - lse) * kLog2e));
+  const float fac = (l > 0.f) ? alpha / l : 0.f;
+  reinterpret_cast<uint32_t*>(p.o + (static_cast<size_t>(bn) * p.hq + h) * D)[lane] =
+      pack_bf16(acc.x * fac, acc.y * fac);
+  if (lane == 0) p.lse[static_cast<size_t>(h) * p.num_seqs * p.n + bn] = lse;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+}  // namespace
+
+DecodePlan decode_plan(const Problem& p, int n) {
+  DecodePlan pl;
+  const int sms = num_sms();
+  std::vector<int> tiles(p.num_seqs);
+  long long total = 0;
+  for (int b = 0; b < p.num_seqs; ++b) {
+    const int len = p.cu_host ? p.cu_host[b + 1] - p.cu_host[b] : p.seqlen;
+    // Same arithmetic as key_range() for query rows [len - n, len - 1].
+    const int q0 = len - n, hi = len - 1;
+    const int lo = (p.window < 0) ? 0 : std::max(0, q0 - p.window);
+    const int pre_end = std::max(0, std::min(std::min(p.prefix, lo), hi + 1));
+    const int lo_t = lo / BN;
+    const int n_pre = std::min((pre_end + BN - 1) / BN, lo_t);
+    tiles[b] = n_pre + (hi / BN - lo_t + 1);
+    total += tiles[b];
+  }
+  // About four CTAs per SM over all (chunk, kv head) pairs, at least two
+  // tiles per chunk, and no more items than the parameter block holds.
+  const long long want = std::max<long long>(1, 4LL * std::max(sms, 1) / std::max(p.hkv, 1));
+  int tps = static_cast<int>(std::max<long long>(2, (total + want - 1) / want));
+  for (;;) {
+    long long items = 0;
+    for (int b = 0; b < p.num_seqs; ++b) items += (tiles[b] + tps - 1) / tps;
+    if (items <= kDecodeMaxItems) break;
+    tps *= 2;
+  }
+  pl.tiles_per_split = tps;
+  pl.items.clear();
+  pl.first.assign(p.num_seqs + 1, 0);
+  for (int b = 0; b < p.num_seqs; ++b) {
+    pl.first[b] = static_cast<uint16_t>(pl.items.size());
+    const int chunks = (tiles[b] + tps - 1) / tps;
+    for (int c = 0; c < chunks; ++c) pl.items.push_back(static_cast<uint32_t>(b) | (static_cast<uint32_t>(c) << 16));
+  }
+  pl.first[p.num_seqs] = static_cast<uint16_t>(pl.items.size());
+  const int R = (p.hq / p.hkv) * n;
+  pl.acc_bytes = pl.items.size() * p.hkv * static_cast<size_t>(R) * D * 4;
+  pl.ml_bytes = pl.items.size() * p.hkv * static_cast<size_t>(R) * 8;
+  return pl;
+}
+
+cudaError_t launch_decode(const Problem& pr, int n, const DecodeArgs& a, const DecodePlan& pl, int* status,
+                          cudaStream_t stream) {
+  if (pr.num_seqs == 0) return cudaSuccess;
+  thread_local DecK k;
+  thread_local MergeK mk;
+  if (!make_rows_map(&k.tm_k, a.k, pr.total_tokens, pr.hkv, BN) ||
+      !make_rows_map(&k.tm_v, a.v, pr.total_tokens, pr.hkv, BN))
+    return cudaErrorInvalidValue;
+  const int group = pr.hq / pr.hkv, R = group * n;
+  k.q = static_cast<const __nv_bfloat16*>(a.q);
+  k.ws_acc = a.ws_acc;
+  k.ws_ml = reinterpret_cast<float2*>(a.ws_ml);
+  k.cu = pr.cu;
+  k.status = status;
+  k.kv_len = pr.seqlen;
+  k.n = n;
+  k.hq = pr.hq;
+  k.hkv = pr.hkv;
+  k.group = group;
+  k.R = R;
+  k.mask = MaskParams{pr.window, pr.prefix, pr.causal};
+  k.scale_log2 = pr.scale * kLog2e;
+  k.tiles_per_split = pl.tiles_per_split;
+  k.n_items = static_cast<int>(pl.items.size());
+  std::copy(pl.items.begin(), pl.items.end(), k.items);
+  const int mb = R <= 16 ? 1 : R <= 32 ? 2 : R <= 64 ? 4 : 8;
+  const dim3 grid(k.n_items, pr.hkv);
+  cudaError_t e = prof_begin(g_prof_dec, stream);
+  if (e != cudaSuccess) return e;
+  switch (mb) {
+#define SA_DECODE_CASE(MBV)                                                                                    \
+  case MBV:                                                                                                    \
+    if ((e = cudaFuncSetAttribute(decode_split_kernel<MBV>, cudaFuncAttributeMaxDynamicSharedMemorySize,      \
+                                  SMEM_DYN)) != cudaSuccess)                                                   \
+      return e;                                                                                                \
+    decode_split_kernel<MBV><<<grid, NTHR, SMEM_DYN, stream>>>(k);                                             \
+    break;
+    SA_DECODE_CASE(1)
+    SA_DECODE_CASE(2)
+    SA_DECODE_CASE(4)
+    SA_DECODE_CASE(8)
+#undef SA_DECODE_CASE
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = prof_end(g_prof_dec, stream)) != cudaSuccess) return e;
+  mk.ws_acc = a.ws_acc;
+  mk.ws_ml = reinterpret_cast<const float2*>(a.ws_ml);
+  mk.sink = a.sink;
+  mk.o = static_cast<__nv_bfloat16*>(a.o);
+  mk.lse = a.lse;
+  mk.num_seqs = pr.num_seqs;
+  mk.n = n;
+  mk.hq = pr.hq;
+  mk.hkv = pr.hkv;
+  mk.group = group;
+  mk.R = R;
+  std::copy(pl.first.begin(), pl.first.end(), mk.first);
+  const long long rows = static_cast<long long>(pr.num_seqs) * n * pr.hq;
+  decode_merge_kernel<<<static_cast<int>((rows * 32 + 127) / 128), 128, 0, stream>>>(mk);
+  return cudaGetLastError();
+}
+
+}  // namespace sa

@@ -74,11 +74,37 @@ int bwd_qchunk(const Problem& p);
 std::vector<BwdItem> bwd_work_list(const Problem& p, int qchunk);
 bool bwd_any_split(const std::vector<BwdItem>& items);
 
+// Decode forward (decode.cu): the last n query rows of each sequence against
+// its whole key/value history, split over the keys and merged afterwards.
+constexpr int kDecodeMaxItems = 4096;  // (sequence, key chunk) items per launch
+
+struct DecodeArgs {
+  const void* q;  // [B * n, Hq, 64]
+  const void* k;  // [T_kv, Hkv, 64]
+  const void* v;
+  const float* sink;
+  void* o;        // [B * n, Hq, 64]
+  float* lse;     // [Hq, B * n]
+  float* ws_acc;  // partial unnormalised outputs
+  void* ws_ml;    // partial (max, sum) pairs
+};
+
+struct DecodePlan {
+  int tiles_per_split = 0;
+  std::vector<uint32_t> items;   // sequence | (chunk << 16), sequence-major
+  std::vector<uint16_t> first;   // items of sequence b: [first[b], first[b + 1])
+  size_t acc_bytes = 0, ml_bytes = 0;
+};
+
+DecodePlan decode_plan(const Problem& p, int n);
+cudaError_t launch_decode(const Problem& p, int n, const DecodeArgs& a, const DecodePlan& pl, int* status,
+                          cudaStream_t s);
+
 // Optional events recorded around the main kernels (measurement hook).
 struct ProfileEvents {
   cudaEvent_t start = nullptr, stop = nullptr;
 };
-extern ProfileEvents g_prof_fwd, g_prof_bwd;
+extern ProfileEvents g_prof_fwd, g_prof_bwd, g_prof_dec;
 
 inline cudaError_t prof_begin(const ProfileEvents& e, cudaStream_t s) {
   return e.start ? cudaEventRecord(e.start, s) : cudaSuccess;

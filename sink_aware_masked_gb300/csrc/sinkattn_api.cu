@@ -10,7 +10,7 @@
 #include "tc.cuh"
 
 namespace sa {
-ProfileEvents g_prof_fwd, g_prof_bwd;
+ProfileEvents g_prof_fwd, g_prof_bwd, g_prof_dec;
 }
 
 namespace {
@@ -193,6 +193,67 @@ sinkattn_status sinkattn_bwd(const sinkattn_problem* prob, const void* q, const 
   return from_cuda(sa::launch_bwd(p, a, status, static_cast<cudaStream_t>(stream)));
 }
 
+}  // extern "C"
+
+namespace {
+
+struct DecodeLayout {
+  sa::DecodePlan plan;
+  size_t acc, ml, total;
+};
+
+// Validates the decode-specific arguments on top of normalise().
+sinkattn_status decode_check(const sa::Problem& p, int32_t q_per_seq) {
+  if (q_per_seq < 1) return SINKATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(p.hq / p.hkv) * q_per_seq > 128) return SINKATTN_ERR_UNSUPPORTED;
+  if (p.num_seqs > sa::kDecodeMaxItems) return SINKATTN_ERR_UNSUPPORTED;
+  for (int b = 0; b < p.num_seqs; ++b) {
+    const int len = p.cu_host ? p.cu_host[b + 1] - p.cu_host[b] : p.seqlen;
+    if (len < q_per_seq) return SINKATTN_ERR_INVALID_ARG;
+  }
+  return SINKATTN_OK;
+}
+
+DecodeLayout decode_layout(const sa::Problem& p, int32_t q_per_seq) {
+  DecodeLayout l;
+  l.plan = sa::decode_plan(p, q_per_seq);
+  l.acc = 0;
+  l.ml = round_up(l.plan.acc_bytes, 256);
+  l.total = l.ml + round_up(l.plan.ml_bytes, 256) + 256;
+  return l;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t sinkattn_decode_workspace_size(const sinkattn_problem* kv, int32_t q_per_seq) {
+  sa::Problem p;
+  if (normalise(kv, p) != SINKATTN_OK || decode_check(p, q_per_seq) != SINKATTN_OK) return 0;
+  return decode_layout(p, q_per_seq).total;
+}
+
+sinkattn_status sinkattn_decode_fwd(const sinkattn_problem* kv, int32_t q_per_seq, const void* q, const void* k,
+                                    const void* v, const float* sink, void* o, float* lse, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  sa::Problem p;
+  sinkattn_status st = normalise(kv, p);
+  if (st != SINKATTN_OK) return st;
+  if ((st = decode_check(p, q_per_seq)) != SINKATTN_OK) return st;
+  if (p.num_seqs == 0) return SINKATTN_OK;
+  if (!q || !k || !v || !sink || !o || !lse) return SINKATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(sink))
+    return SINKATTN_ERR_ALIGNMENT;
+  const DecodeLayout L = decode_layout(p, q_per_seq);
+  if (workspace_bytes < L.total) return SINKATTN_ERR_WORKSPACE;
+  if (workspace == nullptr || !aligned16(workspace)) return workspace ? SINKATTN_ERR_ALIGNMENT : SINKATTN_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  sa::DecodeArgs a{q, k, v, sink, o, lse, reinterpret_cast<float*>(ws + L.acc), ws + L.ml};
+  int* status = status_word();
+  if (status == nullptr) return SINKATTN_ERR_CUDA;
+  return from_cuda(sa::launch_decode(p, q_per_seq, a, L.plan, status, static_cast<cudaStream_t>(stream)));
+}
+
 sinkattn_status sinkattn_varlen_plan(const int32_t* seqlens, int32_t num_seqs, int32_t* cu_seqlens_out,
                                      void* stream) {
   if (num_seqs < 0 || cu_seqlens_out == nullptr || (num_seqs > 0 && seqlens == nullptr))
@@ -241,6 +302,8 @@ sinkattn_status sinkattn_set_profile_events(int32_t kind, void* start, void* sto
     sa::g_prof_fwd = ev;
   else if (kind == 2)
     sa::g_prof_bwd = ev;
+  else if (kind == 3)
+    sa::g_prof_dec = ev;
   else
     return SINKATTN_ERR_INVALID_ARG;
   return SINKATTN_OK;

@@ -135,3 +135,25 @@ def test_pack_validation(lib):
     assert lib.sinkattn_unpack(FAKE + 4, FAKE, 2, 4, 2, 64, FAKE, None) == 3
     assert lib.sinkattn_varlen_plan(FAKE, -3, FAKE, None) == 1
     assert lib.sinkattn_varlen_plan(None, 3, FAKE, None) == 1
+
+
+@pytest.mark.parametrize("n,kw,status", [
+    (0, {}, 1),                                        # no query rows
+    (33, {}, 2),                                       # 4 heads per group x 33 rows > 128
+    (20, dict(seqlen=16, total_tokens=16), 1),         # more query rows than cached positions
+    (1, dict(head_dim=128), 2),
+    (1, dict(num_seqs=4097, seqlen=1, total_tokens=4097), 2),
+])
+def test_decode_validation(lib, n, kw, status):
+    pr = problem(**kw)
+    assert lib.sinkattn_decode_fwd(ctypes.byref(pr), n, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, None) == status
+    assert lib.sinkattn_decode_workspace_size(ctypes.byref(pr), n) == 0
+
+
+def test_decode_pointers_and_workspace(lib):
+    pr = problem()
+    ws = lib.sinkattn_decode_workspace_size(ctypes.byref(pr), 2)
+    assert ws > 0
+    assert lib.sinkattn_decode_fwd(ctypes.byref(pr), 2, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws, None) == 1
+    assert lib.sinkattn_decode_fwd(ctypes.byref(pr), 2, FAKE, FAKE + 4, FAKE, FAKE, FAKE, FAKE, FAKE, ws, None) == 3
+    assert lib.sinkattn_decode_fwd(ctypes.byref(pr), 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws - 1, None) == 4

@@ -4,6 +4,7 @@ gloo ranks on 127.0.0.1."""
 import os
 import socket
 
+import numpy as np
 import pytest
 import torch
 import torch.distributed as dist
@@ -68,3 +69,16 @@ def test_two_rank_max_reduction():
         assert p.exitcode == 0
     for r in range(world):
         assert out[r] == [2.0, 10.0]
+
+
+@pytest.mark.parametrize("lens,n,window,prefix", [((300, 1, 129), 1, -1, 0), ((700, 2048), 4, 128, 4),
+                                                  ((513,), 8, 64, 600), ((90,), 3, 0, 0)])
+def test_decode_visible_keys_match_mask_enumeration(lens, n, window, prefix):
+    import oracle
+
+    wl = W.custom(lens, 4, 2, window=window, prefix=prefix)
+    want = 0
+    for L in lens:
+        m = oracle.visible(np.arange(L - n, L), np.arange(L), window, prefix, True)
+        want += int(np.count_nonzero(m.any(axis=0)))
+    assert bench.decode_visible_keys(wl, n) == want

@@ -1,0 +1,80 @@
+"""Decode forward (last rows of each sequence against its key/value history):
+CUDA path vs the CPU float64 oracle, element by element (needs a GB300)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from tests import parity_util as pu
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from sink_aware_masked_gb300 import build
+
+    build.build()
+
+
+def run_decode(wl, n, sink=None):
+    import sink_aware_masked_gb300 as sa
+
+    inp = W.make_decode_inputs(wl, n)
+    q = inp.q_bf16
+    s = inp.sink if sink is None else sink
+    kw = dict(window=wl.window, prefix=wl.prefix, causal=wl.causal, scale=wl.scale)
+    if wl.uniform:
+        kw["num_seqs"] = wl.num_seqs
+    else:
+        cu = wl.cu_seqlens()
+        kw.update(cu_seqlens=torch.tensor(cu, dtype=torch.int32, device=DEV), cu_seqlens_host=[int(x) for x in cu],
+                  max_seqlen=wl.max_seqlen)
+    o, lse = sa.sinkattn_decode_fwd(q.to(DEV), inp.k_bf16.to(DEV), inp.v_bf16.to(DEV), s.to(DEV), q_per_seq=n, **kw)
+    assert sa.sinkattn_get_device_status() == 0
+    ref_o, ref_lse = oracle.decode_forward(q.to(torch.float64).numpy(), inp.f64("k"), inp.f64("v"),
+                                           s.to(torch.float64).numpy(), wl.cu_seqlens(), n, wl.window, wl.prefix,
+                                           wl.causal, wl.scale)
+    return o.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_lse
+
+
+CASES = [
+    # seqlens, hq, hkv, rows per sequence, window, prefix, seed
+    ((1000, 1000), 16, 2, 1, -1, 0, 91),           # ragged last tile, 8 rows per kv head
+    ((300, 1, 129, 2000), 16, 2, 1, -1, 0, 92),     # packed, a one-token sequence, a 129-token one
+    ((700, 2048), 16, 2, 4, 128, 4, 93),            # 32 rows, window and prefix
+    ((513,), 16, 2, 8, 64, 0, 94),                  # 64 rows
+    ((900, 129), 16, 2, 16, -1, 7, 95),             # 128 rows (the largest supported)
+    ((4096, 4096, 4096), 64, 8, 2, -1, 0, 97),      # 64/8 heads
+    ((32768,), 64, 8, 1, -1, 0, 96),                # long history split over many chunks
+    ((3000,), 12, 4, 3, 10, 2000, 98),              # group of 3, prefix wider than the window
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"L{'-'.join(map(str, c[0]))}_h{c[1]}x{c[2]}_n{c[3]}_w{c[4]}")
+def test_decode_matches_oracle(case):
+    lens, hq, hkv, n, w, p, seed = case
+    wl = W.custom(lens, hq, hkv, window=w, prefix=p, seed=seed, sink_dist="uniform2")
+    o, lse, ref_o, ref_lse = run_decode(wl, n)
+    assert pu.max_abs(o, ref_o) <= pu.TOL["o"], pu.max_abs(o, ref_o)
+    assert pu.max_abs(lse, ref_lse) <= pu.TOL["lse"], pu.max_abs(lse, ref_lse)
+
+
+def test_decode_sink_limits():
+    wl = W.custom((600, 257), 16, 2, seed=99)
+    hq = wl.num_heads_q
+    o, lse, ref_o, ref_lse = run_decode(wl, 2, sink=torch.full((hq,), float("inf")))
+    assert np.all(o == 0.0) and pu.max_abs(lse, ref_lse) <= pu.TOL["lse"]
+    o, lse, ref_o, ref_lse = run_decode(wl, 2, sink=torch.full((hq,), float("-inf")))
+    assert pu.max_abs(o, ref_o) <= pu.TOL["o"] and pu.max_abs(lse, ref_lse) <= pu.TOL["lse"]
+
+
+@pytest.mark.parametrize("name", sorted(W.DECODE_WORKLOADS))
+def test_decode_workloads_sampled(name):
+    """Full-size decode workloads, checked on every row of every head."""
+    wl, n = W.DECODE_WORKLOADS[name]
+    o, lse, ref_o, ref_lse = run_decode(wl, n)
+    assert pu.max_abs(o, ref_o) <= pu.TOL["o"], pu.max_abs(o, ref_o)
+    assert pu.max_abs(lse, ref_lse) <= pu.TOL["lse"], pu.max_abs(lse, ref_lse)

@@ -150,3 +150,49 @@ def random_lengths(n: int, lo: int, hi: int, seed: int) -> List[int]:
     """Seeded sequence lengths, uniform in [lo, hi]."""
     g = torch.Generator().manual_seed(seed)
     return [int(x) for x in torch.randint(lo, hi + 1, (n,), generator=g)]
+
+
+@dataclasses.dataclass
+class DecodeInputs:
+    """Inputs of one decode step: the key/value cache of every sequence and the
+    queries of its last ``n`` positions (rows b * n ... b * n + n - 1)."""
+
+    wl: Workload
+    n: int
+    q_bf16: torch.Tensor     # [B * n, Hq, D]
+    k_bf16: torch.Tensor     # [T, Hkv, D]
+    v_bf16: torch.Tensor     # [T, Hkv, D]
+    sink: torch.Tensor       # [Hq] float32
+
+    def f64(self, name: str) -> np.ndarray:
+        t = getattr(self, name + "_bf16") if name != "sink" else self.sink
+        return t.to(torch.float64).numpy()
+
+
+def make_decode_inputs(wl: Workload, n: int) -> DecodeInputs:
+    """Draw a decode step from the workload's seed: k, v, q, sink in that order."""
+    g = torch.Generator().manual_seed(wl.seed)
+    T, hq, hkv, d = wl.total_tokens, wl.num_heads_q, wl.num_heads_kv, wl.head_dim
+    k = torch.randn((T, hkv, d), generator=g, dtype=torch.float32)
+    v = torch.randn((T, hkv, d), generator=g, dtype=torch.float32)
+    q = torch.randn((wl.num_seqs * n, hq, d), generator=g, dtype=torch.float32)
+    if wl.sink_dist == "normal":
+        sink = torch.randn((hq,), generator=g, dtype=torch.float32)
+    elif wl.sink_dist == "uniform2":
+        sink = torch.rand((hq,), generator=g, dtype=torch.float32) * 4.0 - 2.0
+    else:
+        raise ValueError(wl.sink_dist)
+    return DecodeInputs(wl, n, q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16), sink)
+
+
+# Rollout-side decode steps: one new query row per sequence against long
+# cached histories (the policy samples turn by turn), on the same head
+# layout.  name -> (workload holding the cached sequences, query rows per sequence).
+DECODE_WORKLOADS = {
+    "decode_b32_kv8192": (_uniform("decode_b32_kv8192", 32, 8192, 64, 8, WINDOW_INF, 0, 6, "uniform2"), 1),
+    "decode_b32_kv8192_w128_p4": (
+        _uniform("decode_b32_kv8192_w128_p4", 32, 8192, 64, 8, 128, 4, 6, "uniform2"), 1),
+    "decode_varlen8": (Workload("decode_varlen8", VARLEN_LENGTHS, 64, 8, 64, WINDOW_INF, 0, True, 7,
+                                "uniform2", uniform=False), 1),
+    "decode_b8_kv32768_n4": (_uniform("decode_b8_kv32768_n4", 8, 32768, 64, 8, WINDOW_INF, 0, 8, "uniform2"), 4),
+}
