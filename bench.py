@@ -11,7 +11,7 @@ resident in HBM; L2 is flushed (256 MiB write) before every timed step, and
 each step is timed alone with CUDA events on the stream the kernels run on.
 
 Decode workloads (``--workload decode_*``): one step = one decode forward
-(key-chunk kernel + merge kernel) of the workload's query rows against the
+(one key-chunk kernel that also merges) of the workload's query rows against the
 key/value cache of every sequence, reported in GB/s of algorithmic HBM
 traffic (the visible keys and values once, the queries, O and lse).
 
@@ -48,7 +48,7 @@ FLOP_BWD_PER_PAIR = 10 * 64
 L2_FLUSH_BYTES = 256 << 20
 LAUNCHES_PER_STEP = 4  # forward, backward preprocess, backward main, dQ convert
 DECODE_METRIC = "sink-attn decode GB/s (bf16 KV-cache stream) and % of measured HBM copy bandwidth"
-DECODE_LAUNCHES_PER_STEP = 2  # key-chunk kernel, merge kernel
+DECODE_LAUNCHES_PER_STEP = 1  # key-chunk kernel (the last chunk of each sequence merges)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -540,7 +540,7 @@ def run_gpu_decode(args, world, rank, local):
     prob.update(window=wl.window, prefix=wl.prefix, causal=wl.causal, scale=wl.scale)
     o = torch.empty_like(q)
     lse = torch.empty((wl.num_heads_q, q.shape[0]), dtype=torch.float32, device=dev)
-    ws = torch.empty(max(16, sa.decode_workspace_bytes(q, k, q_per_seq=n, **prob)), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(max(16, sa.decode_workspace_bytes(q, k, q_per_seq=n, **prob)), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     def step():

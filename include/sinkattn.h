@@ -139,7 +139,12 @@ sinkattn_status sinkattn_bwd_noalloc(const sinkattn_problem* prob,
  * (Hq / Hkv) * q_per_seq <= 128 and num_seqs <= 4096, else
  * SINKATTN_ERR_INVALID_ARG / SINKATTN_ERR_UNSUPPORTED.  The workspace
  * (sinkattn_decode_workspace_size bytes, 16-byte aligned) holds the partial
- * results of the key chunks; its size depends on the device's SM count. */
+ * results of the key chunks and one counter per (sequence, kv head); its
+ * size depends on the device's SM count.  Its first 4 * num_seqs * Hkv bytes
+ * (the counters) must be zero before the first call; every completed call
+ * leaves them zero, so a workspace zero-filled once can be reused by later
+ * calls (not by calls that overlap on the GPU).  After SINKATTN_ERR_TIMEOUT,
+ * zero the workspace again. */
 size_t sinkattn_decode_workspace_size(const sinkattn_problem* kv, int32_t q_per_seq);
 sinkattn_status sinkattn_decode_fwd(const sinkattn_problem* kv, int32_t q_per_seq,
                                     const void* q, const void* k, const void* v, const float* sink,

@@ -132,7 +132,8 @@ def sinkattn_decode_fwd(q, k, v, sink, *, q_per_seq: int, o=None, lse=None, work
         lse = torch.empty((hq, R), dtype=torch.float32, device=q.device)
     ws_bytes = int(lib.sinkattn_decode_workspace_size(ctypes.byref(pr), int(q_per_seq)))
     if workspace is None:
-        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+        # zero-filled: the chunk counters at its start must be zero (each call leaves them so)
+        workspace = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
     st = lib.sinkattn_decode_fwd(ctypes.byref(pr), int(q_per_seq), _ptr(q), _ptr(k), _ptr(v), _ptr(sink), _ptr(o),
                                  _ptr(lse), _ptr(workspace), workspace.numel(), _stream())
     _lib.check("sinkattn_decode_fwd", st)

@@ -15,11 +15,14 @@
 // (chunk, kv head) streams its tiles by TMA through a 3-stage mbarrier ring
 // and computes, for the group x n query rows, a partial online softmax
 // (running max m in log2 units, row sum l, unnormalised O) with warp-level
-// bf16 MMAs.  A second kernel merges the partials of each row,
+// bf16 MMAs.  The last CTA of a (sequence, kv head) to finish (a counter in
+// the workspace, incremented after the partial is written and fenced) merges
+// the partials of each row,
 //     m = max m_i,  l = sum 2^{m_i - m} l_i,  O = sum 2^{m_i - m} O_i / l,
 // and only then applies the sink: lse = ln2 (m + log2 l), alpha =
 // sigmoid(lse - s_h), O <- alpha O (summary page, sink scaling of the output
-// by sigma(l - s_h)).
+// by sigma(l - s_h)); it then clears the counter for the next call.  The
+// chunks of a sequence hold equal numbers of tiles (within one).
 //
 // Rows r of one (sequence, kv head): r = i * group + j is query position
 // L - n + i of query head g * group + j.  Warps split the rows into groups of
@@ -49,30 +52,25 @@ constexpr int SMEM_DYN = NS * 2 * TILE + 1024;
 struct DecK {
   CUtensorMap tm_k, tm_v;
   const __nv_bfloat16* q;  // [B * n, Hq, 64]
+  const float* sink;
+  __nv_bfloat16* o;        // [B * n, Hq, 64]
+  float* lse;              // [Hq, B * n]
+  int* counters;           // [B * Hkv] chunks finished; zero between calls
   float* ws_acc;           // [items * Hkv, R, 64] unnormalised O of each partial
-  float2* ws_ml;           // [items * Hkv, R]: (m in log2 units of the scaled score, l)
+  float2* ws_ml;           // [items * Hkv, Rml]: (m in log2 units of the scaled score, l)
   const int32_t* cu;       // key/value offsets or nullptr (uniform length kv_len)
   int* status;
   int kv_len;
   int n, hq, hkv, group, R;
+  int Rml;                 // R rounded up to even: (max, sum) blocks are whole 16-byte units
   MaskParams mask;
   float scale_log2;
-  int tiles_per_split;
+  int num_seqs;
+  int tiles_per_split;  // chunks of a sequence: ceil(tiles / tiles_per_split), equal shares
   int n_items;
-  uint32_t items[kDecodeMaxItems];  // sequence | (chunk << 16)
+  uint32_t items[kDecodeMaxItems];  // sequence | (chunk << 16), chunks of a sequence consecutive
 };
 static_assert(sizeof(DecK) < 32000, "kernel parameter block too large");
-
-struct MergeK {
-  const float* ws_acc;
-  const float2* ws_ml;
-  const float* sink;
-  __nv_bfloat16* o;  // [B * n, Hq, 64]
-  float* lse;        // [Hq, B * n]
-  int num_seqs, n, hq, hkv, group, R;
-  uint16_t first[kDecodeMaxItems + 1];  // items of sequence b: [first[b], first[b + 1])
-};
-static_assert(sizeof(MergeK) < 32000, "kernel parameter block too large");
 
 // Key tiles that the query rows [L - n, L - 1] see: the prefix tiles below the
 // window, then the window/causal band (same arithmetic as the full forward).
@@ -108,6 +106,7 @@ __global__ void __launch_bounds__(NTHR) decode_split_kernel(const __grid_constan
   constexpr int KW = BN / WK;           // keys per warp per tile: 32, 64 or 128
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full[NS];
+  __shared__ uint64_t merge_bar;
   __shared__ int abort_flag;
   __shared__ float red_m[4][32];  // per warp: running max of its (up to) 32 rows
   __shared__ float red_l[4][32];
@@ -120,13 +119,15 @@ __global__ void __launch_bounds__(NTHR) decode_split_kernel(const __grid_constan
   const SeqSpan sp = seq_span(p.cu, p.kv_len, b);
   const int L = sp.len, n = p.n;
   const KeyTiles kt = key_tiles(L, n, p.mask);
-  const int j0 = split * p.tiles_per_split, j1 = min(j0 + p.tiles_per_split, kt.n_tiles);
+  const int nsplit = (kt.n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+  const int j0 = split * kt.n_tiles / nsplit, j1 = (split + 1) * kt.n_tiles / nsplit;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
   if (tid == 0) {
     abort_flag = 0;
     for (int s = 0; s < NS; ++s) mbar_init(smem_u32(&full[s]), 1);
+    mbar_init(smem_u32(&merge_bar), 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -347,39 +348,93 @@ __global__ void __launch_bounds__(NTHR) decode_split_kernel(const __grid_constan
       M = fmaxf(M, red_m[wr2 * WK + w][rl]);
       l += red_l[wr2 * WK + w][rl];
     }
-    p.ws_ml[part * p.R + r] = make_float2(M, l);
+    p.ws_ml[part * p.Rml + r] = make_float2(M, l);
   }
-}
 
-// One warp per output row (sequence b, query i, head h): merge the partials,
-// apply the sink, write O (bf16) and lse.
-__global__ void __launch_bounds__(128) decode_merge_kernel(const __grid_constant__ MergeK p) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  const int rows = p.num_seqs * p.n * p.hq;
-  if (warp >= rows) return;
-  const int bn = warp / p.hq, h = warp - bn * p.hq;
-  const int b = bn / p.n, i = bn - b * p.n;
-  const int g = h / p.group, r = i * p.group + (h - g * p.group);
-  const int f0 = p.first[b], f1 = p.first[b + 1];
-  float M = -INFINITY;
-  for (int it = f0; it < f1; ++it) M = fmaxf(M, p.ws_ml[(static_cast<size_t>(it) * p.hkv + g) * p.R + r].x);
-  float l = 0.f;
-  float2 acc = make_float2(0.f, 0.f);
-  for (int it = f0; it < f1; ++it) {
-    const size_t part = static_cast<size_t>(it) * p.hkv + g;
-    const float2 ml = p.ws_ml[part * p.R + r];
-    const float w = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - M);
-    const float2 a = *reinterpret_cast<const float2*>(p.ws_acc + (part * p.R + r) * D + 2 * lane);
-    l += w * ml.y;
-    acc.x += w * a.x;
-    acc.y += w * a.y;
+  // The last chunk of this (sequence, kv head) to finish merges all of them.
+  __shared__ int is_last;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) is_last = atomicAdd(p.counters + b * p.hkv + g, 1) == nsplit - 1;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  // Partials of chunk c: O at ws_acc + (part0 + c Hkv) R 64, (max, sum) at
+  // ws_ml + (part0 + c Hkv) Rml.  They are staged in batches through the
+  // (now idle) stage buffers by bulk copies, then merged from shared memory
+  // with an online rescale per (row, dim pair) unit.
+  const size_t part0 = static_cast<size_t>(item_idx - split) * p.hkv + g;
+  const uint32_t blk_acc = static_cast<uint32_t>(p.R) * D * 4, blk_ml = static_cast<uint32_t>(p.Rml) * 8;
+  const int per_batch = max(1, (NS * 2 * TILE) / static_cast<int>(blk_acc + blk_ml));
+  constexpr int UP = MB * 4;  // units per thread: (MB * 16 rows) x 32 dim pairs / 128 threads
+  float2 acc[UP];
+  float Mu[UP], lu[UP];
+#pragma unroll
+  for (int k = 0; k < UP; ++k) {
+    acc[k] = make_float2(0.f, 0.f);
+    Mu[k] = -INFINITY;
+    lu[k] = 0.f;
   }
-  const float lse = (l > 0.f) ? (M + __log2f(l)) * kLn2 : -INFINITY;
-  const float alpha = 1.f / (1.f + ex2((__ldg(p.sink + h) - lse) * kLog2e));
-  const float fac = (l > 0.f) ? alpha / l : 0.f;
-  reinterpret_cast<uint32_t*>(p.o + (static_cast<size_t>(bn) * p.hq + h) * D)[lane] =
-      pack_bf16(acc.x * fac, acc.y * fac);
-  if (lane == 0) p.lse[static_cast<size_t>(h) * p.num_seqs * p.n + bn] = lse;
+  const float* stg_acc = reinterpret_cast<const float*>(smem);
+  const float2* ml_s = reinterpret_cast<const float2*>(smem + per_batch * blk_acc);
+  if (tid == 0) fence_proxy_async_global();  // the partials were written through the generic proxy
+  for (int c0 = 0, batch = 0; c0 < nsplit; c0 += per_batch, ++batch) {
+    const int cnt = min(per_batch, nsplit - c0);
+    const uint32_t bar = smem_u32(&merge_bar);
+    if (tid == 0) {
+      mbar_expect_tx(bar, cnt * (blk_acc + blk_ml));
+      for (int c = 0; c < cnt; ++c) {
+        const size_t pc = part0 + static_cast<size_t>(c0 + c) * p.hkv;
+        bulk_load(sb + c * blk_acc, p.ws_acc + pc * p.R * D, blk_acc, bar);
+        bulk_load(sb + per_batch * blk_acc + c * blk_ml, p.ws_ml + pc * p.Rml, blk_ml, bar);
+      }
+    }
+    const bool ok = mbar_wait(bar, batch & 1, ab);
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) {  // let the copies still in flight land before the CTA leaves
+        const long long t0 = clock64();
+        while (!mbar_try_wait(bar, batch & 1) && clock64() - t0 < kTimeoutCycles) {
+        }
+      }
+      return;
+    }
+#pragma unroll
+    for (int k = 0; k < UP; ++k) {
+      const int u = tid + NTHR * k, r = u >> 5, d2 = u & 31;
+      if (r >= p.R) continue;
+      for (int c = 0; c < cnt; ++c) {
+        const float2 mv = ml_s[c * p.Rml + r];
+        if (mv.x == -INFINITY) continue;
+        if (mv.x > Mu[k]) {
+          const float sc = (Mu[k] == -INFINITY) ? 0.f : ex2(Mu[k] - mv.x);
+          acc[k].x *= sc;
+          acc[k].y *= sc;
+          lu[k] *= sc;
+          Mu[k] = mv.x;
+        }
+        const float w = ex2(mv.x - Mu[k]);
+        const float2 a = reinterpret_cast<const float2*>(stg_acc + (static_cast<size_t>(c) * p.R + r) * D)[d2];
+        acc[k].x += w * a.x;
+        acc[k].y += w * a.y;
+        lu[k] += w * mv.y;
+      }
+    }
+    __syncthreads();  // the next batch overwrites the staging buffers
+  }
+#pragma unroll
+  for (int k = 0; k < UP; ++k) {
+    const int u = tid + NTHR * k, r = u >> 5, d2 = u & 31;
+    if (r >= p.R) continue;
+    const float l = lu[k], M = Mu[k];
+    const int i = r / p.group, h = g * p.group + (r - i * p.group), bn = b * n + i;
+    const float lse = (l > 0.f) ? (M + __log2f(l)) * kLn2 : -INFINITY;
+    const float alpha = 1.f / (1.f + ex2((__ldg(p.sink + h) - lse) * kLog2e));
+    const float fac = (l > 0.f) ? alpha / l : 0.f;
+    reinterpret_cast<uint32_t*>(p.o + (static_cast<size_t>(bn) * p.hq + h) * D)[d2] =
+        pack_bf16(acc[k].x * fac, acc[k].y * fac);
+    if (d2 == 0) p.lse[static_cast<size_t>(h) * p.num_seqs * n + bn] = lse;
+  }
+  if (tid == 0) p.counters[b * p.hkv + g] = 0;  // every chunk of this call has counted
 }
 
 int num_sms() {
@@ -407,9 +462,13 @@ DecodePlan decode_plan(const Problem& p, int n) {
     tiles[b] = n_pre + (hi / BN - lo_t + 1);
     total += tiles[b];
   }
-  // About four CTAs per SM over all (chunk, kv head) pairs, at least two
-  // tiles per chunk, and no more items than the parameter block holds.
-  const long long want = std::max<long long>(1, 4LL * std::max(sms, 1) / std::max(p.hkv, 1));
+  // About three (chunk, kv head) CTAs per SM: each CTA pays a pipeline fill
+  // and a partial write, and the key stream shares HBM bandwidth, so fewer,
+  // longer chunks win until the grid covers the SMs about 1.5 times (1 to 6
+  // CTAs per SM measured on 32 x 8192, 8 x 32768 x 4 rows and the packed
+  // trajectories; 3 was best on all three).  At least two tiles per chunk,
+  // and no more items than the parameter block holds.
+  const long long want = std::max<long long>(1, 3LL * std::max(sms, 1) / std::max(p.hkv, 1));
   int tps = static_cast<int>(std::max<long long>(2, (total + want - 1) / want));
   for (;;) {
     long long items = 0;
@@ -419,16 +478,14 @@ DecodePlan decode_plan(const Problem& p, int n) {
   }
   pl.tiles_per_split = tps;
   pl.items.clear();
-  pl.first.assign(p.num_seqs + 1, 0);
   for (int b = 0; b < p.num_seqs; ++b) {
-    pl.first[b] = static_cast<uint16_t>(pl.items.size());
     const int chunks = (tiles[b] + tps - 1) / tps;
     for (int c = 0; c < chunks; ++c) pl.items.push_back(static_cast<uint32_t>(b) | (static_cast<uint32_t>(c) << 16));
   }
-  pl.first[p.num_seqs] = static_cast<uint16_t>(pl.items.size());
   const int R = (p.hq / p.hkv) * n;
   pl.acc_bytes = pl.items.size() * p.hkv * static_cast<size_t>(R) * D * 4;
-  pl.ml_bytes = pl.items.size() * p.hkv * static_cast<size_t>(R) * 8;
+  pl.ml_bytes = pl.items.size() * p.hkv * static_cast<size_t>((R + 1) & ~1) * 8;
+  pl.counter_bytes = static_cast<size_t>(p.num_seqs) * p.hkv * 4;
   return pl;
 }
 
@@ -436,12 +493,16 @@ cudaError_t launch_decode(const Problem& pr, int n, const DecodeArgs& a, const D
                           cudaStream_t stream) {
   if (pr.num_seqs == 0) return cudaSuccess;
   thread_local DecK k;
-  thread_local MergeK mk;
   if (!make_rows_map(&k.tm_k, a.k, pr.total_tokens, pr.hkv, BN) ||
       !make_rows_map(&k.tm_v, a.v, pr.total_tokens, pr.hkv, BN))
     return cudaErrorInvalidValue;
   const int group = pr.hq / pr.hkv, R = group * n;
   k.q = static_cast<const __nv_bfloat16*>(a.q);
+  k.sink = a.sink;
+  k.o = static_cast<__nv_bfloat16*>(a.o);
+  k.lse = a.lse;
+  k.counters = a.counters;
+  k.num_seqs = pr.num_seqs;
   k.ws_acc = a.ws_acc;
   k.ws_ml = reinterpret_cast<float2*>(a.ws_ml);
   k.cu = pr.cu;
@@ -452,6 +513,7 @@ cudaError_t launch_decode(const Problem& pr, int n, const DecodeArgs& a, const D
   k.hkv = pr.hkv;
   k.group = group;
   k.R = R;
+  k.Rml = (R + 1) & ~1;
   k.mask = MaskParams{pr.window, pr.prefix, pr.causal};
   k.scale_log2 = pr.scale * kLog2e;
   k.tiles_per_split = pl.tiles_per_split;
@@ -476,22 +538,7 @@ cudaError_t launch_decode(const Problem& pr, int n, const DecodeArgs& a, const D
 #undef SA_DECODE_CASE
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if ((e = prof_end(g_prof_dec, stream)) != cudaSuccess) return e;
-  mk.ws_acc = a.ws_acc;
-  mk.ws_ml = reinterpret_cast<const float2*>(a.ws_ml);
-  mk.sink = a.sink;
-  mk.o = static_cast<__nv_bfloat16*>(a.o);
-  mk.lse = a.lse;
-  mk.num_seqs = pr.num_seqs;
-  mk.n = n;
-  mk.hq = pr.hq;
-  mk.hkv = pr.hkv;
-  mk.group = group;
-  mk.R = R;
-  std::copy(pl.first.begin(), pl.first.end(), mk.first);
-  const long long rows = static_cast<long long>(pr.num_seqs) * n * pr.hq;
-  decode_merge_kernel<<<static_cast<int>((rows * 32 + 127) / 128), 128, 0, stream>>>(mk);
-  return cudaGetLastError();
+  return prof_end(g_prof_dec, stream);
 }
 
 }  // namespace sa

@@ -85,15 +85,15 @@ struct DecodeArgs {
   const float* sink;
   void* o;        // [B * n, Hq, 64]
   float* lse;     // [Hq, B * n]
-  float* ws_acc;  // partial unnormalised outputs
-  void* ws_ml;    // partial (max, sum) pairs
+  float* ws_acc;   // partial unnormalised outputs
+  void* ws_ml;     // partial (max, sum) pairs
+  int* counters;   // chunks finished per (sequence, kv head); zero between calls
 };
 
 struct DecodePlan {
   int tiles_per_split = 0;
   std::vector<uint32_t> items;   // sequence | (chunk << 16), sequence-major
-  std::vector<uint16_t> first;   // items of sequence b: [first[b], first[b + 1])
-  size_t acc_bytes = 0, ml_bytes = 0;
+  size_t acc_bytes = 0, ml_bytes = 0, counter_bytes = 0;
 };
 
 DecodePlan decode_plan(const Problem& p, int n);

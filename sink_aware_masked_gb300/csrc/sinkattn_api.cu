@@ -199,7 +199,7 @@ namespace {
 
 struct DecodeLayout {
   sa::DecodePlan plan;
-  size_t acc, ml, total;
+  size_t counters, acc, ml, total;
 };
 
 // Validates the decode-specific arguments on top of normalise().
@@ -217,8 +217,9 @@ sinkattn_status decode_check(const sa::Problem& p, int32_t q_per_seq) {
 DecodeLayout decode_layout(const sa::Problem& p, int32_t q_per_seq) {
   DecodeLayout l;
   l.plan = sa::decode_plan(p, q_per_seq);
-  l.acc = 0;
-  l.ml = round_up(l.plan.acc_bytes, 256);
+  l.counters = 0;
+  l.acc = round_up(l.plan.counter_bytes, 256);
+  l.ml = l.acc + round_up(l.plan.acc_bytes, 256);
   l.total = l.ml + round_up(l.plan.ml_bytes, 256) + 256;
   return l;
 }
@@ -248,7 +249,8 @@ sinkattn_status sinkattn_decode_fwd(const sinkattn_problem* kv, int32_t q_per_se
   if (workspace_bytes < L.total) return SINKATTN_ERR_WORKSPACE;
   if (workspace == nullptr || !aligned16(workspace)) return workspace ? SINKATTN_ERR_ALIGNMENT : SINKATTN_ERR_INVALID_ARG;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  sa::DecodeArgs a{q, k, v, sink, o, lse, reinterpret_cast<float*>(ws + L.acc), ws + L.ml};
+  sa::DecodeArgs a{q, k, v, sink, o, lse, reinterpret_cast<float*>(ws + L.acc), ws + L.ml,
+                   reinterpret_cast<int*>(ws + L.counters)};
   int* status = status_word();
   if (status == nullptr) return SINKATTN_ERR_CUDA;
   return from_cuda(sa::launch_decode(p, q_per_seq, a, L.plan, status, static_cast<cudaStream_t>(stream)));

@@ -106,6 +106,17 @@ SA_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, ui
       : "memory");
 }
 
+// Contiguous bulk copy global -> shared on the TMA unit, completing on `bar`
+// (both addresses 16-byte aligned, bytes a multiple of 16).
+SA_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+// Orders this thread's earlier generic-proxy global accesses (and those it
+// has acquired) before its later async-proxy (TMA) accesses.
+SA_DEV void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;\n" ::: "memory"); }
+
 // 4-byte asynchronous copy global -> shared (Ampere-style cp.async).
 SA_DEV void cp_async4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");
