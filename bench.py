@@ -15,6 +15,10 @@ Decode workloads (``--workload decode_*``): one step = one decode forward
 key/value cache of every sequence, reported in GB/s of algorithmic HBM
 traffic (the visible keys and values once, the queries, O and lse).
 
+GRPO workloads (``--workload grpo_*``): one step = the GRPO token loss and
+its gradient over one update batch of rollouts, in GB/s of algorithmic HBM
+traffic (three fp32 log-probabilities and the mask read, the gradient written).
+
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
        python bench.py --impl reference ...   (times the CPU float64 oracle)
 Under torchrun each rank runs its own batch (weak scaling, no collective on
@@ -49,6 +53,8 @@ L2_FLUSH_BYTES = 256 << 20
 LAUNCHES_PER_STEP = 4  # forward, backward preprocess, backward main, dQ convert
 DECODE_METRIC = "sink-attn decode GB/s (bf16 KV-cache stream) and % of measured HBM copy bandwidth"
 DECODE_LAUNCHES_PER_STEP = 1  # key-chunk kernel (the last chunk of each sequence merges)
+GRPO_METRIC = "GRPO token loss GB/s (fp32 log-probs) and % of measured HBM copy bandwidth"
+GRPO_LAUNCHES_PER_STEP = 2  # per-rollout counts and advantages, token pass
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -95,6 +101,29 @@ def decode_bytes(wl, n):
     kv = decode_visible_keys(wl, n) * wl.num_heads_kv * wl.head_dim * 2 * 2
     q = rows * wl.num_heads_q * wl.head_dim * 2
     return kv + 2 * q + rows * wl.num_heads_q * 4
+
+
+def grpo_bytes(inp):
+    """Algorithmic HBM bytes of one GRPO step: logp, logp_old, logp_ref and
+    the mask read once, dlogp written; rewards in, advantages and stats out."""
+    T = int(inp.cu_tokens[-1])
+    R = len(inp.cu_tokens) - 1
+    ref = 4 if inp.wl.kl_beta else 0
+    return T * (4 + 4 + ref + 1 + 4) + R * (4 + 4 + 4) + 16
+
+
+def grpo_oracle_seconds(inp, rounds):
+    import oracle.grpo_ref as gref
+
+    args = (inp.logp.astype(np.float64), inp.logp_old.astype(np.float64), inp.logp_ref.astype(np.float64), inp.mask,
+            inp.rewards.astype(np.float64), inp.cu_tokens, inp.wl.group_size, inp.wl.clip_eps, inp.wl.adv_eps,
+            inp.wl.kl_beta)
+    secs = []
+    for _ in range(rounds):
+        t = time.perf_counter()
+        gref.grpo_loss(*args)
+        secs.append(time.perf_counter() - t)
+    return secs
 
 
 def load_peaks():
@@ -300,8 +329,32 @@ def run_reference_decode(args, rank):
     return 0
 
 
+def run_reference_grpo(args, rank):
+    if rank != 0:
+        return 0
+    inp = W.make_grpo_inputs(W.GRPO_WORKLOADS[args.workload])
+    grpo_oracle_seconds(inp, max(0, args.warmup))
+    secs = grpo_oracle_seconds(inp, args.steps)
+    total = sum(secs)
+    nbytes = grpo_bytes(inp)
+    value = nbytes * len(secs) / total / 1e9
+    line = {
+        "impl": "reference", "metric": GRPO_METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(secs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": inp.wl.name, "tokens": int(inp.cu_tokens[-1])},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: the whole {inp.wl.name} batch, one NumPy process"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_reference(args, rank):
     """The oracle as the reference arm, on the host cores of rank 0."""
+    if args.workload in W.GRPO_WORKLOADS:
+        return run_reference_grpo(args, rank)
     if args.workload in W.DECODE_WORKLOADS:
         return run_reference_decode(args, rank)
     if rank != 0:
@@ -552,11 +605,14 @@ def run_gpu_decode(args, world, rank, local):
     torch.cuda.synchronize()
     if sa.sinkattn_get_device_status() != 0:
         raise RuntimeError("device status reported a timed-out wait during warm-up")
+    # The step is one kernel; a graph replay of it is timed, so the events
+    # measure the kernel without the Python-side argument marshalling.
+    graph = capture_step(step)
+    for _ in range(max(args.warmup, 0)):
+        flush.fill_(1.0)
+        graph.replay()
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-    for e in ev:
-        for x in e:
-            x.record()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     torch.cuda.synchronize()
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     barrier(world)
@@ -565,16 +621,14 @@ def run_gpu_decode(args, world, rank, local):
     for i in range(K):
         flush.fill_(float(i))
         e = ev[i]
-        sa.sinkattn_set_profile_events(sa.PROFILE_DECODE, e[2], e[3])
         e[0].record()
-        step()
+        graph.replay()
         e[1].record()
     torch.cuda.synchronize()
     barrier(world)
     clock_info = clocks.stop()
-    sa.sinkattn_set_profile_events(sa.PROFILE_DECODE)
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    split_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    split_ms = step_ms
     if sa.sinkattn_get_device_status() != 0:
         raise RuntimeError("device status reported a timed-out wait")
 
@@ -614,6 +668,7 @@ def run_gpu_decode(args, world, rank, local):
                    "head_dim": wl.head_dim, "window": wl.window, "prefix": wl.prefix, "causal": wl.causal,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "flushed before every step (256 MiB write, outside the step events)",
+                   "timing": "CUDA graph replay of one step (one kernel); e2e = eager calls with host copies",
                    "algorithmic_bytes_per_step": nbytes,
                    "decode_rows_per_s": world * wl.num_seqs * n * K / (tot / 1e3)},
         "pct_of_peak": 100.0 * value / world / peaks["hbm_gbs"],
@@ -635,6 +690,143 @@ def run_gpu_decode(args, world, rank, local):
 
         dist.destroy_process_group()
     return 0
+
+
+def run_gpu_grpo(args, world, rank, local):
+    """GRPO loss steps; each rank its own batch (weak scaling)."""
+    import dataclasses
+
+    import torch
+
+    import sink_aware_masked_gb300 as sa
+    from sink_aware_masked_gb300 import build as sa_build
+
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    sa_build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    base = W.GRPO_WORKLOADS[args.workload]
+    inp = W.make_grpo_inputs(dataclasses.replace(base, seed=base.seed + 1000 * rank))
+    wl = inp.wl
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    logp, old, lref, mask, rew, cu = (t(a) for a in (inp.logp, inp.logp_old, inp.logp_ref, inp.mask, inp.rewards,
+                                                      inp.cu_tokens))
+    cu_host = [int(x) for x in inp.cu_tokens]
+    dlogp = torch.empty_like(logp)
+    kw = dict(group_size=wl.group_size, clip_eps=wl.clip_eps, adv_eps=wl.adv_eps, kl_beta=wl.kl_beta,
+              logp_ref=lref if wl.kl_beta else None, dlogp=dlogp)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    out = {}
+
+    def step():
+        out["stats"], _, out["adv"] = sa.grpo_loss(logp, old, mask, rew, cu, cu_host, **kw)
+
+    for _ in range(max(args.warmup, 0)):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    graph = capture_step(step)
+    for _ in range(max(args.warmup, 0)):
+        flush.fill_(1.0)
+        graph.replay()
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    for i in range(K):
+        flush.fill_(float(i))
+        ev[i][0].record()
+        graph.replay()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clock_info = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+
+    host_in = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+               for a in (inp.logp, inp.logp_old, inp.logp_ref, inp.mask, inp.rewards)]
+    dev_in = (logp, old, lref, mask, rew)
+    host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (dlogp, out["stats"])]
+    h2d = sum(x.numel() * x.element_size() for x in host_in)
+    d2h = sum(x.numel() * x.element_size() for x in host_out)
+    Ke = max(1, min(K, 20))
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ke)]
+    barrier(world)
+    for i in range(Ke):
+        flush.fill_(float(i))
+        e2e_ev[i][0].record()
+        for d_, h_ in zip(dev_in, host_in):
+            d_.copy_(h_, non_blocking=True)
+        step()
+        for h_, d_ in zip(host_out, (dlogp, out["stats"])):
+            h_.copy_(d_, non_blocking=True)
+        e2e_ev[i][1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = [a.elapsed_time(b) for a, b in e2e_ev]
+
+    tot, e2e_tot = reduce_max([sum(step_ms), sum(e2e_ms)], world, dev)
+    nbytes = grpo_bytes(inp)
+    value = world * nbytes * K / (tot / 1e3) / 1e9
+    peaks, peak_src = load_peaks()
+    achieved = nbytes / (statistics.mean(step_ms) / 1e3) / 1e9
+    line = {
+        "metric": GRPO_METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": tot / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "prompts": wl.prompts * world, "group_size": wl.group_size,
+                   "tokens": int(inp.cu_tokens[-1]), "optimised_tokens": int(np.count_nonzero(inp.mask)),
+                   "clip_eps": wl.clip_eps, "kl_beta": wl.kl_beta,
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "flushed before every step (256 MiB write, outside the step events)",
+                   "timing": "CUDA graph replay of one step (both kernels); e2e = eager calls with host copies",
+                   "algorithmic_bytes_per_step": nbytes},
+        "pct_of_peak": 100.0 * value / world / peaks["hbm_gbs"],
+        "roofline": {"bound": "hbm", "kernel": "grpo_prep + grpo_loss (whole step)", "achieved": achieved,
+                     "peak": peaks["hbm_gbs"], "peak_source": f"{peak_src} HBM copy", "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": _committed_traffic(args.workload, "grpo"),
+                     "algorithmic_bytes": nbytes},
+        "e2e": {"value": world * nbytes * Ke / (e2e_tot / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": K * GRPO_LAUNCHES_PER_STEP,
+        "clocks": clock_info,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        secs = grpo_oracle_seconds(inp, 3)
+        line["cpu_baseline"] = {"value": 3 * nbytes / sum(secs) / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": f"3 rounds of the whole {wl.name} batch, one NumPy process, "
+                                          f"{sum(secs):.2f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def capture_step(step):
+    """One step captured as a CUDA graph (for microsecond-scale steps whose
+    Python-side argument marshalling would otherwise be timed as GPU idle)."""
+    import torch
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    torch.cuda.synchronize()
+    return graph
 
 
 def _committed_traffic(workload, kernel):
@@ -663,7 +855,8 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS) + sorted(W.DECODE_WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(W.WORKLOADS) + sorted(W.DECODE_WORKLOADS) + sorted(W.GRPO_WORKLOADS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU baseline leg")
     args = ap.parse_args(argv)
@@ -672,6 +865,8 @@ def main(argv=None):
         return run_reference(args, rank)
     if args.workload in W.DECODE_WORKLOADS:
         return run_gpu_decode(args, world, rank, local)
+    if args.workload in W.GRPO_WORKLOADS:
+        return run_gpu_grpo(args, world, rank, local)
     return run_gpu(args, world, rank, local)
 
 

@@ -151,6 +151,41 @@ sinkattn_status sinkattn_decode_fwd(const sinkattn_problem* kv, int32_t q_per_se
                                     void* o, float* lse,
                                     void* workspace, size_t workspace_bytes, void* stream);
 
+/* GRPO token loss and its gradient (SinkFlex-RL, zh page, "Policy update",
+ * equations (3)-(7)), the memory-bound step of the same training loop.
+ * Rollouts are consecutive groups of group_size (the G rollouts of one
+ * prompt); rollout i owns tokens [cu_tokens[i], cu_tokens[i + 1]) of the
+ * fp32 arrays logp (current policy), logp_old (sampling policy) and
+ * logp_ref (reference policy; may be NULL when kl_beta == 0); mask (uint8,
+ * nonzero = optimised token); rewards fp32 [num_rollouts].
+ *   A_i = (R_i - mean_group) / (population std of the group + adv_eps)
+ *   rho = exp(logp - logp_old),  J = min(rho A_i, clip(rho, 1 -+ clip_eps) A_i)
+ *   loss = -(1/N) sum J + kl_beta (1/N) sum (e^r - r - 1),  r = logp_ref - logp
+ * with both sums over optimised tokens and N their count.  Writes stats fp32
+ * [4] = {loss, -(1/N) sum J, (1/N) sum (e^r - r - 1), fraction of optimised
+ * tokens whose gradient the clip removes}, dlogp fp32 [total_tokens] =
+ * dloss/dlogp (0 on tokens that are not optimised) and, if non-NULL,
+ * advantages fp32 [num_rollouts].  With N = 0 everything is 0.  logp,
+ * logp_old, logp_ref, mask and dlogp must be 16-byte aligned.  Workspace:
+ * sinkattn_grpo_workspace_size bytes, 16-byte aligned, no initial content.
+ * Checks: group_size >= 1 dividing num_rollouts, clip_eps > 0, adv_eps >= 0,
+ * kl_beta >= 0 (all finite), offsets as for sinkattn_problem. */
+typedef struct {
+  int32_t num_rollouts;
+  int32_t group_size;
+  const int32_t* cu_tokens;       /* device [num_rollouts + 1] */
+  const int32_t* cu_tokens_host;  /* host copy */
+  int32_t total_tokens;
+  float clip_eps;
+  float adv_eps;
+  float kl_beta;
+} sinkattn_grpo_problem;
+size_t sinkattn_grpo_workspace_size(const sinkattn_grpo_problem* g);
+sinkattn_status sinkattn_grpo_loss(const sinkattn_grpo_problem* g, const float* logp, const float* logp_old,
+                                   const float* logp_ref, const uint8_t* mask, const float* rewards,
+                                   float* stats, float* dlogp, float* advantages,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
 /* Packed-sequence front end (multi-turn trajectories of different lengths,
  * SinkFlex-RL section 3).  seqlens: device int32 [num_seqs];
  * cu_seqlens_out: device int32 [num_seqs + 1] receives the exclusive prefix

@@ -10,6 +10,7 @@ from .api import (  # noqa: F401
     SinkAttention,
     bwd_workspace_bytes,
     decode_workspace_bytes,
+    grpo_loss,
     make_problem,
     sink_attention,
     sinkattn_bwd,

@@ -38,7 +38,21 @@ class Problem(ctypes.Structure):
     ]
 
 
+class GrpoProblem(ctypes.Structure):
+    _fields_ = [
+        ("num_rollouts", ctypes.c_int32),
+        ("group_size", ctypes.c_int32),
+        ("cu_tokens", ctypes.c_void_p),
+        ("cu_tokens_host", ctypes.c_void_p),
+        ("total_tokens", ctypes.c_int32),
+        ("clip_eps", ctypes.c_float),
+        ("adv_eps", ctypes.c_float),
+        ("kl_beta", ctypes.c_float),
+    ]
+
+
 _PP = ctypes.POINTER(Problem)
+_GP = ctypes.POINTER(GrpoProblem)
 SIGNATURES = {
     "sinkattn_fwd_workspace_size": (_sz, [_PP]),
     "sinkattn_bwd_workspace_size": (_sz, [_PP]),
@@ -47,6 +61,8 @@ SIGNATURES = {
     "sinkattn_bwd_noalloc": (ctypes.c_int, [_PP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "sinkattn_decode_workspace_size": (_sz, [_PP, _i32]),
     "sinkattn_decode_fwd": (ctypes.c_int, [_PP, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "sinkattn_grpo_workspace_size": (_sz, [_GP]),
+    "sinkattn_grpo_loss": (ctypes.c_int, [_GP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "sinkattn_varlen_plan": (ctypes.c_int, [_vp, _i32, _vp, _vp]),
     "sinkattn_pack": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp]),
     "sinkattn_unpack": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp]),

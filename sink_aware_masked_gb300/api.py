@@ -140,6 +140,32 @@ def sinkattn_decode_fwd(q, k, v, sink, *, q_per_seq: int, o=None, lse=None, work
     return o, lse
 
 
+def grpo_loss(logp, logp_old, mask, rewards, cu_tokens, cu_tokens_host, *, group_size: int, clip_eps: float = 0.2,
+              adv_eps: float = 1e-6, kl_beta: float = 0.0, logp_ref=None, dlogp=None, workspace=None):
+    """GRPO token loss: returns (stats [4] fp32, dlogp [T] fp32, advantages [R] fp32).
+
+    stats = (loss, policy term, KL term, clipped fraction); all tensors on the
+    GPU (logp/logp_old/logp_ref fp32 [T], mask uint8 [T], rewards fp32 [R],
+    cu_tokens int32 [R + 1] with its host copy cu_tokens_host).
+    """
+    lib = _lib.load()
+    host = (ctypes.c_int32 * len(cu_tokens_host))(*[int(x) for x in cu_tokens_host])
+    R = len(cu_tokens_host) - 1
+    g = _lib.GrpoProblem(num_rollouts=R, group_size=int(group_size), cu_tokens=_ptr(cu_tokens),
+                         cu_tokens_host=ctypes.cast(host, ctypes.c_void_p).value, total_tokens=int(cu_tokens_host[-1]),
+                         clip_eps=float(clip_eps), adv_eps=float(adv_eps), kl_beta=float(kl_beta))
+    stats = torch.empty(4, dtype=torch.float32, device=logp.device)
+    dlogp = torch.empty_like(logp) if dlogp is None else dlogp
+    adv = torch.empty(R, dtype=torch.float32, device=logp.device)
+    ws_bytes = int(lib.sinkattn_grpo_workspace_size(ctypes.byref(g)))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=logp.device)
+    st = lib.sinkattn_grpo_loss(ctypes.byref(g), _ptr(logp), _ptr(logp_old), _ptr(logp_ref), _ptr(mask), _ptr(rewards),
+                                _ptr(stats), _ptr(dlogp), _ptr(adv), _ptr(workspace), workspace.numel(), _stream())
+    _lib.check("sinkattn_grpo_loss", st)
+    return stats, dlogp, adv
+
+
 def sinkattn_varlen_plan(seqlens: torch.Tensor) -> torch.Tensor:
     """Device int32 lengths [B] -> device int32 offsets [B + 1]."""
     lib = _lib.load()

@@ -100,6 +100,24 @@ DecodePlan decode_plan(const Problem& p, int n);
 cudaError_t launch_decode(const Problem& p, int n, const DecodeArgs& a, const DecodePlan& pl, int* status,
                           cudaStream_t s);
 
+// GRPO token loss (grpo.cu).
+struct GrpoArgs {
+  int num_rollouts, group_size, total_tokens;
+  const int32_t* cu_tokens;  // device [num_rollouts + 1]
+  float clip_eps, adv_eps, kl_beta;
+  const float* logp;
+  const float* logp_old;
+  const float* logp_ref;
+  const uint8_t* mask;
+  const float* rewards;
+  float* stats;       // [4]
+  float* dlogp;
+  float* advantages;  // or nullptr
+  void* workspace;
+};
+size_t grpo_workspace_bytes(int num_rollouts, int total_tokens);
+cudaError_t launch_grpo(const GrpoArgs& a, cudaStream_t s);
+
 // Optional events recorded around the main kernels (measurement hook).
 struct ProfileEvents {
   cudaEvent_t start = nullptr, stop = nullptr;

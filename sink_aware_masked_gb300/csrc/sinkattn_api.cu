@@ -256,6 +256,52 @@ sinkattn_status sinkattn_decode_fwd(const sinkattn_problem* kv, int32_t q_per_se
   return from_cuda(sa::launch_decode(p, q_per_seq, a, L.plan, status, static_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+
+sinkattn_status grpo_check(const sinkattn_grpo_problem* g) {
+  if (g == nullptr) return SINKATTN_ERR_INVALID_ARG;
+  if (g->num_rollouts < 0 || g->group_size < 1 || g->total_tokens < 0) return SINKATTN_ERR_INVALID_ARG;
+  if (g->num_rollouts % g->group_size != 0) return SINKATTN_ERR_INVALID_ARG;
+  if (!(g->clip_eps > 0.f) || !std::isfinite(g->clip_eps)) return SINKATTN_ERR_INVALID_ARG;
+  if (!(g->adv_eps >= 0.f) || !std::isfinite(g->adv_eps)) return SINKATTN_ERR_INVALID_ARG;
+  if (!(g->kl_beta >= 0.f) || !std::isfinite(g->kl_beta)) return SINKATTN_ERR_INVALID_ARG;
+  if (g->num_rollouts > 0 && (g->cu_tokens == nullptr || g->cu_tokens_host == nullptr)) return SINKATTN_ERR_INVALID_ARG;
+  if (g->num_rollouts > 0) {
+    const int32_t* cu = g->cu_tokens_host;
+    if (cu[0] != 0 || cu[g->num_rollouts] != g->total_tokens) return SINKATTN_ERR_INVALID_ARG;
+    for (int i = 0; i < g->num_rollouts; ++i)
+      if (cu[i + 1] < cu[i]) return SINKATTN_ERR_INVALID_ARG;
+  }
+  return SINKATTN_OK;
+}
+
+}  // namespace
+
+size_t sinkattn_grpo_workspace_size(const sinkattn_grpo_problem* g) {
+  if (grpo_check(g) != SINKATTN_OK) return 0;
+  return sa::grpo_workspace_bytes(g->num_rollouts, g->total_tokens);
+}
+
+sinkattn_status sinkattn_grpo_loss(const sinkattn_grpo_problem* g, const float* logp, const float* logp_old,
+                                   const float* logp_ref, const uint8_t* mask, const float* rewards, float* stats,
+                                   float* dlogp, float* advantages, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+  sinkattn_status st = grpo_check(g);
+  if (st != SINKATTN_OK) return st;
+  if (!stats) return SINKATTN_ERR_INVALID_ARG;
+  if (g->num_rollouts == 0) return from_cuda(cudaMemsetAsync(stats, 0, 4 * sizeof(float), static_cast<cudaStream_t>(stream)));
+  if (!logp || !logp_old || !mask || !rewards || !dlogp || (g->kl_beta != 0.f && !logp_ref))
+    return SINKATTN_ERR_INVALID_ARG;
+  if (!aligned16(logp) || !aligned16(logp_old) || !aligned16(mask) || !aligned16(dlogp) ||
+      (g->kl_beta != 0.f && !aligned16(logp_ref)))
+    return SINKATTN_ERR_ALIGNMENT;
+  if (!aligned16(workspace)) return workspace ? SINKATTN_ERR_ALIGNMENT : SINKATTN_ERR_INVALID_ARG;
+  if (workspace_bytes < sa::grpo_workspace_bytes(g->num_rollouts, g->total_tokens)) return SINKATTN_ERR_WORKSPACE;
+  sa::GrpoArgs a{g->num_rollouts, g->group_size, g->total_tokens, g->cu_tokens, g->clip_eps, g->adv_eps, g->kl_beta,
+                 logp, logp_old, logp_ref, mask, rewards, stats, dlogp, advantages, workspace};
+  return from_cuda(sa::launch_grpo(a, static_cast<cudaStream_t>(stream)));
+}
+
 sinkattn_status sinkattn_varlen_plan(const int32_t* seqlens, int32_t num_seqs, int32_t* cu_seqlens_out,
                                      void* stream) {
   if (num_seqs < 0 || cu_seqlens_out == nullptr || (num_seqs > 0 && seqlens == nullptr))

@@ -157,3 +157,47 @@ def test_decode_pointers_and_workspace(lib):
     assert lib.sinkattn_decode_fwd(ctypes.byref(pr), 2, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws, None) == 1
     assert lib.sinkattn_decode_fwd(ctypes.byref(pr), 2, FAKE, FAKE + 4, FAKE, FAKE, FAKE, FAKE, FAKE, ws, None) == 3
     assert lib.sinkattn_decode_fwd(ctypes.byref(pr), 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws - 1, None) == 4
+
+
+def grpo_problem(**kw):
+    from sink_aware_masked_gb300 import _lib
+
+    host = (ctypes.c_int32 * 3)(0, 5, 9)
+    base = dict(num_rollouts=2, group_size=2, cu_tokens=FAKE, cu_tokens_host=ctypes.cast(host, ctypes.c_void_p).value,
+                total_tokens=9, clip_eps=0.2, adv_eps=1e-6, kl_beta=0.0)
+    base.update(kw)
+    return _lib.GrpoProblem(**base), host
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(group_size=0), 1),
+    (dict(group_size=3), 1),            # does not divide the rollouts
+    (dict(clip_eps=0.0), 1),
+    (dict(adv_eps=-1.0), 1),
+    (dict(kl_beta=float("nan")), 1),
+    (dict(total_tokens=10), 1),         # offsets end elsewhere
+])
+def test_grpo_validation(lib, kw, status):
+    g, host = grpo_problem(**kw)
+    assert lib.sinkattn_grpo_loss(ctypes.byref(g), FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, None, FAKE, 1 << 20,
+                                  None) == status
+    assert lib.sinkattn_grpo_workspace_size(ctypes.byref(g)) == 0
+
+
+def test_grpo_pointers(lib):
+    g, host = grpo_problem(kl_beta=0.1)
+    ws = lib.sinkattn_grpo_workspace_size(ctypes.byref(g))
+    assert ws > 0
+    # logp_ref is required when the KL term is on
+    assert lib.sinkattn_grpo_loss(ctypes.byref(g), FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, None, FAKE, ws, None) == 1
+    assert lib.sinkattn_grpo_loss(ctypes.byref(g), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, ws - 1,
+                                  None) == 4
+
+
+def test_grpo_alignment(lib):
+    g, host = grpo_problem()
+    ws = lib.sinkattn_grpo_workspace_size(ctypes.byref(g))
+    assert lib.sinkattn_grpo_loss(ctypes.byref(g), FAKE + 4, FAKE, None, FAKE, FAKE, FAKE, FAKE, None, FAKE, ws,
+                                  None) == 3
+    assert lib.sinkattn_grpo_loss(ctypes.byref(g), FAKE, FAKE, None, FAKE + 1, FAKE, FAKE, FAKE, None, FAKE, ws,
+                                  None) == 3

@@ -196,3 +196,62 @@ DECODE_WORKLOADS = {
                                 "uniform2", uniform=False), 1),
     "decode_b8_kv32768_n4": (_uniform("decode_b8_kv32768_n4", 8, 32768, 64, 8, WINDOW_INF, 0, 8, "uniform2"), 4),
 }
+
+
+# ------------------------------------------------------------------ GRPO
+@dataclasses.dataclass(frozen=True)
+class GrpoWorkload:
+    """One GRPO update batch: prompts x G rollouts of drawn token lengths."""
+
+    name: str
+    prompts: int
+    group_size: int
+    len_lo: int
+    len_hi: int
+    seed: int
+    clip_eps: float = 0.2
+    adv_eps: float = 1e-6
+    kl_beta: float = 0.04
+
+
+@dataclasses.dataclass
+class GrpoInputs:
+    wl: GrpoWorkload
+    cu_tokens: np.ndarray    # int32 [R + 1]
+    logp: np.ndarray         # float32 [T]
+    logp_old: np.ndarray
+    logp_ref: np.ndarray
+    mask: np.ndarray         # uint8 [T]: optimised (policy-generated) tokens
+    rewards: np.ndarray      # float32 [R]
+
+
+def make_grpo_inputs(wl: GrpoWorkload) -> GrpoInputs:
+    """Rollout lengths U[len_lo, len_hi]; each rollout alternates observation
+    spans (not optimised) and action spans (optimised) of U[16, 256] tokens;
+    logp_old = -Gamma(2, 1), logp = logp_old + N(0, 0.3), logp_ref = logp_old
+    + N(0, 0.2); task rewards in {0, 1} (a group can be all-equal)."""
+    rng = np.random.default_rng(wl.seed)
+    R = wl.prompts * wl.group_size
+    lens = rng.integers(wl.len_lo, wl.len_hi + 1, R)
+    cu = np.zeros(R + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(lens)
+    T = int(cu[-1])
+    logp_old = -rng.gamma(2.0, 1.0, T).astype(np.float32)
+    logp = (logp_old + rng.normal(0.0, 0.3, T)).astype(np.float32)
+    logp_ref = (logp_old + rng.normal(0.0, 0.2, T)).astype(np.float32)
+    mask = np.zeros(T, dtype=np.uint8)
+    for i in range(R):
+        t, on = int(cu[i]), False
+        while t < cu[i + 1]:
+            span = int(rng.integers(16, 257))
+            if on:
+                mask[t:min(t + span, int(cu[i + 1]))] = 1
+            t += span
+            on = not on
+    rewards = rng.integers(0, 2, R).astype(np.float32)
+    return GrpoInputs(wl, cu, logp, logp_old, logp_ref, mask, rewards)
+
+
+GRPO_WORKLOADS = {
+    "grpo_64x8_traj1k8k": GrpoWorkload("grpo_64x8_traj1k8k", 64, 8, 1024, 8192, 9),
+}
