@@ -7,7 +7,8 @@ one batch of the workload.  Default workload: 2 sequences x 8192 tokens,
 
 The line's value is TFLOP/s counting only unmasked (query, key, head) pairs
 at 14 * 64 FLOP per pair (forward 4 * 64, backward 10 * 64).  Inputs are
-resident in HBM; L2 is flushed (256 MiB write) before every timed step, and
+resident in HBM; L2 is flushed before every timed step (a 256 MiB write, then a
+256 MiB read so the written lines drain outside the timed region), and
 each step is timed alone with CUDA events on the stream the kernels run on.
 
 Decode workloads (``--workload decode_*``): one step = one decode forward
@@ -385,6 +386,25 @@ def run_reference(args, rank):
 
 
 # ----------------------------------------------------------------- GPU arm
+class L2Flush:
+    """Between timed steps: write a buffer larger than L2 (evicts every line
+    a step could reuse), then read a second one, so the write's dirty lines
+    go back to HBM here and not during the next timed step."""
+
+    def __init__(self, device):
+        import torch
+
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.out = torch.empty((), dtype=torch.float32, device=device)
+
+    def __call__(self, value=1.0):
+        import torch
+
+        self.w.fill_(float(value))
+        torch.sum(self.r, out=self.out)
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -441,14 +461,14 @@ def run_gpu(args, world, rank, local):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dsink = torch.empty_like(sink)
     ws = torch.empty(max(16, sa.bwd_workspace_bytes(q, k, **prob)), dtype=torch.uint8, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
 
     def step():
         sa.sinkattn_fwd(q, k, v, sink, o=o, lse=lse, **prob)
         sa.sinkattn_bwd(q, k, v, o, lse, do, sink, dq=dq, dk=dk, dv=dv, dsink=dsink, workspace=ws, **prob)
 
     for _ in range(max(args.warmup, 0)):
-        flush.fill_(1.0)
+        flush(1.0)
         step()
     torch.cuda.synchronize()
     if sa.sinkattn_get_device_status() != 0:
@@ -465,7 +485,7 @@ def run_gpu(args, world, rank, local):
     torch.cuda.synchronize()
     clocks.start()
     for i in range(K):
-        flush.fill_(float(i))
+        flush(float(i))
         e = ev[i]
         sa.sinkattn_set_profile_events(sa.PROFILE_FWD, e[2], e[3])
         sa.sinkattn_set_profile_events(sa.PROFILE_BWD_MAIN, e[4], e[5])
@@ -494,7 +514,7 @@ def run_gpu(args, world, rank, local):
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ke)]
     barrier(world)
     for i in range(Ke):
-        flush.fill_(float(i))
+        flush(float(i))
         e2e_ev[i][0].record()
         for d_, h_ in zip(dev_in, host_in):
             d_.copy_(h_, non_blocking=True)
@@ -538,7 +558,7 @@ def run_gpu(args, world, rank, local):
                    "heads_q": wl.num_heads_q, "heads_kv": wl.num_heads_kv, "head_dim": wl.head_dim,
                    "window": wl.window, "prefix": wl.prefix, "causal": wl.causal,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "l2": "flushed before every step (256 MiB write, outside the step events)",
+                   "l2": "flushed before every step (256 MiB write, then 256 MiB read so the written lines drain; outside the step events)",
                    "flop_per_step": flop_step, "unmasked_pairs": pairs},
         "pct_of_peak": 100.0 * value / world / peaks["bf16_tflops"],
         "breakdown_ms": {"fwd_kernel": avg_fwd, "bwd_main_kernel": avg_bwd,
@@ -594,13 +614,13 @@ def run_gpu_decode(args, world, rank, local):
     o = torch.empty_like(q)
     lse = torch.empty((wl.num_heads_q, q.shape[0]), dtype=torch.float32, device=dev)
     ws = torch.zeros(max(16, sa.decode_workspace_bytes(q, k, q_per_seq=n, **prob)), dtype=torch.uint8, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
 
     def step():
         sa.sinkattn_decode_fwd(q, k, v, sink, q_per_seq=n, o=o, lse=lse, workspace=ws, **prob)
 
     for _ in range(max(args.warmup, 0)):
-        flush.fill_(1.0)
+        flush(1.0)
         step()
     torch.cuda.synchronize()
     if sa.sinkattn_get_device_status() != 0:
@@ -609,7 +629,7 @@ def run_gpu_decode(args, world, rank, local):
     # measure the kernel without the Python-side argument marshalling.
     graph = capture_step(step)
     for _ in range(max(args.warmup, 0)):
-        flush.fill_(1.0)
+        flush(1.0)
         graph.replay()
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
@@ -619,7 +639,7 @@ def run_gpu_decode(args, world, rank, local):
     torch.cuda.synchronize()
     clocks.start()
     for i in range(K):
-        flush.fill_(float(i))
+        flush(float(i))
         e = ev[i]
         e[0].record()
         graph.replay()
@@ -641,7 +661,7 @@ def run_gpu_decode(args, world, rank, local):
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ke)]
     barrier(world)
     for i in range(Ke):
-        flush.fill_(float(i))
+        flush(float(i))
         e2e_ev[i][0].record()
         q.copy_(host_q, non_blocking=True)
         step()
@@ -667,7 +687,7 @@ def run_gpu_decode(args, world, rank, local):
                    "query_rows_per_seq": n, "heads_q": wl.num_heads_q, "heads_kv": wl.num_heads_kv,
                    "head_dim": wl.head_dim, "window": wl.window, "prefix": wl.prefix, "causal": wl.causal,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "l2": "flushed before every step (256 MiB write, outside the step events)",
+                   "l2": "flushed before every step (256 MiB write, then 256 MiB read so the written lines drain; outside the step events)",
                    "timing": "CUDA graph replay of one step (one kernel); e2e = eager calls with host copies",
                    "algorithmic_bytes_per_step": nbytes,
                    "decode_rows_per_s": world * wl.num_seqs * n * K / (tot / 1e3)},
@@ -718,19 +738,19 @@ def run_gpu_grpo(args, world, rank, local):
     dlogp = torch.empty_like(logp)
     kw = dict(group_size=wl.group_size, clip_eps=wl.clip_eps, adv_eps=wl.adv_eps, kl_beta=wl.kl_beta,
               logp_ref=lref if wl.kl_beta else None, dlogp=dlogp)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     out = {}
 
     def step():
         out["stats"], _, out["adv"] = sa.grpo_loss(logp, old, mask, rew, cu, cu_host, **kw)
 
     for _ in range(max(args.warmup, 0)):
-        flush.fill_(1.0)
+        flush(1.0)
         step()
     torch.cuda.synchronize()
     graph = capture_step(step)
     for _ in range(max(args.warmup, 0)):
-        flush.fill_(1.0)
+        flush(1.0)
         graph.replay()
     torch.cuda.synchronize()
     K = args.steps
@@ -740,7 +760,7 @@ def run_gpu_grpo(args, world, rank, local):
     torch.cuda.synchronize()
     clocks.start()
     for i in range(K):
-        flush.fill_(float(i))
+        flush(float(i))
         ev[i][0].record()
         graph.replay()
         ev[i][1].record()
@@ -759,7 +779,7 @@ def run_gpu_grpo(args, world, rank, local):
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ke)]
     barrier(world)
     for i in range(Ke):
-        flush.fill_(float(i))
+        flush(float(i))
         e2e_ev[i][0].record()
         for d_, h_ in zip(dev_in, host_in):
             d_.copy_(h_, non_blocking=True)
@@ -784,7 +804,7 @@ def run_gpu_grpo(args, world, rank, local):
                    "tokens": int(inp.cu_tokens[-1]), "optimised_tokens": int(np.count_nonzero(inp.mask)),
                    "clip_eps": wl.clip_eps, "kl_beta": wl.kl_beta,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "l2": "flushed before every step (256 MiB write, outside the step events)",
+                   "l2": "flushed before every step (256 MiB write, then 256 MiB read so the written lines drain; outside the step events)",
                    "timing": "CUDA graph replay of one step (both kernels); e2e = eager calls with host copies",
                    "algorithmic_bytes_per_step": nbytes},
         "pct_of_peak": 100.0 * value / world / peaks["hbm_gbs"],
