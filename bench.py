@@ -402,7 +402,7 @@ class L2Flush:
         import torch
 
         self.w.fill_(float(value))
-        torch.sum(self.r, out=self.out)
+        torch.sum(self.r, dim=0, out=self.out)
 
 
 def dist_setup():
