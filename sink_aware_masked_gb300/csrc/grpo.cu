@@ -14,16 +14,19 @@
 // tokens, dJ = rho A unless the clipped branch is strictly smaller (then 0).
 //
 // A memory-bound stream (13 bytes read and 4 written per token) over chunks
-// of 4096 tokens, each thread taking four 16-byte vectors of a chunk with all
-// loads issued before use; both passes run a persistent grid of three CTAs
-// per SM that strides over the chunks.  Pass 1 counts the optimised tokens
-// (one partial per CTA), computes the advantages (one thread per rollout) and
-// records the rollout of each chunk's first token.  Pass 2 needs
-// N = sum_i T_i before it can scale the gradient, so every CTA sums the
-// pass-1 counts itself; per chunk it stages the offsets and advantages of the
-// next 256 rollouts in shared memory, finds each token's rollout there by
-// binary search, writes dL/dlogp and accumulates its partial sums; the last
-// CTA to finish reduces the partials in a fixed order (deterministic).
+// of 2048 tokens, each thread taking two 16-byte vectors of a chunk; both
+// passes run a persistent grid that strides over the chunks.  Pass 1 counts
+// the optimised tokens (one partial per CTA) and computes the advantages
+// (one thread per rollout).  Pass 2 needs N = sum_i T_i before it can scale
+// the gradient, so every CTA sums the pass-1 counts itself and stages the
+// rollout offsets and advantages in shared memory (8 bytes per rollout),
+// both while its first chunk's token loads are in flight; it finds each
+// vector's rollout by binary search there (the streaming loads would evict
+// the offsets from L1), writes dL/dlogp and accumulates partial sums; the
+// last CTA to finish reduces the partials in a fixed order (deterministic).
+// (Measured and not kept: staging the chunks through a shared-memory ring by
+// bulk copies, and per-chunk rollout lists; neither was faster — the pass
+// is bound by its per-token instruction latency, not by bytes in flight.)
 #include "common.cuh"
 #include "internal.h"
 
@@ -33,11 +36,12 @@ namespace sa {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kVec = 4;                          // 16-byte vectors per thread
-constexpr int kTokPerCta = kThreads * kVec * 4;  // 4096 tokens
-constexpr int kWindow = 256;                     // rollouts staged per chunk in pass 2
+constexpr int kVec = 2;                          // 16-byte vectors per thread and chunk
+constexpr int kTokPerCta = kThreads * kVec * 4;  // 2048 tokens per chunk
 constexpr int kRewardStage = 2048;               // rewards of one pass-1 CTA's groups staged up to this
-constexpr int kCtasPerSm = 3;
+constexpr int kStageRollouts = 6000;             // pass 2 stages offsets and advantages up to this many rollouts
+constexpr int kLossCtasPerSm = 4;
+constexpr int kCtasPerSm = 4;
 
 struct GrpoK {
   const float* logp;
@@ -52,9 +56,8 @@ struct GrpoK {
   int* counts;     // workspace [P]: optimised tokens per pass-1 CTA
   float* adv;      // workspace [R]
   float4* part;    // workspace [grid]: sum J, sum k3, clipped count
-  int* first;      // workspace [chunks]: rollout of each chunk's first token
   unsigned* done;  // workspace: pass-2 CTAs finished
-  int R, G, T, chunks, grid;
+  int R, G, T, chunks, grid, grid2;
   float clip_eps, adv_eps, beta;
 };
 
@@ -85,9 +88,10 @@ __global__ void __launch_bounds__(kThreads) grpo_prep_kernel(const GrpoK p) {
   __shared__ int red[kThreads / 32];
   __shared__ float rew_s[kRewardStage];
   const int tid = threadIdx.x;
-  // Optimised tokens of the chunks this CTA strides over, 16 per load.
+  // Optimised tokens of the chunks this CTA strides over, 16 per load (the
+  // first 128 threads of the CTA cover a 2048-token chunk).
   int n = 0;
-  for (int c = blockIdx.x; c < p.chunks; c += gridDim.x) {
+  for (int c = blockIdx.x; c < p.chunks && tid < kTokPerCta / 16; c += gridDim.x) {
     const long long t = static_cast<long long>(c) * kTokPerCta + 16LL * tid;
     if (t + 16 <= p.T) {
       const uint4 m = __ldg(reinterpret_cast<const uint4*>(p.mask + t));
@@ -122,9 +126,6 @@ __global__ void __launch_bounds__(kThreads) grpo_prep_kernel(const GrpoK p) {
       const float a = (rew(i) - mu) / (sqrtf(var / static_cast<float>(p.G)) + p.adv_eps);
       p.adv[i] = a;
       if (p.adv_out) p.adv_out[i] = a;
-      // Chunks whose first token lies in this (non-empty) rollout.
-      const int t0 = __ldg(p.cu + i), t1 = __ldg(p.cu + i + 1);
-      for (int c = (t0 + kTokPerCta - 1) / kTokPerCta; c * kTokPerCta < t1; ++c) p.first[c] = i;
     }
   }
   n = block_sum(n, red);
@@ -134,25 +135,34 @@ __global__ void __launch_bounds__(kThreads) grpo_prep_kernel(const GrpoK p) {
   }
 }
 
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) grpo_loss_kernel(const GrpoK p) {
+__global__ void __launch_bounds__(kThreads, kLossCtasPerSm) grpo_loss_kernel(const GrpoK p) {
   __shared__ long long red_ll[kThreads / 32];
   __shared__ float3 red_f3[kThreads / 32];
   __shared__ double red_d[kThreads / 32];
-  __shared__ int cu_w[kWindow + 1];
-  __shared__ float adv_w[kWindow];
   __shared__ float sh_inv_n;
   __shared__ bool is_last;
+  extern __shared__ int dyn_s[];  // [R + 1] offsets, then [R] advantages (when staged)
   const int tid = threadIdx.x;
-  // N = sum of the pass-1 counts (every CTA sums them itself).
+  const bool staged = p.R <= kStageRollouts;
+  const int* cu_s = dyn_s;
+  const float* adv_s = reinterpret_cast<const float*>(dyn_s + p.R + 1);
   long long n = 0;
-  for (int j = tid; j < p.grid; j += kThreads) n += __ldcg(p.counts + j);
-  n = block_sum(n, red_ll);
-  if (tid == 0) sh_inv_n = n > 0 ? static_cast<float>(1.0 / static_cast<double>(n)) : 0.f;
+  float inv_n = 0.f;
   const float beta = p.beta;
   const float lo = 1.f - p.clip_eps, hi = 1.f + p.clip_eps;
   const int nvec = p.T / 4;
+  auto cu_at = [&](int j) { return staged ? cu_s[j] : __ldg(p.cu + j); };
+  auto adv_at = [&](int i) { return staged ? adv_s[i] : __ldg(p.adv + i); };
+  // Rollout of token t: the last i with cu[i] <= t (skips empty rollouts).
+  auto rollout = [&](int t, int a, int b) {  // cu[a] <= t < cu[b]
+    while (b - a > 1) {
+      const int mid = (a + b) >> 1;
+      if (cu_at(mid) <= t) a = mid; else b = mid;
+    }
+    return a;
+  };
   float sj = 0.f, sk = 0.f, sc = 0.f;
-  auto token = [&](float x, float xo, float xr, bool m, float A, float inv_n) -> float {
+  auto token = [&](float x, float xo, float xr, bool m, float A) -> float {
     const float rho = expf(x - xo);
     const float J = fminf(rho * A, fminf(fmaxf(rho, lo), hi) * A);
     const bool clipped = (A > 0.f && rho > hi) || (A < 0.f && rho < lo);
@@ -172,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) grpo_loss_kernel(const G
     return m ? g * inv_n : 0.f;
   };
   for (int c = blockIdx.x; c < p.chunks; c += gridDim.x) {
-    // All loads of this chunk first.
+    // The chunk's token loads first.
     float4 lp[kVec], old[kVec], lr[kVec];
     uchar4 mk[kVec];
 #pragma unroll
@@ -185,44 +195,33 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) grpo_loss_kernel(const G
         mk[k] = __ldg(reinterpret_cast<const uchar4*>(p.mask) + v);
       }
     }
-    // Offsets and advantages of the 256 rollouts from the chunk's first one.
-    const int i0 = __ldcg(p.first + c);
-    const int nw = min(kWindow, p.R - i0);
-    __syncthreads();
-    for (int j = tid; j <= nw; j += kThreads) cu_w[j] = __ldg(p.cu + i0 + j);
-    if (tid < nw) adv_w[tid] = __ldcg(p.adv + i0 + tid);
-    __syncthreads();
-    const float inv_n = sh_inv_n;
-    const int w_end = cu_w[nw];  // tokens beyond this need a global search
-    // Rollout of token t: the last i with cu[i] <= t (skips empty rollouts).
-    auto adv_of = [&](int t) -> float {
-      if (t < w_end) {
-        int a = 0, b = nw;
-        while (b - a > 1) {
-          const int mid = (a + b) >> 1;
-          if (cu_w[mid] <= t) a = mid; else b = mid;
-        }
-        return adv_w[a];
+    if (c == static_cast<int>(blockIdx.x)) {
+      // N = sum of the pass-1 counts (every CTA sums them itself) and the
+      // staged offsets and advantages, while the first chunk's loads are in flight.
+      if (staged) {
+        for (int j = tid; j <= p.R; j += kThreads) dyn_s[j] = __ldg(p.cu + j);
+        for (int j = tid; j < p.R; j += kThreads) reinterpret_cast<float*>(dyn_s + p.R + 1)[j] = __ldg(p.adv + j);
       }
-      int a = i0 + nw, b = p.R;
-      while (b - a > 1) {
-        const int mid = (a + b) >> 1;
-        if (__ldg(p.cu + mid) <= t) a = mid; else b = mid;
-      }
-      return __ldcg(p.adv + a);
-    };
+      for (int j = tid; j < p.grid; j += kThreads) n += __ldcg(p.counts + j);
+      n = block_sum(n, red_ll);
+      if (tid == 0) sh_inv_n = n > 0 ? static_cast<float>(1.0 / static_cast<double>(n)) : 0.f;
+      __syncthreads();
+      inv_n = sh_inv_n;
+    }
 #pragma unroll
     for (int k = 0; k < kVec; ++k) {
       const int v = c * (kTokPerCta / 4) + tid + kThreads * k;
       if (v < nvec) {
         const int t = 4 * v;
+        const int i0 = rollout(t, 0, p.R);
+        const float a0 = adv_at(i0);
+        // The four tokens usually share the rollout; otherwise look each up.
+        const bool same = t + 3 < cu_at(i0 + 1);
         float4 d;
-        const float a0 = adv_of(t), a3 = adv_of(t + 3);
-        const bool same = a0 == a3;  // equal advantages: the middle tokens' value is the same either way
-        d.x = token(lp[k].x, old[k].x, lr[k].x, mk[k].x != 0, a0, inv_n);
-        d.y = token(lp[k].y, old[k].y, lr[k].y, mk[k].y != 0, same ? a0 : adv_of(t + 1), inv_n);
-        d.z = token(lp[k].z, old[k].z, lr[k].z, mk[k].z != 0, same ? a0 : adv_of(t + 2), inv_n);
-        d.w = token(lp[k].w, old[k].w, lr[k].w, mk[k].w != 0, a3, inv_n);
+        d.x = token(lp[k].x, old[k].x, lr[k].x, mk[k].x != 0, a0);
+        d.y = token(lp[k].y, old[k].y, lr[k].y, mk[k].y != 0, same ? a0 : adv_at(rollout(t + 1, i0, p.R)));
+        d.z = token(lp[k].z, old[k].z, lr[k].z, mk[k].z != 0, same ? a0 : adv_at(rollout(t + 2, i0, p.R)));
+        d.w = token(lp[k].w, old[k].w, lr[k].w, mk[k].w != 0, same ? a0 : adv_at(rollout(t + 3, i0, p.R)));
         reinterpret_cast<float4*>(p.dlogp)[v] = d;
       }
     }
@@ -230,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) grpo_loss_kernel(const G
     if (tid == 0 && nvec / (kTokPerCta / 4) == c)
       for (int t = 4 * nvec; t < p.T; ++t)
         p.dlogp[t] = token(__ldg(p.logp + t), __ldg(p.logp_old + t), beta != 0.f ? __ldg(p.logp_ref + t) : 0.f,
-                           __ldg(p.mask + t) != 0, adv_of(t), inv_n);
+                           __ldg(p.mask + t) != 0, adv_at(rollout(t, 0, p.R)));
   }
   // One reduction of the three partial sums.
   float3 s3 = make_float3(sj, sk, sc);
@@ -260,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) grpo_loss_kernel(const G
   // Every thread sums a fixed strided subset of the partials, then a fixed
   // shuffle tree: the result does not depend on which CTA finished last.
   double dj = 0.0, dk = 0.0, dc = 0.0;
-  for (int j = tid; j < p.grid; j += kThreads) {
+  for (int j = tid; j < static_cast<int>(gridDim.x); j += kThreads) {
     const float4 v = __ldcg(p.part + j);
     dj += v.x;
     dk += v.y;
@@ -292,18 +291,27 @@ int grid_ctas(int T) {
   return std::min(num_chunks(T), kCtasPerSm * sms);
 }
 
+int loss_ctas(int T) {
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms <= 0)
+    sms = 152;
+  return std::min(num_chunks(T), kLossCtasPerSm * sms);
+}
+
 size_t a256(size_t x) { return (x + 255) / 256 * 256; }
 
 }  // namespace
 
 size_t grpo_workspace_bytes(int num_rollouts, int total_tokens) {
-  const size_t G = static_cast<size_t>(grid_ctas(total_tokens)), C = static_cast<size_t>(num_chunks(total_tokens));
-  return a256(G * 4) + a256(static_cast<size_t>(num_rollouts) * 4) + a256(G * 16) + a256(C * 4) + 256;
+  const size_t G = static_cast<size_t>(grid_ctas(total_tokens)), G2 = static_cast<size_t>(loss_ctas(total_tokens));
+  return a256(G * 4) + a256(static_cast<size_t>(num_rollouts) * 4) + a256(G2 * 16) + 256;
 }
 
 cudaError_t launch_grpo(const GrpoArgs& a, cudaStream_t stream) {
   if (a.num_rollouts == 0) return cudaSuccess;
   const int grid = grid_ctas(a.total_tokens), chunks = num_chunks(a.total_tokens);
+  const int grid2 = loss_ctas(a.total_tokens);
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   GrpoK k;
   k.logp = a.logp;
@@ -321,22 +329,22 @@ cudaError_t launch_grpo(const GrpoArgs& a, cudaStream_t stream) {
   k.adv = reinterpret_cast<float*>(ws + off);
   off += a256(static_cast<size_t>(a.num_rollouts) * 4);
   k.part = reinterpret_cast<float4*>(ws + off);
-  off += a256(static_cast<size_t>(grid) * 16);
-  k.first = reinterpret_cast<int*>(ws + off);
-  off += a256(static_cast<size_t>(chunks) * 4);
+  off += a256(static_cast<size_t>(grid2) * 16);
   k.done = reinterpret_cast<unsigned*>(ws + off);
   k.R = a.num_rollouts;
   k.G = a.group_size;
   k.T = a.total_tokens;
   k.chunks = chunks;
   k.grid = grid;
+  k.grid2 = grid2;
   k.clip_eps = a.clip_eps;
   k.adv_eps = a.adv_eps;
   k.beta = a.kl_beta;
   grpo_prep_kernel<<<grid, kThreads, 0, stream>>>(k);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  grpo_loss_kernel<<<grid, kThreads, 0, stream>>>(k);
+  const size_t dyn = a.num_rollouts <= kStageRollouts ? (2 * static_cast<size_t>(a.num_rollouts) + 1) * 4 : 0;
+  grpo_loss_kernel<<<grid2, kThreads, dyn, stream>>>(k);
   return cudaGetLastError();
 }
 
