@@ -736,8 +736,10 @@ def run_gpu_grpo(args, world, rank, local):
                                                       inp.cu_tokens))
     cu_host = [int(x) for x in inp.cu_tokens]
     dlogp = torch.empty_like(logp)
+    # Zero-filled once; every completed call leaves it reusable.
+    ws = torch.zeros(sa.grpo_workspace_bytes(cu, cu_host, group_size=wl.group_size), dtype=torch.uint8, device=dev)
     kw = dict(group_size=wl.group_size, clip_eps=wl.clip_eps, adv_eps=wl.adv_eps, kl_beta=wl.kl_beta,
-              logp_ref=lref if wl.kl_beta else None, dlogp=dlogp)
+              logp_ref=lref if wl.kl_beta else None, dlogp=dlogp, workspace=ws)
     flush = L2Flush(dev)
     out = {}
 

@@ -167,7 +167,12 @@ sinkattn_status sinkattn_decode_fwd(const sinkattn_problem* kv, int32_t q_per_se
  * dloss/dlogp (0 on tokens that are not optimised) and, if non-NULL,
  * advantages fp32 [num_rollouts].  With N = 0 everything is 0.  logp,
  * logp_old, logp_ref, mask and dlogp must be 16-byte aligned.  Workspace:
- * sinkattn_grpo_workspace_size bytes, 16-byte aligned, no initial content.
+ * sinkattn_grpo_workspace_size bytes, 16-byte aligned, zero-filled before
+ * its first use; every completed call leaves it reusable (its barrier words
+ * zero again).  The kernel is one cooperative launch whose CTAs meet at a
+ * grid-wide barrier with a bounded wait: if that wait runs out of time the
+ * outputs are not written, sinkattn_get_device_status reports TIMEOUT and
+ * the workspace must be zero-filled again.
  * Checks: group_size >= 1 dividing num_rollouts, clip_eps > 0, adv_eps >= 0,
  * kl_beta >= 0 (all finite), offsets as for sinkattn_problem. */
 typedef struct {

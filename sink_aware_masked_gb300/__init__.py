@@ -11,6 +11,7 @@ from .api import (  # noqa: F401
     bwd_workspace_bytes,
     decode_workspace_bytes,
     grpo_loss,
+    grpo_workspace_bytes,
     make_problem,
     sink_attention,
     sinkattn_bwd,

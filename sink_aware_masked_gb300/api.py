@@ -140,26 +140,45 @@ def sinkattn_decode_fwd(q, k, v, sink, *, q_per_seq: int, o=None, lse=None, work
     return o, lse
 
 
+def _grpo_problem(cu_tokens, cu_tokens_host, group_size, clip_eps=0.2, adv_eps=1e-6, kl_beta=0.0):
+    host = (ctypes.c_int32 * len(cu_tokens_host))(*[int(x) for x in cu_tokens_host])
+    g = _lib.GrpoProblem(num_rollouts=len(cu_tokens_host) - 1, group_size=int(group_size),
+                         cu_tokens=_ptr(cu_tokens),
+                         cu_tokens_host=ctypes.cast(host, ctypes.c_void_p).value, total_tokens=int(cu_tokens_host[-1]),
+                         clip_eps=float(clip_eps), adv_eps=float(adv_eps), kl_beta=float(kl_beta))
+    return g, host
+
+
+def grpo_workspace_bytes(cu_tokens, cu_tokens_host, *, group_size: int) -> int:
+    """Workspace bytes of grpo_loss for these rollout offsets (device tensor and host list)."""
+    lib = _lib.load()
+    g, keep = _grpo_problem(cu_tokens, cu_tokens_host, group_size)
+    n = int(lib.sinkattn_grpo_workspace_size(ctypes.byref(g)))
+    if n == 0 and len(cu_tokens_host) > 1:
+        raise ValueError("grpo_workspace_bytes: invalid rollout offsets or group size")
+    return n
+
+
 def grpo_loss(logp, logp_old, mask, rewards, cu_tokens, cu_tokens_host, *, group_size: int, clip_eps: float = 0.2,
               adv_eps: float = 1e-6, kl_beta: float = 0.0, logp_ref=None, dlogp=None, workspace=None):
     """GRPO token loss: returns (stats [4] fp32, dlogp [T] fp32, advantages [R] fp32).
 
     stats = (loss, policy term, KL term, clipped fraction); all tensors on the
     GPU (logp/logp_old/logp_ref fp32 [T], mask uint8 [T], rewards fp32 [R],
-    cu_tokens int32 [R + 1] with its host copy cu_tokens_host).
+    cu_tokens int32 [R + 1] with its host copy cu_tokens_host).  A caller
+    that passes ``workspace`` (uint8, grpo_workspace_bytes long) zero-fills it
+    once; each completed call leaves it reusable.  Without one, a zero-filled
+    workspace is allocated per call.
     """
     lib = _lib.load()
-    host = (ctypes.c_int32 * len(cu_tokens_host))(*[int(x) for x in cu_tokens_host])
     R = len(cu_tokens_host) - 1
-    g = _lib.GrpoProblem(num_rollouts=R, group_size=int(group_size), cu_tokens=_ptr(cu_tokens),
-                         cu_tokens_host=ctypes.cast(host, ctypes.c_void_p).value, total_tokens=int(cu_tokens_host[-1]),
-                         clip_eps=float(clip_eps), adv_eps=float(adv_eps), kl_beta=float(kl_beta))
+    g, keep = _grpo_problem(cu_tokens, cu_tokens_host, group_size, clip_eps, adv_eps, kl_beta)
     stats = torch.empty(4, dtype=torch.float32, device=logp.device)
     dlogp = torch.empty_like(logp) if dlogp is None else dlogp
     adv = torch.empty(R, dtype=torch.float32, device=logp.device)
     ws_bytes = int(lib.sinkattn_grpo_workspace_size(ctypes.byref(g)))
     if workspace is None:
-        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=logp.device)
+        workspace = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=logp.device)
     st = lib.sinkattn_grpo_loss(ctypes.byref(g), _ptr(logp), _ptr(logp_old), _ptr(logp_ref), _ptr(mask), _ptr(rewards),
                                 _ptr(stats), _ptr(dlogp), _ptr(adv), _ptr(workspace), workspace.numel(), _stream())
     _lib.check("sinkattn_grpo_loss", st)

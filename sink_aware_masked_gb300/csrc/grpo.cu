@@ -1,5 +1,5 @@
 // GRPO token loss and its gradient with respect to the policy's token
-// log-probabilities, fused into two passes over the tokens.
+// log-probabilities, in one cooperative kernel over the tokens.
 //
 // "Efficient Reinforcement Learning for Long-Horizon Tool-Use Agentic Tasks"
 // (SinkFlex-RL), zh page, "Policy update", equations (3)-(7):
@@ -13,20 +13,21 @@
 // the policy term.  dL/dlogp = (-dJ + beta (1 - e^r)) / N on optimised
 // tokens, dJ = rho A unless the clipped branch is strictly smaller (then 0).
 //
-// A memory-bound stream (13 bytes read and 4 written per token) over chunks
-// of 2048 tokens, each thread taking two 16-byte vectors of a chunk; both
-// passes run a persistent grid that strides over the chunks.  Pass 1 counts
-// the optimised tokens (one partial per CTA) and computes the advantages
-// (one thread per rollout).  Pass 2 needs N = sum_i T_i before it can scale
-// the gradient, so every CTA sums the pass-1 counts itself and stages the
-// rollout offsets and advantages in shared memory (8 bytes per rollout),
-// both while its first chunk's token loads are in flight; it finds each
-// vector's rollout by binary search there (the streaming loads would evict
-// the offsets from L1), writes dL/dlogp and accumulates partial sums; the
-// last CTA to finish reduces the partials in a fixed order (deterministic).
-// (Measured and not kept: staging the chunks through a shared-memory ring by
-// bulk copies, and per-chunk rollout lists; neither was faster — the pass
-// is bound by its per-token instruction latency, not by bytes in flight.)
+// A memory-bound stream (13 bytes read and 4 written per token) in a
+// persistent grid of co-resident CTAs (a cooperative launch), each CTA
+// taking an equal contiguous range of 16-byte vectors (four tokens) in
+// batches of two vectors per thread.  Only the final 1/N depends on all
+// tokens, so everything else happens before one grid-wide barrier: every
+// CTA stages the rollout offsets and computes the advantages in shared
+// memory (while its first batch's loads are in flight), bounds the rollouts
+// its range touches, finds each vector's rollout by binary lifting within
+// them, writes the unscaled gradient (keeping its last batch's in
+// registers), counts the optimised tokens and accumulates the partial sums.
+// The barrier's arrival word carries the token counts, so the last CTA to
+// arrive knows N and publishes it with the release; after the barrier each
+// CTA only scales its gradients by 1/N (the earlier batches re-read from
+// L2), and the last CTA reduces the partial sums in a fixed order
+// (deterministic).
 #include "common.cuh"
 #include "internal.h"
 
@@ -37,11 +38,13 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kVec = 2;                          // 16-byte vectors per thread and chunk
-constexpr int kTokPerCta = kThreads * kVec * 4;  // 2048 tokens per chunk
-constexpr int kRewardStage = 2048;               // rewards of one pass-1 CTA's groups staged up to this
-constexpr int kStageRollouts = 6000;             // pass 2 stages offsets and advantages up to this many rollouts
-constexpr int kLossCtasPerSm = 4;
+constexpr int kTokPerCta = kThreads * kVec * 4;  // 2048 tokens: the least work per CTA
+constexpr int kStageRollouts = 6000;             // offsets and advantages staged up to this many rollouts
+constexpr int kRegStage = 4;                     // offsets and rewards per thread loaded ahead of the tokens
 constexpr int kCtasPerSm = 4;
+constexpr int kArriveBits = 20;                  // arrival count in the low bits of the barrier word
+constexpr int kStatusTimeout = 6;                // SINKATTN_ERR_TIMEOUT, raised in the status word
+constexpr long long kTimeoutCycles = 2000000000LL;  // about one second at 2 GHz
 
 struct GrpoK {
   const float* logp;
@@ -50,14 +53,17 @@ struct GrpoK {
   const uint8_t* mask;
   const float* rewards;
   const int32_t* cu;
-  float* stats;    // [4]: loss, policy term, KL term (unscaled), clipped fraction
+  float* stats;     // [4]: loss, policy term, KL term (unscaled), clipped fraction
   float* dlogp;
-  float* adv_out;  // [R] or nullptr
-  int* counts;     // workspace [P]: optimised tokens per pass-1 CTA
-  float* adv;      // workspace [R]
-  float4* part;    // workspace [grid]: sum J, sum k3, clipped count
-  unsigned* done;  // workspace: pass-2 CTAs finished
-  int R, G, T, chunks, grid, grid2;
+  float* adv_out;   // [R] or nullptr
+  // workspace: [0] arrivals (low kArriveBits bits) plus optimised tokens
+  // (high bits), zero between launches; [16] (another 128-byte line, which
+  // the waiting CTAs poll) generation (high 32 bits) and the last N (low 32
+  // bits).
+  unsigned long long* sync;
+  float4* part;     // workspace [grid]: sum J, sum k3, clipped count per CTA
+  int* status;      // library status word
+  int R, G, T;
   float clip_eps, adv_eps, beta;
 };
 
@@ -84,88 +90,225 @@ SA_DEV int nonzero_bytes(uint32_t w) {
   return __popc(x & 0x80808080u);
 }
 
-__global__ void __launch_bounds__(kThreads) grpo_prep_kernel(const GrpoK p) {
-  __shared__ int red[kThreads / 32];
-  __shared__ float rew_s[kRewardStage];
-  const int tid = threadIdx.x;
-  // Optimised tokens of the chunks this CTA strides over, 16 per load (the
-  // first 128 threads of the CTA cover a 2048-token chunk).
-  int n = 0;
-  for (int c = blockIdx.x; c < p.chunks && tid < kTokPerCta / 16; c += gridDim.x) {
-    const long long t = static_cast<long long>(c) * kTokPerCta + 16LL * tid;
-    if (t + 16 <= p.T) {
-      const uint4 m = __ldg(reinterpret_cast<const uint4*>(p.mask + t));
-      n += nonzero_bytes(m.x) + nonzero_bytes(m.y) + nonzero_bytes(m.z) + nonzero_bytes(m.w);
-    } else {
-      for (long long u = t; u < p.T && u < t + 16; ++u) n += __ldg(p.mask + u) != 0;
-    }
-  }
-  // Equation (3) for rollouts i = 256 b + tid; the rewards of the block's
-  // groups are staged in shared memory by one coalesced load per thread.
-  for (int b = blockIdx.x; b * kThreads < p.R; b += gridDim.x) {
-    const int r_lo = min(p.R, (b * kThreads / p.G) * p.G);
-    const int r_hi = min(p.R, ((min(p.R, b * kThreads + kThreads) + p.G - 1) / p.G) * p.G);
-    const bool staged = r_hi - r_lo <= kRewardStage;
-    __syncthreads();
-    if (staged)
-      for (int j = r_lo + tid; j < r_hi; j += kThreads) rew_s[j - r_lo] = __ldg(p.rewards + j);
-    __syncthreads();
-    const int i = b * kThreads + tid;
-    if (i < p.R) {
-      // In fp32: FP64 issues at a small fraction of the FP32 rate on this part,
-      // and a group's mean and spread need no more than fp32 keeps.
-      const int g0 = (i / p.G) * p.G;
-      auto rew = [&](int j) { return staged ? rew_s[j - r_lo] : __ldg(p.rewards + j); };
-      float mu = 0.f, var = 0.f;
-      for (int j = g0; j < g0 + p.G; ++j) mu += rew(j);
-      mu /= static_cast<float>(p.G);
-      for (int j = g0; j < g0 + p.G; ++j) {
-        const float d = rew(j) - mu;
-        var += d * d;
-      }
-      const float a = (rew(i) - mu) / (sqrtf(var / static_cast<float>(p.G)) + p.adv_eps);
-      p.adv[i] = a;
-      if (p.adv_out) p.adv_out[i] = a;
-    }
-  }
-  n = block_sum(n, red);
-  if (tid == 0) {
-    p.counts[blockIdx.x] = n;
-    if (blockIdx.x == 0) *p.done = 0u;
-  }
+SA_DEV unsigned long long ld_acquire_gpu(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];\n" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+// Acquire-release add at GPU scope (returns the old value).
+SA_DEV unsigned long long atom_add_acq_rel_gpu(unsigned long long* p, unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.add.acq_rel.gpu.global.u64 %0, [%1], %2;\n" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  return old;
+}
+SA_DEV void st_release_gpu(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;\n" ::"l"(p), "l"(v) : "memory");
 }
 
-__global__ void __launch_bounds__(kThreads, kLossCtasPerSm) grpo_loss_kernel(const GrpoK p) {
-  __shared__ long long red_ll[kThreads / 32];
-  __shared__ float3 red_f3[kThreads / 32];
-  __shared__ double red_d[kThreads / 32];
-  __shared__ float sh_inv_n;
-  __shared__ bool is_last;
-  extern __shared__ int dyn_s[];  // [R + 1] offsets, then [R] advantages (when staged)
-  const int tid = threadIdx.x;
-  const bool staged = p.R <= kStageRollouts;
-  const int* cu_s = dyn_s;
-  const float* adv_s = reinterpret_cast<const float*>(dyn_s + p.R + 1);
-  long long n = 0;
-  float inv_n = 0.f;
-  const float beta = p.beta;
-  const float lo = 1.f - p.clip_eps, hi = 1.f + p.clip_eps;
-  const int nvec = p.T / 4;
-  auto cu_at = [&](int j) { return staged ? cu_s[j] : __ldg(p.cu + j); };
-  auto adv_at = [&](int i) { return staged ? adv_s[i] : __ldg(p.adv + i); };
-  // Rollout of token t: the last i with cu[i] <= t (skips empty rollouts).
-  auto rollout = [&](int t, int a, int b) {  // cu[a] <= t < cu[b]
-    while (b - a > 1) {
-      const int mid = (a + b) >> 1;
-      if (cu_at(mid) <= t) a = mid; else b = mid;
+// Barrier over the whole (co-resident) grid that also sums one count per
+// CTA.  Thread 0 of each CTA adds (count << kArriveBits) + 1 to the arrival
+// word (release: its earlier writes, the CTA's partial sums among them, are
+// visible to whoever acquires the word later); the CTA that completes it
+// (acquire: it then sees every CTA's partial sums) clears the word for the
+// next launch and publishes the next generation together with the total,
+// which the others poll for.  Only thread 0's own writes are published this
+// way, which is all the other CTAs read.  Returns the total in every thread
+// (-1 when the wait ran out of time, after raising the status word) and
+// whether this CTA arrived last.
+SA_DEV long long grid_sync_sum(unsigned long long* sync, long long count, int* status, long long* sh_total,
+                               bool* sh_last) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned gen = static_cast<unsigned>(ld_acquire_gpu(sync + 16) >> 32);
+    const unsigned long long add = (static_cast<unsigned long long>(count) << kArriveBits) + 1ull;
+    const unsigned long long old = atom_add_acq_rel_gpu(sync, add);
+    long long total = -1;
+    bool last = false;
+    if ((old & ((1ull << kArriveBits) - 1ull)) == gridDim.x - 1) {
+      total = static_cast<long long>((old + add) >> kArriveBits);
+      last = true;
+      *reinterpret_cast<volatile unsigned long long*>(sync) = 0ull;  // no CTA touches it again this launch
+      st_release_gpu(sync + 16, (static_cast<unsigned long long>(gen + 1u) << 32) | static_cast<unsigned long long>(total));
+    } else {
+      const long long t0 = clock64();
+      for (;;) {
+        const unsigned long long w = ld_acquire_gpu(sync + 16);
+        if (static_cast<unsigned>(w >> 32) != gen) {
+          total = static_cast<long long>(w & 0xFFFFFFFFull);
+          break;
+        }
+        if (clock64() - t0 > kTimeoutCycles) {
+          atomicExch(status, kStatusTimeout);
+          break;
+        }
+        __nanosleep(20);
+      }
     }
+    *sh_total = total;
+    *sh_last = last;
+  }
+  __syncthreads();
+  return *sh_total;
+}
+
+// Mean and population std + eps of the rewards of one group (shared or
+// global memory), by one thread.
+SA_DEV float2 group_stats(const float* rew, int g0, int G, float eps) {
+  float mu = 0.f, var = 0.f;
+  for (int j = g0; j < g0 + G; ++j) mu += rew[j];
+  mu /= static_cast<float>(G);
+  for (int j = g0; j < g0 + G; ++j) {
+    const float d = rew[j] - mu;
+    var += d * d;
+  }
+  return make_float2(mu, sqrtf(var / static_cast<float>(G)) + eps);
+}
+
+// The same by one warp (lanes stride over the group); valid in every lane.
+SA_DEV float2 group_stats_warp(const float* rew, int g0, int G, float eps) {
+  const int lane = threadIdx.x & 31;
+  float mu = 0.f, var = 0.f;
+  for (int j = g0 + lane; j < g0 + G; j += 32) mu += rew[j];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mu += __shfl_xor_sync(0xffffffffu, mu, o);
+  mu /= static_cast<float>(G);
+  for (int j = g0 + lane; j < g0 + G; j += 32) {
+    const float d = rew[j] - mu;
+    var += d * d;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) var += __shfl_xor_sync(0xffffffffu, var, o);
+  return make_float2(mu, sqrtf(var / static_cast<float>(G)) + eps);
+}
+
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) grpo_kernel(const GrpoK p) {
+  __shared__ int red_i[kThreads / 32];
+  __shared__ float3 red_f3[kThreads / 32];
+  __shared__ long long sh_total;
+  __shared__ bool sh_last;
+  extern __shared__ int dyn_s[];  // staged: [R + 1] offsets, then [R] advantages
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool staged = p.R <= kStageRollouts;
+  int* cu_s = dyn_s;
+  float* adv_s = reinterpret_cast<float*>(dyn_s + p.R + 1);
+  const float beta = p.beta;
+  const int nvec = p.T / 4;
+  const int G = p.G, ngroups = p.R / p.G;
+  // This CTA's vectors [v_lo, v_hi): an equal share in units of 32 vectors
+  // (128 tokens), taken by the threads in batches of kVec * kThreads.
+  const int n32 = (nvec + 31) / 32;
+  const int v_lo = static_cast<int>(static_cast<long long>(blockIdx.x) * n32 / gridDim.x) * 32;
+  const int v_hi = min(nvec, static_cast<int>(static_cast<long long>(blockIdx.x + 1) * n32 / gridDim.x) * 32);
+  const int nbatch = (v_hi - v_lo + kThreads * kVec - 1) / (kThreads * kVec);
+  auto vec_of = [&](int b, int k) { return v_lo + b * (kThreads * kVec) + tid + kThreads * k; };
+
+  float4 lp[kVec], old[kVec], lr[kVec];
+  uint32_t mk[kVec];
+  auto load_batch = [&](int b) {
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) {
+      const int v = vec_of(b, k);
+      if (v < v_hi) {
+        lp[k] = __ldg(reinterpret_cast<const float4*>(p.logp) + v);
+        old[k] = __ldg(reinterpret_cast<const float4*>(p.logp_old) + v);
+        lr[k] = beta != 0.f ? __ldg(reinterpret_cast<const float4*>(p.logp_ref) + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+        mk[k] = __ldg(reinterpret_cast<const uint32_t*>(p.mask) + v);
+      }
+    }
+  };
+  // Equation (3): every CTA stages all offsets and advantages (CTA 0 also
+  // writes the advantages out): the rewards are loaded into the advantage
+  // slots, and each group's statistics are computed and its slots
+  // overwritten by the thread (G <= 32) or warp that owns the group.  Beyond
+  // kStageRollouts rollouts the grid writes the advantages out and each
+  // token computes its own.
+  // The offsets and rewards are loaded before the first batch's token
+  // loads (loads return in about the order they were issued), and the group
+  // statistics are computed while the token loads are in flight.
+  if (staged) {
+    const bool write_adv = p.adv_out != nullptr && blockIdx.x == 0;
+    int cu_r[kRegStage];
+    float rw_r[kRegStage];
+#pragma unroll
+    for (int q = 0; q < kRegStage; ++q) {
+      const int j = tid + kThreads * q;
+      if (j <= p.R) cu_r[q] = __ldg(p.cu + j);
+      if (j < p.R) rw_r[q] = __ldg(p.rewards + j);
+    }
+    if (nbatch > 0) load_batch(0);
+#pragma unroll
+    for (int q = 0; q < kRegStage; ++q) {
+      const int j = tid + kThreads * q;
+      if (j <= p.R) cu_s[j] = cu_r[q];
+      if (j < p.R) adv_s[j] = rw_r[q];
+    }
+    for (int j = tid + kThreads * kRegStage; j <= p.R; j += kThreads) {
+      cu_s[j] = __ldg(p.cu + j);
+      if (j < p.R) adv_s[j] = __ldg(p.rewards + j);
+    }
+    __syncthreads();
+    if (G <= 32) {
+      for (int grp = tid; grp < ngroups; grp += kThreads) {
+        const int g0 = grp * G;
+        const float2 st = group_stats(adv_s, g0, G, p.adv_eps);
+        for (int j = g0; j < g0 + G; ++j) {
+          const float a = (adv_s[j] - st.x) / st.y;
+          adv_s[j] = a;
+          if (write_adv) p.adv_out[j] = a;
+        }
+      }
+    } else {
+      for (int grp = warp; grp < ngroups; grp += kThreads / 32) {
+        const int g0 = grp * G;
+        const float2 st = group_stats_warp(adv_s, g0, G, p.adv_eps);  // every lane has read the group
+        for (int j = g0 + lane; j < g0 + G; j += 32) {
+          const float a = (adv_s[j] - st.x) / st.y;
+          adv_s[j] = a;
+          if (write_adv) p.adv_out[j] = a;
+        }
+      }
+    }
+    __syncthreads();
+  } else {
+    if (nbatch > 0) load_batch(0);
+    if (p.adv_out != nullptr)
+    for (int grp = blockIdx.x * kThreads + tid; grp < ngroups; grp += gridDim.x * kThreads) {
+      const int g0 = grp * G;
+      const float2 st = group_stats(p.rewards, g0, G, p.adv_eps);
+      for (int j = g0; j < g0 + G; ++j) p.adv_out[j] = (__ldg(p.rewards + j) - st.x) / st.y;
+    }
+  }
+  auto cu_at = [&](int j) { return staged ? cu_s[j] : __ldg(p.cu + j); };
+  auto adv_at = [&](int i) -> float {
+    if (staged) return adv_s[i];
+    const float2 st = group_stats(p.rewards, (i / G) * G, G, p.adv_eps);
+    return (__ldg(p.rewards + i) - st.x) / st.y;
+  };
+  // Rollout of token t: the last i with cu[i] <= t (skips empty rollouts),
+  // by binary lifting from a over steps top, top / 2, ..., 1 within [a, b]
+  // (cu[a] <= t).  The rollouts of this CTA's range bound every search.
+  auto lift = [&](int t, int a, int b, int top) {
+    for (int step = top; step > 0; step >>= 1)
+      if (a + step <= b && cu_at(a + step) <= t) a += step;
     return a;
   };
-  float sj = 0.f, sk = 0.f, sc = 0.f;
-  auto token = [&](float x, float xo, float xr, bool m, float A) -> float {
+  auto pow2_floor = [](int x) { return x > 0 ? 1 << (31 - __clz(x)) : 0; };
+  const int r_first = v_hi > v_lo ? lift(4 * v_lo, 0, p.R - 1, pow2_floor(p.R - 1)) : 0;
+  const int r_last = v_hi > v_lo ? lift(4 * v_hi - 1, r_first, p.R - 1, pow2_floor(p.R - 1 - r_first)) : 0;
+  const int top = pow2_floor(r_last - r_first);
+
+  const float lo = 1.f - p.clip_eps, hi = 1.f + p.clip_eps;
+  float sj = 0.f, sk = 0.f;
+  int nclip = 0, n = 0;
+  // One token: returns the unscaled gradient -dJ + beta dk3 (0 when not
+  // optimised).  With s = sign(A) and sb = s * (the bound on A's side of the
+  // clip), J = |A| min(s rho, sb) and the clip removes the gradient exactly
+  // when s rho > sb (sb = +inf for A = 0).
+  auto token = [&](float x, float xo, float xr, uint32_t mbyte, float absA, float s, float sb, float A) -> float {
     const float rho = expf(x - xo);
-    const float J = fminf(rho * A, fminf(fmaxf(rho, lo), hi) * A);
-    const bool clipped = (A > 0.f && rho > hi) || (A < 0.f && rho < lo);
+    const float sr = s * rho;
+    const float J = absA * fminf(sr, sb);
+    const bool clipped = sr > sb;
     float g = clipped ? 0.f : -rho * A;
     float k3 = 0.f;
     if (beta != 0.f) {
@@ -174,74 +317,88 @@ __global__ void __launch_bounds__(kThreads, kLossCtasPerSm) grpo_loss_kernel(con
       k3 = (e - 1.f) - r;
       g += beta * (1.f - e);
     }
+    const bool m = mbyte != 0u;
     if (m) {
       sj += J;
       sk += k3;
-      sc += clipped ? 1.f : 0.f;
+      nclip += clipped;
     }
-    return m ? g * inv_n : 0.f;
+    return m ? g : 0.f;
   };
-  for (int c = blockIdx.x; c < p.chunks; c += gridDim.x) {
-    // The chunk's token loads first.
-    float4 lp[kVec], old[kVec], lr[kVec];
-    uchar4 mk[kVec];
+  auto side = [&](float A, float& absA, float& s, float& sb) {
+    absA = fabsf(A);
+    s = A > 0.f ? 1.f : -1.f;
+    sb = A > 0.f ? hi : (A < 0.f ? -lo : __int_as_float(0x7f800000));
+  };
+  auto tokens4 = [&](int t, float4 x, float4 xo, float4 xr, uint32_t mw, int i0) -> float4 {
+    const float A0 = adv_at(i0);
+    float absA, s, sb;
+    side(A0, absA, s, sb);
+    float4 d;
+    if (t + 3 < cu_at(i0 + 1)) {  // the usual case: all four in rollout i0
+      d.x = token(x.x, xo.x, xr.x, mw & 0xFFu, absA, s, sb, A0);
+      d.y = token(x.y, xo.y, xr.y, mw & 0xFF00u, absA, s, sb, A0);
+      d.z = token(x.z, xo.z, xr.z, mw & 0xFF0000u, absA, s, sb, A0);
+      d.w = token(x.w, xo.w, xr.w, mw & 0xFF000000u, absA, s, sb, A0);
+    } else {
+      d.x = token(x.x, xo.x, xr.x, mw & 0xFFu, absA, s, sb, A0);
+      const float A1 = adv_at(lift(t + 1, i0, r_last, top));
+      side(A1, absA, s, sb);
+      d.y = token(x.y, xo.y, xr.y, mw & 0xFF00u, absA, s, sb, A1);
+      const float A2 = adv_at(lift(t + 2, i0, r_last, top));
+      side(A2, absA, s, sb);
+      d.z = token(x.z, xo.z, xr.z, mw & 0xFF0000u, absA, s, sb, A2);
+      const float A3 = adv_at(lift(t + 3, i0, r_last, top));
+      side(A3, absA, s, sb);
+      d.w = token(x.w, xo.w, xr.w, mw & 0xFF000000u, absA, s, sb, A3);
+    }
+    return d;
+  };
+
+  // ---- before the barrier: unscaled gradients, counts and partial sums.
+  float4 dl[kVec];  // the last batch's unscaled gradients stay here
+  for (int b = 0; b < nbatch; ++b) {
+    if (b > 0) load_batch(b);
+    int ia[kVec];
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) ia[k] = r_first;
+    for (int step = top; step > 0; step >>= 1) {
+#pragma unroll
+      for (int k = 0; k < kVec; ++k)
+        if (ia[k] + step <= r_last && cu_at(ia[k] + step) <= 4 * vec_of(b, k)) ia[k] += step;
+    }
 #pragma unroll
     for (int k = 0; k < kVec; ++k) {
-      const int v = c * (kTokPerCta / 4) + tid + kThreads * k;
-      if (v < nvec) {
-        lp[k] = __ldg(reinterpret_cast<const float4*>(p.logp) + v);
-        old[k] = __ldg(reinterpret_cast<const float4*>(p.logp_old) + v);
-        lr[k] = beta != 0.f ? __ldg(reinterpret_cast<const float4*>(p.logp_ref) + v) : make_float4(0.f, 0.f, 0.f, 0.f);
-        mk[k] = __ldg(reinterpret_cast<const uchar4*>(p.mask) + v);
+      const int v = vec_of(b, k);
+      if (v < v_hi) {
+        n += nonzero_bytes(mk[k]);
+        const float4 d = tokens4(4 * v, lp[k], old[k], lr[k], mk[k], ia[k]);
+        if (b == nbatch - 1) dl[k] = d;
+        else reinterpret_cast<float4*>(p.dlogp)[v] = d;
       }
     }
-    if (c == static_cast<int>(blockIdx.x)) {
-      // N = sum of the pass-1 counts (every CTA sums them itself) and the
-      // staged offsets and advantages, while the first chunk's loads are in flight.
-      if (staged) {
-        for (int j = tid; j <= p.R; j += kThreads) dyn_s[j] = __ldg(p.cu + j);
-        for (int j = tid; j < p.R; j += kThreads) reinterpret_cast<float*>(dyn_s + p.R + 1)[j] = __ldg(p.adv + j);
-      }
-      for (int j = tid; j < p.grid; j += kThreads) n += __ldcg(p.counts + j);
-      n = block_sum(n, red_ll);
-      if (tid == 0) sh_inv_n = n > 0 ? static_cast<float>(1.0 / static_cast<double>(n)) : 0.f;
-      __syncthreads();
-      inv_n = sh_inv_n;
-    }
-#pragma unroll
-    for (int k = 0; k < kVec; ++k) {
-      const int v = c * (kTokPerCta / 4) + tid + kThreads * k;
-      if (v < nvec) {
-        const int t = 4 * v;
-        const int i0 = rollout(t, 0, p.R);
-        const float a0 = adv_at(i0);
-        // The four tokens usually share the rollout; otherwise look each up.
-        const bool same = t + 3 < cu_at(i0 + 1);
-        float4 d;
-        d.x = token(lp[k].x, old[k].x, lr[k].x, mk[k].x != 0, a0);
-        d.y = token(lp[k].y, old[k].y, lr[k].y, mk[k].y != 0, same ? a0 : adv_at(rollout(t + 1, i0, p.R)));
-        d.z = token(lp[k].z, old[k].z, lr[k].z, mk[k].z != 0, same ? a0 : adv_at(rollout(t + 2, i0, p.R)));
-        d.w = token(lp[k].w, old[k].w, lr[k].w, mk[k].w != 0, same ? a0 : adv_at(rollout(t + 3, i0, p.R)));
-        reinterpret_cast<float4*>(p.dlogp)[v] = d;
-      }
-    }
-    // The last T % 4 tokens belong to the chunk that would hold vector nvec.
-    if (tid == 0 && nvec / (kTokPerCta / 4) == c)
-      for (int t = 4 * nvec; t < p.T; ++t)
-        p.dlogp[t] = token(__ldg(p.logp + t), __ldg(p.logp_old + t), beta != 0.f ? __ldg(p.logp_ref + t) : 0.f,
-                           __ldg(p.mask + t) != 0, adv_at(rollout(t, 0, p.R)));
   }
-  // One reduction of the three partial sums.
-  float3 s3 = make_float3(sj, sk, sc);
+  // The last T % 4 tokens: thread 0 of the last CTA (its range ends at nvec).
+  const bool tail = tid == 0 && blockIdx.x == gridDim.x - 1;
+  if (tail)
+    for (int t = 4 * nvec; t < p.T; ++t) {
+      const uint32_t m = __ldg(p.mask + t);
+      n += m != 0u;
+      const float A = adv_at(lift(t, 0, p.R - 1, pow2_floor(p.R - 1)));
+      float absA, s, sb;
+      side(A, absA, s, sb);
+      p.dlogp[t] = token(__ldg(p.logp + t), __ldg(p.logp_old + t), beta != 0.f ? __ldg(p.logp_ref + t) : 0.f, m, absA,
+                         s, sb, A);
+    }
+  float3 s3 = make_float3(sj, sk, static_cast<float>(nclip));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     s3.x += __shfl_xor_sync(0xffffffffu, s3.x, o);
     s3.y += __shfl_xor_sync(0xffffffffu, s3.y, o);
     s3.z += __shfl_xor_sync(0xffffffffu, s3.z, o);
   }
-  __syncthreads();
-  if ((tid & 31) == 0) red_f3[tid >> 5] = s3;
-  __syncthreads();
+  if (lane == 0) red_f3[warp] = s3;
+  n = block_sum(n, red_i);  // its barriers also publish red_f3
   if (tid == 0) {
     float3 t3 = make_float3(0.f, 0.f, 0.f);
     for (int w = 0; w < kThreads / 32; ++w) {
@@ -250,68 +407,107 @@ __global__ void __launch_bounds__(kThreads, kLossCtasPerSm) grpo_loss_kernel(con
       t3.z += red_f3[w].z;
     }
     p.part[blockIdx.x] = make_float4(t3.x, t3.y, t3.z, 0.f);
-    __threadfence();
-    is_last = atomicAdd(p.done, 1u) == gridDim.x - 1;
   }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
+  const long long N = grid_sync_sum(p.sync, n, p.status, &sh_total, &sh_last);
+  if (N < 0) return;
+
+  // ---- after the barrier: scale by 1/N.
+  // fp32 throughout: FP64 issues at a small fraction of the FP32 rate on this part.
+  const float inv_n = N > 0 ? __frcp_rn(static_cast<float>(N)) : 0.f;
+  auto scale = [&](float4 d) { return make_float4(d.x * inv_n, d.y * inv_n, d.z * inv_n, d.w * inv_n); };
+  for (int b = 0; b < nbatch - 1; ++b) {
+    // Written by this same thread before the barrier.
+    float4 d[kVec];
+#pragma unroll
+    for (int k = 0; k < kVec; ++k)
+      if (vec_of(b, k) < v_hi) d[k] = __ldcg(reinterpret_cast<const float4*>(p.dlogp) + vec_of(b, k));
+#pragma unroll
+    for (int k = 0; k < kVec; ++k)
+      if (vec_of(b, k) < v_hi) reinterpret_cast<float4*>(p.dlogp)[vec_of(b, k)] = scale(d[k]);
+  }
+  if (nbatch > 0) {
+#pragma unroll
+    for (int k = 0; k < kVec; ++k)
+      if (vec_of(nbatch - 1, k) < v_hi) reinterpret_cast<float4*>(p.dlogp)[vec_of(nbatch - 1, k)] = scale(dl[k]);
+  }
+  if (tail)
+    for (int t = 4 * nvec; t < p.T; ++t) p.dlogp[t] = __ldcg(p.dlogp + t) * inv_n;
+
+  // ---- the last CTA to arrive: the loss terms from the partial sums.
+  if (!sh_last) return;  // thread 0 acquired every CTA's partial sums at the barrier
   // Every thread sums a fixed strided subset of the partials, then a fixed
-  // shuffle tree: the result does not depend on which CTA finished last.
-  double dj = 0.0, dk = 0.0, dc = 0.0;
+  // shuffle tree and the eight warp sums in order: the result does not
+  // depend on which CTA arrived last.
+  float3 t3 = make_float3(0.f, 0.f, 0.f);
   for (int j = tid; j < static_cast<int>(gridDim.x); j += kThreads) {
     const float4 v = __ldcg(p.part + j);
-    dj += v.x;
-    dk += v.y;
-    dc += v.z;
+    t3.x += v.x;
+    t3.y += v.y;
+    t3.z += v.z;
   }
-  dj = block_sum(dj, red_d);
-  dk = block_sum(dk, red_d);
-  dc = block_sum(dc, red_d);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    t3.x += __shfl_xor_sync(0xffffffffu, t3.x, o);
+    t3.y += __shfl_xor_sync(0xffffffffu, t3.y, o);
+    t3.z += __shfl_xor_sync(0xffffffffu, t3.z, o);
+  }
+  __syncthreads();
+  if (lane == 0) red_f3[warp] = t3;
+  __syncthreads();
   if (tid == 0) {
-    const double inv = n > 0 ? 1.0 / static_cast<double>(n) : 0.0;
-    const double policy = -dj * inv, kl = dk * inv;
-    p.stats[0] = static_cast<float>(policy + static_cast<double>(beta) * kl);
-    p.stats[1] = static_cast<float>(policy);
-    p.stats[2] = static_cast<float>(kl);
-    p.stats[3] = static_cast<float>(dc * inv);
+    float dj = 0.f, dk = 0.f, dc = 0.f;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      dj += red_f3[w].x;
+      dk += red_f3[w].y;
+      dc += red_f3[w].z;
+    }
+    const float policy = -dj * inv_n, kl = dk * inv_n;
+    p.stats[0] = policy + beta * kl;
+    p.stats[1] = policy;
+    p.stats[2] = kl;
+    p.stats[3] = dc * inv_n;
   }
 }
 
-int num_chunks(int T) { return std::max(1, (T + kTokPerCta - 1) / kTokPerCta); }
-
-int grid_ctas(int T) {
+// Grid bound: one CTA per 512 vectors (2048 tokens) at most, and at most
+// kCtasPerSm per SM.
+int max_ctas(int T) {
   static int sms = 0;
   if (sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      sms = 0;
-    if (sms <= 0) sms = 152;
+    int dev = 0, s = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&s, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        s <= 0)
+      s = 152;
+    sms = s;
   }
-  return std::min(num_chunks(T), kCtasPerSm * sms);
-}
-
-int loss_ctas(int T) {
-  int sms = 0, dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      sms <= 0)
-    sms = 152;
-  return std::min(num_chunks(T), kLossCtasPerSm * sms);
+  const int by_work = std::max(1, (T / 4 + kTokPerCta / 4 - 1) / (kTokPerCta / 4));
+  return std::min(by_work, kCtasPerSm * sms);
 }
 
 size_t a256(size_t x) { return (x + 255) / 256 * 256; }
 
+size_t dyn_bytes(int R) { return R <= kStageRollouts ? (2 * static_cast<size_t>(R) + 1) * 4 : 0; }
+
 }  // namespace
 
 size_t grpo_workspace_bytes(int num_rollouts, int total_tokens) {
-  const size_t G = static_cast<size_t>(grid_ctas(total_tokens)), G2 = static_cast<size_t>(loss_ctas(total_tokens));
-  return a256(G * 4) + a256(static_cast<size_t>(num_rollouts) * 4) + a256(G2 * 16) + 256;
+  (void)num_rollouts;
+  return 256 + a256(static_cast<size_t>(max_ctas(total_tokens)) * 16);
 }
 
 cudaError_t launch_grpo(const GrpoArgs& a, cudaStream_t stream) {
   if (a.num_rollouts == 0) return cudaSuccess;
-  const int grid = grid_ctas(a.total_tokens), chunks = num_chunks(a.total_tokens);
-  const int grid2 = loss_ctas(a.total_tokens);
+  const size_t dyn = dyn_bytes(a.num_rollouts);
+  // Every CTA waits at the grid barrier, so the grid must be co-resident.
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, grpo_kernel, kThreads, dyn);
+  if (e != cudaSuccess) return e;
+  if (per_sm <= 0) return cudaErrorInvalidConfiguration;
+  int sms = 0, dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess || (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  const int grid = std::min(max_ctas(a.total_tokens), per_sm * sms);
+  if (grid >= (1 << kArriveBits)) return cudaErrorInvalidConfiguration;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   GrpoK k;
   k.logp = a.logp;
@@ -323,29 +519,26 @@ cudaError_t launch_grpo(const GrpoArgs& a, cudaStream_t stream) {
   k.stats = a.stats;
   k.dlogp = a.dlogp;
   k.adv_out = a.advantages;
-  size_t off = 0;
-  k.counts = reinterpret_cast<int*>(ws + off);
-  off += a256(static_cast<size_t>(grid) * 4);
-  k.adv = reinterpret_cast<float*>(ws + off);
-  off += a256(static_cast<size_t>(a.num_rollouts) * 4);
-  k.part = reinterpret_cast<float4*>(ws + off);
-  off += a256(static_cast<size_t>(grid2) * 16);
-  k.done = reinterpret_cast<unsigned*>(ws + off);
+  k.sync = reinterpret_cast<unsigned long long*>(ws);
+  k.part = reinterpret_cast<float4*>(ws + 256);
+  k.status = a.status;
   k.R = a.num_rollouts;
   k.G = a.group_size;
   k.T = a.total_tokens;
-  k.chunks = chunks;
-  k.grid = grid;
-  k.grid2 = grid2;
   k.clip_eps = a.clip_eps;
   k.adv_eps = a.adv_eps;
   k.beta = a.kl_beta;
-  grpo_prep_kernel<<<grid, kThreads, 0, stream>>>(k);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const size_t dyn = a.num_rollouts <= kStageRollouts ? (2 * static_cast<size_t>(a.num_rollouts) + 1) * 4 : 0;
-  grpo_loss_kernel<<<grid2, kThreads, dyn, stream>>>(k);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = dyn;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, grpo_kernel, k);
 }
 
 }  // namespace sa

@@ -113,7 +113,8 @@ struct GrpoArgs {
   float* stats;       // [4]
   float* dlogp;
   float* advantages;  // or nullptr
-  void* workspace;
+  void* workspace;   // barrier words zero on entry (left zero on exit)
+  int* status;        // library status word (the grid barrier's bounded wait)
 };
 size_t grpo_workspace_bytes(int num_rollouts, int total_tokens);
 cudaError_t launch_grpo(const GrpoArgs& a, cudaStream_t s);

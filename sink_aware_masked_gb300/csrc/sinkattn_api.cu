@@ -298,7 +298,8 @@ sinkattn_status sinkattn_grpo_loss(const sinkattn_grpo_problem* g, const float* 
   if (!aligned16(workspace)) return workspace ? SINKATTN_ERR_ALIGNMENT : SINKATTN_ERR_INVALID_ARG;
   if (workspace_bytes < sa::grpo_workspace_bytes(g->num_rollouts, g->total_tokens)) return SINKATTN_ERR_WORKSPACE;
   sa::GrpoArgs a{g->num_rollouts, g->group_size, g->total_tokens, g->cu_tokens, g->clip_eps, g->adv_eps, g->kl_beta,
-                 logp, logp_old, logp_ref, mask, rewards, stats, dlogp, advantages, workspace};
+                 logp, logp_old, logp_ref, mask, rewards, stats, dlogp, advantages, workspace, status_word()};
+  if (a.status == nullptr) return SINKATTN_ERR_CUDA;
   return from_cuda(sa::launch_grpo(a, static_cast<cudaStream_t>(stream)));
 }
 
