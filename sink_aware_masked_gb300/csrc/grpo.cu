@@ -30,21 +30,23 @@
 // (deterministic).
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 #include <algorithm>
 
 namespace sa {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kVec = 2;                          // 16-byte vectors per thread and chunk
-constexpr int kTokPerCta = kThreads * kVec * 4;  // 2048 tokens: the least work per CTA
+using namespace tc;
+
+constexpr int kThreads = 512;
+constexpr int kStageVec = kThreads;              // 16-byte vectors (four tokens) per stage: one per thread
+constexpr int kStageBytes = kStageVec * 52;      // logp, logp_old, logp_ref (16 B each) and mask (4 B) per vector
+constexpr int kStages = 4;                       // shared-memory ring of stages
 constexpr int kStageRollouts = 6000;             // offsets and advantages staged up to this many rollouts
-constexpr int kRegStage = 4;                     // offsets and rewards per thread loaded ahead of the tokens
-constexpr int kCtasPerSm = 4;
+constexpr int kRegStage = 2;                     // offsets and rewards per thread loaded ahead of the tokens
+constexpr int kCtasPerSm = 2;
 constexpr int kArriveBits = 20;                  // arrival count in the low bits of the barrier word
-constexpr int kStatusTimeout = 6;                // SINKATTN_ERR_TIMEOUT, raised in the status word
-constexpr long long kTimeoutCycles = 2000000000LL;  // about one second at 2 GHz
 
 struct GrpoK {
   const float* logp;
@@ -141,7 +143,7 @@ SA_DEV long long grid_sync_sum(unsigned long long* sync, long long count, int* s
           atomicExch(status, kStatusTimeout);
           break;
         }
-        __nanosleep(20);
+        __nanosleep(64);
       }
     }
     *sh_total = total;
@@ -182,60 +184,73 @@ SA_DEV float2 group_stats_warp(const float* rew, int g0, int G, float eps) {
 }
 
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) grpo_kernel(const GrpoK p) {
+  __shared__ uint64_t full[kStages];
+  __shared__ int abort_flag;
   __shared__ int red_i[kThreads / 32];
   __shared__ float3 red_f3[kThreads / 32];
   __shared__ long long sh_total;
   __shared__ bool sh_last;
-  extern __shared__ int dyn_s[];  // staged: [R + 1] offsets, then [R] advantages
+  // Dynamic shared memory: kStages stages of kStageBytes (logp [512 x 16 B],
+  // logp_old, logp_ref, mask [512 x 4 B]), then, when staged, [R + 1]
+  // offsets and [R] advantages.
+  extern __shared__ __align__(128) uint8_t dyn_raw[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool staged = p.R <= kStageRollouts;
-  int* cu_s = dyn_s;
-  float* adv_s = reinterpret_cast<float*>(dyn_s + p.R + 1);
+  int* cu_s = reinterpret_cast<int*>(dyn_raw + kStages * kStageBytes);
+  float* adv_s = reinterpret_cast<float*>(cu_s + p.R + 1);
   const float beta = p.beta;
   const int nvec = p.T / 4;
   const int G = p.G, ngroups = p.R / p.G;
   // This CTA's vectors [v_lo, v_hi): an equal share in units of 32 vectors
-  // (128 tokens), taken by the threads in batches of kVec * kThreads.
+  // (128 tokens), in stages of kStageVec vectors.
   const int n32 = (nvec + 31) / 32;
   const int v_lo = static_cast<int>(static_cast<long long>(blockIdx.x) * n32 / gridDim.x) * 32;
   const int v_hi = min(nvec, static_cast<int>(static_cast<long long>(blockIdx.x + 1) * n32 / gridDim.x) * 32);
-  const int nbatch = (v_hi - v_lo + kThreads * kVec - 1) / (kThreads * kVec);
-  auto vec_of = [&](int b, int k) { return v_lo + b * (kThreads * kVec) + tid + kThreads * k; };
-
-  float4 lp[kVec], old[kVec], lr[kVec];
-  uint32_t mk[kVec];
-  auto load_batch = [&](int b) {
-#pragma unroll
-    for (int k = 0; k < kVec; ++k) {
-      const int v = vec_of(b, k);
-      if (v < v_hi) {
-        lp[k] = __ldg(reinterpret_cast<const float4*>(p.logp) + v);
-        old[k] = __ldg(reinterpret_cast<const float4*>(p.logp_old) + v);
-        lr[k] = beta != 0.f ? __ldg(reinterpret_cast<const float4*>(p.logp_ref) + v) : make_float4(0.f, 0.f, 0.f, 0.f);
-        mk[k] = __ldg(reinterpret_cast<const uint32_t*>(p.mask) + v);
-      }
-    }
+  const int nstage = (v_hi - v_lo + kStageVec - 1) / kStageVec;
+  const uint32_t sbase = smem_u32(dyn_raw);
+  if (tid == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&full[s]), 1);
+    fence_mbar_init();
+  }
+  const Abort ab{&abort_flag, p.status};
+  // Stage b: vectors [v0, v1) of the four arrays by bulk copies (16-byte
+  // aligned: v0 is a multiple of 32); the mask of the last v1 - v0 mod 4
+  // vectors, if any, is read from global memory instead.
+  auto issue = [&](int b) {
+    const int v0 = v_lo + b * kStageVec, nv = min(kStageVec, v_hi - v0), nvm = nv & ~3;
+    const uint32_t bar = smem_u32(&full[b % kStages]);
+    const uint32_t dst = sbase + (b % kStages) * kStageBytes;
+    mbar_expect_tx(bar, nv * (beta != 0.f ? 48 : 32) + nvm * 4);
+    bulk_load(dst, p.logp + 4LL * v0, nv * 16, bar);
+    bulk_load(dst + kStageVec * 16, p.logp_old + 4LL * v0, nv * 16, bar);
+    if (beta != 0.f) bulk_load(dst + kStageVec * 32, p.logp_ref + 4LL * v0, nv * 16, bar);
+    if (nvm > 0) bulk_load(dst + kStageVec * 48, p.mask + 4LL * v0, nvm * 4, bar);
   };
+
   // Equation (3): every CTA stages all offsets and advantages (CTA 0 also
   // writes the advantages out): the rewards are loaded into the advantage
   // slots, and each group's statistics are computed and its slots
-  // overwritten by the thread (G <= 32) or warp that owns the group.  Beyond
-  // kStageRollouts rollouts the grid writes the advantages out and each
-  // token computes its own.
-  // The offsets and rewards are loaded before the first batch's token
-  // loads (loads return in about the order they were issued), and the group
-  // statistics are computed while the token loads are in flight.
+  // overwritten by the thread (G <= 32) or warp that owns the group.  The
+  // first offsets and rewards are loaded before the token copies are issued
+  // and stored after, so that the statistics are computed while the copies
+  // are in flight.  Beyond kStageRollouts rollouts the grid writes the
+  // advantages out and each token computes its own.
+  int cu_r[kRegStage];
+  float rw_r[kRegStage];
   if (staged) {
-    const bool write_adv = p.adv_out != nullptr && blockIdx.x == 0;
-    int cu_r[kRegStage];
-    float rw_r[kRegStage];
 #pragma unroll
     for (int q = 0; q < kRegStage; ++q) {
       const int j = tid + kThreads * q;
       if (j <= p.R) cu_r[q] = __ldg(p.cu + j);
       if (j < p.R) rw_r[q] = __ldg(p.rewards + j);
     }
-    if (nbatch > 0) load_batch(0);
+  }
+  __syncthreads();  // the barriers are initialised
+  if (tid == 0)
+    for (int b = 0; b < min(nstage, kStages); ++b) issue(b);
+  if (staged) {
+    const bool write_adv = p.adv_out != nullptr && blockIdx.x == 0;
 #pragma unroll
     for (int q = 0; q < kRegStage; ++q) {
       const int j = tid + kThreads * q;
@@ -269,9 +284,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) grpo_kernel(const GrpoK 
       }
     }
     __syncthreads();
-  } else {
-    if (nbatch > 0) load_batch(0);
-    if (p.adv_out != nullptr)
+  } else if (p.adv_out != nullptr) {
     for (int grp = blockIdx.x * kThreads + tid; grp < ngroups; grp += gridDim.x * kThreads) {
       const int g0 = grp * G;
       const float2 st = group_stats(p.rewards, g0, G, p.adv_eps);
@@ -309,14 +322,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) grpo_kernel(const GrpoK 
     const float sr = s * rho;
     const float J = absA * fminf(sr, sb);
     const bool clipped = sr > sb;
-    float g = clipped ? 0.f : -rho * A;
-    float k3 = 0.f;
+    float k3 = 0.f, gk = 0.f;  // k3 and beta dk3/dlogp = beta (1 - e^r)
     if (beta != 0.f) {
       const float r = xr - x;
       const float e = expf(r);
       k3 = (e - 1.f) - r;
-      g += beta * (1.f - e);
+      gk = fmaf(-beta, e, beta);
     }
+    const float g = clipped ? gk : fmaf(-rho, A, gk);
     const bool m = mbyte != 0u;
     if (m) {
       sj += J;
@@ -355,28 +368,62 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) grpo_kernel(const GrpoK 
     return d;
   };
 
+
   // ---- before the barrier: unscaled gradients, counts and partial sums.
-  float4 dl[kVec];  // the last batch's unscaled gradients stay here
-  for (int b = 0; b < nbatch; ++b) {
-    if (b > 0) load_batch(b);
-    int ia[kVec];
+  // Thread tid takes vector tid of each stage; the gradients of the last
+  // group of kStages stages stay in registers, earlier ones are written out
+  // unscaled (and re-read after the barrier).
+  float4 dk[kStages];
+  bool failed = false;
+  int consumed = 0, issued = min(nstage, kStages);
+  for (int b0 = 0; b0 < nstage && !failed; b0 += kStages) {
 #pragma unroll
-    for (int k = 0; k < kVec; ++k) ia[k] = r_first;
-    for (int step = top; step > 0; step >>= 1) {
-#pragma unroll
-      for (int k = 0; k < kVec; ++k)
-        if (ia[k] + step <= r_last && cu_at(ia[k] + step) <= 4 * vec_of(b, k)) ia[k] += step;
-    }
-#pragma unroll
-    for (int k = 0; k < kVec; ++k) {
-      const int v = vec_of(b, k);
-      if (v < v_hi) {
-        n += nonzero_bytes(mk[k]);
-        const float4 d = tokens4(4 * v, lp[k], old[k], lr[k], mk[k], ia[k]);
-        if (b == nbatch - 1) dl[k] = d;
-        else reinterpret_cast<float4*>(p.dlogp)[v] = d;
+    for (int q = 0; q < kStages; ++q) {
+      const int b = b0 + q;
+      if (b >= nstage) break;
+      const bool ok = mbar_wait(smem_u32(&full[q]), (b / kStages) & 1, ab);
+      if (__syncthreads_or(!ok)) {
+        failed = true;
+        break;
+      }
+      const int v0 = v_lo + b * kStageVec, nv = min(kStageVec, v_hi - v0);
+      if (tid < nv) {
+        const int v = v0 + tid;
+        const uint8_t* st = dyn_raw + q * kStageBytes;
+        const float4 x = reinterpret_cast<const float4*>(st)[tid];
+        const float4 xo = reinterpret_cast<const float4*>(st + kStageVec * 16)[tid];
+        const float4 xr =
+            beta != 0.f ? reinterpret_cast<const float4*>(st + kStageVec * 32)[tid] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const uint32_t mw = tid < (nv & ~3) ? reinterpret_cast<const uint32_t*>(st + kStageVec * 48)[tid]
+                                            : __ldg(reinterpret_cast<const uint32_t*>(p.mask) + v);
+        n += nonzero_bytes(mw);
+        dk[q] = tokens4(4 * v, x, xo, xr, mw, lift(4 * v, r_first, r_last, top));
+      }
+      consumed = b + 1;
+      if (b + kStages < nstage) {
+        __syncthreads();  // every thread is done with this stage's buffer
+        if (tid == 0) issue(b + kStages);
+        ++issued;
       }
     }
+    if (!failed && b0 + kStages < nstage) {
+#pragma unroll
+      for (int q = 0; q < kStages; ++q) {
+        const int v = v_lo + (b0 + q) * kStageVec + tid;
+        if (v < v_hi) reinterpret_cast<float4*>(p.dlogp)[v] = dk[q];
+      }
+    }
+  }
+  if (failed) {
+    // Let the copies still in flight land before the CTA leaves (the grid
+    // barrier then runs out of time in the other CTAs too).
+    if (tid == 0)
+      for (int b = consumed; b < issued; ++b) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(smem_u32(&full[b % kStages]), (b / kStages) & 1))
+          if (clock64() - t0 > kTimeoutCycles) break;
+      }
+    return;
   }
   // The last T % 4 tokens: thread 0 of the last CTA (its range ends at nvec).
   const bool tail = tid == 0 && blockIdx.x == gridDim.x - 1;
@@ -415,20 +462,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) grpo_kernel(const GrpoK 
   // fp32 throughout: FP64 issues at a small fraction of the FP32 rate on this part.
   const float inv_n = N > 0 ? __frcp_rn(static_cast<float>(N)) : 0.f;
   auto scale = [&](float4 d) { return make_float4(d.x * inv_n, d.y * inv_n, d.z * inv_n, d.w * inv_n); };
-  for (int b = 0; b < nbatch - 1; ++b) {
+  const int b_keep = nstage > 0 ? ((nstage - 1) / kStages) * kStages : 0;  // first stage held in registers
+  for (int b = 0; b < b_keep; ++b) {
     // Written by this same thread before the barrier.
-    float4 d[kVec];
-#pragma unroll
-    for (int k = 0; k < kVec; ++k)
-      if (vec_of(b, k) < v_hi) d[k] = __ldcg(reinterpret_cast<const float4*>(p.dlogp) + vec_of(b, k));
-#pragma unroll
-    for (int k = 0; k < kVec; ++k)
-      if (vec_of(b, k) < v_hi) reinterpret_cast<float4*>(p.dlogp)[vec_of(b, k)] = scale(d[k]);
+    const int v = v_lo + b * kStageVec + tid;
+    if (v < v_hi) {
+      float4* d = reinterpret_cast<float4*>(p.dlogp) + v;
+      *d = scale(__ldcg(d));
+    }
   }
-  if (nbatch > 0) {
 #pragma unroll
-    for (int k = 0; k < kVec; ++k)
-      if (vec_of(nbatch - 1, k) < v_hi) reinterpret_cast<float4*>(p.dlogp)[vec_of(nbatch - 1, k)] = scale(dl[k]);
+  for (int q = 0; q < kStages; ++q) {
+    const int v = v_lo + (b_keep + q) * kStageVec + tid;
+    if (b_keep + q < nstage && v < v_hi) reinterpret_cast<float4*>(p.dlogp)[v] = scale(dk[q]);
   }
   if (tail)
     for (int t = 4 * nvec; t < p.T; ++t) p.dlogp[t] = __ldcg(p.dlogp + t) * inv_n;
@@ -469,8 +515,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) grpo_kernel(const GrpoK 
   }
 }
 
-// Grid bound: one CTA per 512 vectors (2048 tokens) at most, and at most
-// kCtasPerSm per SM.
+// Grid bound: one CTA per stage of vectors (2048 tokens) at most, and at
+// most kCtasPerSm per SM.
 int max_ctas(int T) {
   static int sms = 0;
   if (sms == 0) {
@@ -480,13 +526,15 @@ int max_ctas(int T) {
       s = 152;
     sms = s;
   }
-  const int by_work = std::max(1, (T / 4 + kTokPerCta / 4 - 1) / (kTokPerCta / 4));
+  const int by_work = std::max(1, (T / 4 + kStageVec - 1) / kStageVec);
   return std::min(by_work, kCtasPerSm * sms);
 }
 
 size_t a256(size_t x) { return (x + 255) / 256 * 256; }
 
-size_t dyn_bytes(int R) { return R <= kStageRollouts ? (2 * static_cast<size_t>(R) + 1) * 4 : 0; }
+size_t dyn_bytes(int R) {
+  return static_cast<size_t>(kStages) * kStageBytes + (R <= kStageRollouts ? (2 * static_cast<size_t>(R) + 1) * 4 : 0);
+}
 
 }  // namespace
 
@@ -499,8 +547,10 @@ cudaError_t launch_grpo(const GrpoArgs& a, cudaStream_t stream) {
   if (a.num_rollouts == 0) return cudaSuccess;
   const size_t dyn = dyn_bytes(a.num_rollouts);
   // Every CTA waits at the grid barrier, so the grid must be co-resident.
+  cudaError_t e = cudaFuncSetAttribute(grpo_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(dyn));
+  if (e != cudaSuccess) return e;
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, grpo_kernel, kThreads, dyn);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, grpo_kernel, kThreads, dyn);
   if (e != cudaSuccess) return e;
   if (per_sm <= 0) return cudaErrorInvalidConfiguration;
   int sms = 0, dev = 0;
