@@ -55,7 +55,7 @@ LAUNCHES_PER_STEP = 4  # forward, backward preprocess, backward main, dQ convert
 DECODE_METRIC = "sink-attn decode GB/s (bf16 KV-cache stream) and % of measured HBM copy bandwidth"
 DECODE_LAUNCHES_PER_STEP = 1  # key-chunk kernel (the last chunk of each sequence merges)
 GRPO_METRIC = "GRPO token loss GB/s (fp32 log-probs) and % of measured HBM copy bandwidth"
-GRPO_LAUNCHES_PER_STEP = 2  # per-rollout counts and advantages, token pass
+GRPO_LAUNCHES_PER_STEP = 1  # one cooperative kernel: advantages, tokens, grid barrier, 1/N scaling
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -807,10 +807,10 @@ def run_gpu_grpo(args, world, rank, local):
                    "clip_eps": wl.clip_eps, "kl_beta": wl.kl_beta,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "flushed before every step (256 MiB write, then 256 MiB read so the written lines drain; outside the step events)",
-                   "timing": "CUDA graph replay of one step (both kernels); e2e = eager calls with host copies",
+                   "timing": "CUDA graph replay of one step (one kernel); e2e = eager calls with host copies",
                    "algorithmic_bytes_per_step": nbytes},
         "pct_of_peak": 100.0 * value / world / peaks["hbm_gbs"],
-        "roofline": {"bound": "hbm", "kernel": "grpo_prep + grpo_loss (whole step)", "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": "grpo_kernel (the whole step: one launch)", "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "peak_source": f"{peak_src} HBM copy", "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": _committed_traffic(args.workload, "grpo"),
                      "algorithmic_bytes": nbytes},

@@ -166,6 +166,13 @@ SA_DEV float2 group_stats(const float* rew, int g0, int G, float eps) {
   return make_float2(mu, sqrtf(var / static_cast<float>(G)) + eps);
 }
 
+// Equation (3) for rollout i straight from the rewards (when the advantages
+// are not staged).
+SA_DEV float advantage_of(const float* rewards, int i, int G, float eps) {
+  const float2 st = group_stats(rewards, (i / G) * G, G, eps);
+  return (__ldg(rewards + i) - st.x) / st.y;
+}
+
 // The same by one warp (lanes stride over the group); valid in every lane.
 SA_DEV float2 group_stats_warp(const float* rew, int g0, int G, float eps) {
   const int lane = threadIdx.x & 31;
@@ -292,11 +299,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) grpo_kernel(const GrpoK 
     }
   }
   auto cu_at = [&](int j) { return staged ? cu_s[j] : __ldg(p.cu + j); };
-  auto adv_at = [&](int i) -> float {
-    if (staged) return adv_s[i];
-    const float2 st = group_stats(p.rewards, (i / G) * G, G, p.adv_eps);
-    return (__ldg(p.rewards + i) - st.x) / st.y;
-  };
+  auto adv_at = [&](int i) -> float { return staged ? adv_s[i] : advantage_of(p.rewards, i, G, p.adv_eps); };
   // Rollout of token t: the last i with cu[i] <= t (skips empty rollouts),
   // by binary lifting from a over steps top, top / 2, ..., 1 within [a, b]
   // (cu[a] <= t).  The rollouts of this CTA's range bound every search.
@@ -353,17 +356,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) grpo_kernel(const GrpoK 
       d.y = token(x.y, xo.y, xr.y, mw & 0xFF00u, absA, s, sb, A0);
       d.z = token(x.z, xo.z, xr.z, mw & 0xFF0000u, absA, s, sb, A0);
       d.w = token(x.w, xo.w, xr.w, mw & 0xFF000000u, absA, s, sb, A0);
-    } else {
-      d.x = token(x.x, xo.x, xr.x, mw & 0xFFu, absA, s, sb, A0);
-      const float A1 = adv_at(lift(t + 1, i0, r_last, top));
-      side(A1, absA, s, sb);
-      d.y = token(x.y, xo.y, xr.y, mw & 0xFF00u, absA, s, sb, A1);
-      const float A2 = adv_at(lift(t + 2, i0, r_last, top));
-      side(A2, absA, s, sb);
-      d.z = token(x.z, xo.z, xr.z, mw & 0xFF0000u, absA, s, sb, A2);
-      const float A3 = adv_at(lift(t + 3, i0, r_last, top));
-      side(A3, absA, s, sb);
-      d.w = token(x.w, xo.w, xr.w, mw & 0xFF000000u, absA, s, sb, A3);
+    } else {  // a rollout ends inside the vector: one token at a time (kept small: rare)
+#pragma unroll 1
+      for (int j = 0; j < 4; ++j) {
+        const float A = adv_at(lift(t + j, i0, r_last, top));
+        side(A, absA, s, sb);
+        const float xj = j == 0 ? x.x : j == 1 ? x.y : j == 2 ? x.z : x.w;
+        const float xoj = j == 0 ? xo.x : j == 1 ? xo.y : j == 2 ? xo.z : xo.w;
+        const float xrj = j == 0 ? xr.x : j == 1 ? xr.y : j == 2 ? xr.z : xr.w;
+        const float g = token(xj, xoj, xrj, (mw >> (8 * j)) & 0xFFu, absA, s, sb, A);
+        if (j == 0) d.x = g; else if (j == 1) d.y = g; else if (j == 2) d.z = g; else d.w = g;
+      }
     }
     return d;
   };
