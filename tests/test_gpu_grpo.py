@@ -58,7 +58,10 @@ CASES = [
     W.GrpoWorkload("small", 3, 4, 1, 300, 1),
     W.GrpoWorkload("single_rollout_groups", 5, 1, 10, 2000, 2),   # G = 1: every advantage is 0
     W.GrpoWorkload("wide_groups", 2, 16, 0, 700, 3),              # zero-length rollouts allowed
-    W.GrpoWorkload("many_short", 100, 6, 1, 40, 4),               # 600 rollouts: more than one offset window per chunk
+    W.GrpoWorkload("many_short", 100, 6, 1, 40, 4),               # 600 rollouts, many crossing a 4-token vector
+    W.GrpoWorkload("warp_groups", 3, 48, 0, 200, 6),              # G > 32: one warp per group
+    W.GrpoWorkload("unstaged_rollouts", 1000, 8, 1, 64, 5),       # 8000 rollouts: offsets and advantages not staged
+    W.GrpoWorkload("long_rollouts", 64, 8, 8192, 16384, 7),       # > 4 stages per CTA: the ring refills
 ]
 
 
@@ -80,3 +83,29 @@ def test_grpo_empty_mask_and_equal_rewards():
 def test_grpo_workload(name):
     wl = W.GRPO_WORKLOADS[name]
     check(W.make_grpo_inputs(wl), clip_eps=wl.clip_eps, adv_eps=wl.adv_eps, kl_beta=wl.kl_beta)
+
+
+def test_grpo_barrier_timeout_reports_and_recovers():
+    """The grid barrier's wait is bounded: with an arrival word that can never
+    complete (its count already past the grid size), every CTA gives up after
+    about a second, the status word reports TIMEOUT, and a later call on a
+    zero-filled workspace is correct again."""
+    import sink_aware_masked_gb300 as sa
+
+    inp = W.make_grpo_inputs(CASES[3])
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)  # noqa: E731
+    cu_host = [int(x) for x in inp.cu_tokens]
+    cu = t(inp.cu_tokens)
+    ws = torch.zeros(sa.grpo_workspace_bytes(cu, cu_host, group_size=inp.wl.group_size), dtype=torch.uint8, device=DEV)
+    assert sa.sinkattn_get_device_status() == 0
+    ws[:8] = torch.tensor([1 << 19], dtype=torch.int64).view(torch.uint8).to(DEV)  # arrivals: 2^19, never grid - 1
+    args = (t(inp.logp), t(inp.logp_old), t(inp.mask), t(inp.rewards), cu, cu_host)
+    sa.grpo_loss(*args, group_size=inp.wl.group_size, workspace=ws)
+    torch.cuda.synchronize()
+    assert sa.sinkattn_get_device_status() == 6  # SINKATTN_ERR_TIMEOUT
+    ws.zero_()
+    stats, dlogp, adv = sa.grpo_loss(*args, group_size=inp.wl.group_size, workspace=ws)
+    assert sa.sinkattn_get_device_status() == 0
+    want = ref.grpo_loss(inp.logp.astype(np.float64), inp.logp_old.astype(np.float64), None, inp.mask,
+                         inp.rewards.astype(np.float64), inp.cu_tokens, inp.wl.group_size)
+    assert abs(float(stats[1]) - want["policy"]) <= 1e-5 * max(1.0, abs(want["policy"])) + 1e-3
