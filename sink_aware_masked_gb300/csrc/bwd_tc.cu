@@ -616,31 +616,37 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
   }
 }
 
-// dK, dV of split key tiles: fp32 accumulator -> bf16 (dK scaled).  One
-// block per work item; only the first chunk of a split tile converts it.
+// dK, dV of split key tiles: fp32 accumulator -> bf16 (dK scaled).  A flat
+// grid-stride pass over every 8-element group of the split tiles' rows, so
+// that many loads are in flight (the work is a few MB spread over a few
+// tiles: one block per tile would leave most SMs idle).
 struct DkvConvK {
   const float* acc;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   const int32_t* cu;
-  int seqlen, hkv;
+  int seqlen, hkv, n_tiles;
   float scale;
-  BwdItem items[2048];
+  uint32_t tiles[2048];  // split key tiles: sequence | key tile << 16
 };
 
 __global__ void __launch_bounds__(256) dkv_convert_kernel(const __grid_constant__ DkvConvK p) {
-  const BwdItem item = p.items[blockIdx.x];
-  if (item.nchunks <= 1 || item.chunk != 0) return;
-  const SeqSpan sp = seq_span(p.cu, p.seqlen, item.b);
-  const int k0 = item.kt * BN, rows = min(BN, sp.len - k0);
   const int per_row = p.hkv * 2 * (D / 8);  // 8-element groups per key row
-  for (int i = threadIdx.x; i < rows * per_row; i += blockDim.x) {
-    const int r = i / per_row, rem = i - r * per_row;
+  const long long per_tile = static_cast<long long>(BN) * per_row;
+  const long long total = per_tile * p.n_tiles;
+  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < total; i += static_cast<long long>(gridDim.x) * 256) {
+    const int s = static_cast<int>(i / per_tile);
+    const int rem0 = static_cast<int>(i - s * per_tile);
+    const int r = rem0 / per_row, rem = rem0 - r * per_row;
+    const uint32_t code = p.tiles[s];
+    const SeqSpan sp = seq_span(p.cu, p.seqlen, static_cast<int>(code & 0xFFFFu));
+    const int k0 = static_cast<int>(code >> 16) * BN;
+    if (k0 + r >= sp.len) continue;
     const int g = rem / (2 * (D / 8)), which = (rem / (D / 8)) & 1, c8 = rem % (D / 8);
     const size_t row = static_cast<size_t>(sp.start + k0 + r);
     const float* src = p.acc + ((row * p.hkv + g) * 2 + which) * D + 8 * c8;
     const float mul = which ? p.scale : 1.f;
-    const float4 x = reinterpret_cast<const float4*>(src)[0], y = reinterpret_cast<const float4*>(src)[1];
+    const float4 x = __ldcs(reinterpret_cast<const float4*>(src)), y = __ldcs(reinterpret_cast<const float4*>(src) + 1);
     uint4 o;
     o.x = pack_bf16(x.x * mul, x.y * mul);
     o.y = pack_bf16(x.z * mul, x.w * mul);
@@ -711,10 +717,17 @@ cudaError_t launch_bwd_tc_main(const Problem& pr, const BwdArgs& a, int* status,
     c.seqlen = pr.seqlen;
     c.hkv = pr.hkv;
     c.scale = pr.scale;
-    for (size_t first = 0; first < items.size(); first += kMax) {
-      const int n = static_cast<int>(std::min<size_t>(kMax, items.size() - first));
-      std::copy(items.begin() + first, items.begin() + first + n, c.items);
-      dkv_convert_kernel<<<n, 256, 0, stream>>>(c);
+    std::vector<uint32_t> tiles;  // each split tile once (its chunk 0)
+    for (const BwdItem& it : items)
+      if (it.nchunks > 1 && it.chunk == 0) tiles.push_back(static_cast<uint32_t>(it.b) | (static_cast<uint32_t>(it.kt) << 16));
+    constexpr int kMaxTiles = static_cast<int>(sizeof(c.tiles) / sizeof(c.tiles[0]));
+    for (size_t first = 0; first < tiles.size(); first += kMaxTiles) {
+      const int n = static_cast<int>(std::min<size_t>(kMaxTiles, tiles.size() - first));
+      std::copy(tiles.begin() + first, tiles.begin() + first + n, c.tiles);
+      c.n_tiles = n;
+      const long long groups = static_cast<long long>(n) * BN * pr.hkv * 2 * (D / 8);
+      const int blocks = static_cast<int>(std::min<long long>((groups + 255) / 256, 152LL * 8));
+      dkv_convert_kernel<<<blocks, 256, 0, stream>>>(c);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
   }
