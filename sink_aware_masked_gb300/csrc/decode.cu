@@ -12,7 +12,8 @@
 // V bounded by HBM bandwidth (the 8 query heads of a GQA group share every
 // key: about 8 FLOP per byte at n = 1).  The key range of each (sequence, kv
 // head) is split into chunks of whole 128-key tiles (split-KV); one CTA per
-// (chunk, kv head) streams its tiles by TMA through a 3-stage mbarrier ring
+// (chunk, kv head) streams its tiles by TMA through a 2-stage mbarrier ring
+// (three such CTAs resident per SM)
 // and computes, for the group x n query rows, a partial online softmax
 // (running max m in log2 units, row sum l, unnormalised O) with warp-level
 // bf16 MMAs.  The last CTA of a (sequence, kv head) to finish (a counter in
@@ -44,7 +45,7 @@ using namespace tc;
 
 constexpr int D = kHeadDim;
 constexpr int BN = 128;           // keys per tile
-constexpr int NS = 3;             // K/V stages
+constexpr int NS = 2;             // K/V stages (three CTAs per SM fit: 65 KB of shared memory each)
 constexpr int NTHR = 128;
 constexpr int TILE = BN * D * 2;  // 16 KB
 constexpr int SMEM_DYN = NS * 2 * TILE + 1024;
@@ -99,7 +100,7 @@ SA_DEV float quad_sum(float x) {
 
 // MB: 16-row blocks covering the R rows (1, 2, 4 or 8).
 template <int MB>
-__global__ void __launch_bounds__(NTHR) decode_split_kernel(const __grid_constant__ DecK p) {
+__global__ void __launch_bounds__(NTHR, 3) decode_split_kernel(const __grid_constant__ DecK p) {
   constexpr int MBW = MB < 2 ? MB : 2;  // row blocks per warp
   constexpr int WR = MB / MBW;          // warps splitting the rows
   constexpr int WK = 4 / WR;            // warps splitting the keys of a tile
@@ -462,13 +463,19 @@ DecodePlan decode_plan(const Problem& p, int n) {
     tiles[b] = n_pre + (hi / BN - lo_t + 1);
     total += tiles[b];
   }
-  // About three (chunk, kv head) CTAs per SM: each CTA pays a pipeline fill
-  // and a partial write, and the key stream shares HBM bandwidth, so fewer,
-  // longer chunks win until the grid covers the SMs about 1.5 times (1 to 6
-  // CTAs per SM measured on 32 x 8192, 8 x 32768 x 4 rows and the packed
-  // trajectories; 3 was best on all three).  At least two tiles per chunk,
-  // and no more items than the parameter block holds.
-  const long long want = std::max<long long>(1, 3LL * std::max(sms, 1) / std::max(p.hkv, 1));
+  // Chunks per kv head: `factor` x the SMs / kv heads.  Each CTA pays a
+  // pipeline fill and a partial write, and the key stream shares HBM
+  // bandwidth, so fewer, longer chunks win until the grid keeps the three
+  // resident CTAs per SM busy; the chunks of a sequence are equal, so the CTA
+  // count rounds per sequence.  Measured (2 to 6 x the SMs, two-stage ring,
+  // three CTAs per SM): a single 16-row block per kv head (one query row per
+  // sequence for GQA 8) with at least 1024 key tiles per kv head, e.g.
+  // 32 x 8192, wins at 4; fewer tiles (packed trajectories, windows) and
+  // wider row blocks (8 x 32768 x 4 rows) win at 2.  At least two tiles per
+  // chunk, and no more items than the parameter block holds.
+  const int rows = (p.hq / std::max(p.hkv, 1)) * n;
+  const int factor = (rows <= 16 && total >= 1024) ? 4 : 2;
+  const long long want = std::max<long long>(1, static_cast<long long>(factor) * std::max(sms, 1) / std::max(p.hkv, 1));
   int tps = static_cast<int>(std::max<long long>(2, (total + want - 1) / want));
   for (;;) {
     long long items = 0;
