@@ -65,7 +65,7 @@ struct GrpoK {
   unsigned long long* sync;
   float4* part;     // workspace [grid]: sum J, sum k3, clipped count per CTA
   int* status;      // library status word
-  int R, G, T;
+  int R, G, T, ngroups;
   float clip_eps, adv_eps, beta;
 };
 
@@ -192,6 +192,7 @@ SA_DEV float2 group_stats_warp(const float* rew, int g0, int G, float eps) {
 
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) grpo_kernel(const GrpoK p) {
   __shared__ uint64_t full[kStages];
+  __shared__ int range_s[2];  // this CTA's vectors [v_lo, v_hi)
   __shared__ int abort_flag;
   __shared__ int red_i[kThreads / 32];
   __shared__ float3 red_f3[kThreads / 32];
@@ -207,13 +208,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) grpo_kernel(const GrpoK 
   float* adv_s = reinterpret_cast<float*>(cu_s + p.R + 1);
   const float beta = p.beta;
   const int nvec = p.T / 4;
-  const int G = p.G, ngroups = p.R / p.G;
+  const int G = p.G, ngroups = p.ngroups;
   // This CTA's vectors [v_lo, v_hi): an equal share in units of 32 vectors
   // (128 tokens), in stages of kStageVec vectors.
-  const int n32 = (nvec + 31) / 32;
-  const int v_lo = static_cast<int>(static_cast<long long>(blockIdx.x) * n32 / gridDim.x) * 32;
-  const int v_hi = min(nvec, static_cast<int>(static_cast<long long>(blockIdx.x + 1) * n32 / gridDim.x) * 32);
-  const int nstage = (v_hi - v_lo + kStageVec - 1) / kStageVec;
+  // (Thread 0 does the 64-bit divisions; the others read the bounds after
+  // the first barrier.)
+  int v_lo = 0, v_hi = 0;
+  if (tid == 0) {
+    const long long n32 = (nvec + 31) / 32;
+    v_lo = static_cast<int>(static_cast<long long>(blockIdx.x) * n32 / gridDim.x) * 32;
+    v_hi = min(nvec, static_cast<int>(static_cast<long long>(blockIdx.x + 1) * n32 / gridDim.x) * 32);
+    range_s[0] = v_lo;
+    range_s[1] = v_hi;
+  }
+  int nstage = (v_hi - v_lo + kStageVec - 1) / kStageVec;
   const uint32_t sbase = smem_u32(dyn_raw);
   if (tid == 0) {
     abort_flag = 0;
@@ -253,7 +261,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) grpo_kernel(const GrpoK 
       if (j < p.R) rw_r[q] = __ldg(p.rewards + j);
     }
   }
-  __syncthreads();  // the barriers are initialised
+  __syncthreads();  // the barriers are initialised, the range is published
+  v_lo = range_s[0];
+  v_hi = range_s[1];
+  nstage = (v_hi - v_lo + kStageVec - 1) / kStageVec;
   if (tid == 0)
     for (int b = 0; b < min(nstage, kStages); ++b) issue(b);
   if (staged) {
@@ -577,6 +588,7 @@ cudaError_t launch_grpo(const GrpoArgs& a, cudaStream_t stream) {
   k.status = a.status;
   k.R = a.num_rollouts;
   k.G = a.group_size;
+  k.ngroups = a.num_rollouts / a.group_size;
   k.T = a.total_tokens;
   k.clip_eps = a.clip_eps;
   k.adv_eps = a.adv_eps;
