@@ -201,3 +201,53 @@ def test_grpo_alignment(lib):
                                   None) == 3
     assert lib.sinkattn_grpo_loss(ctypes.byref(g), FAKE, FAKE, None, FAKE + 1, FAKE, FAKE, FAKE, None, FAKE, ws,
                                   None) == 3
+
+
+def _decode_plan_items(lens, hq, hkv, n, window=-1, prefix=0, sms=152):
+    """The decode planner's chunk count, restated: 128-key tiles per sequence
+    (prefix tiles, then the band of the last n rows), a chunk factor of 4 x the
+    SMs per kv head for a single 16-row block with >= 1024 tiles, else 2, at
+    least two tiles per chunk."""
+    tiles = []
+    for L in lens:
+        q0, hi = L - n, L - 1
+        lo = 0 if window < 0 else max(0, q0 - window)
+        pre_end = max(0, min(min(prefix, lo), hi + 1))
+        lo_t = lo // 128
+        n_pre = min((pre_end + 127) // 128, lo_t)
+        tiles.append(n_pre + (hi // 128 - lo_t + 1))
+    total = sum(tiles)
+    rows = (hq // hkv) * n
+    factor = 4 if rows <= 16 and total >= 1024 else 2
+    want = max(1, factor * sms // hkv)
+    tps = max(2, -(-total // want))
+    while sum(-(-t // tps) for t in tiles) > 4096:
+        tps *= 2
+    return sum(-(-t // tps) for t in tiles)
+
+
+@pytest.mark.parametrize("lens,n,window,prefix", [
+    ([8192] * 32, 1, -1, 0),                                       # 32 x 8192: factor 4
+    ([32768] * 8, 4, -1, 0),                                       # 32 rows per kv head: factor 2
+    ([6111, 5036, 1589, 6459, 1056, 6459, 3018, 2085], 1, -1, 0),  # packed: < 1024 tiles per kv head
+    ([8192] * 32, 1, 128, 4),                                      # window and prefix
+])
+def test_decode_plan_chunk_count(lib, lens, n, window, prefix):
+    """The workspace size encodes the plan: counters, one partial (O and
+    (max, sum)) per chunk, kv head and row, each region 256-byte aligned."""
+    from sink_aware_masked_gb300 import _lib
+
+    hq, hkv = 64, 8
+    cu = [0]
+    for L in lens:
+        cu.append(cu[-1] + L)
+    arr = (ctypes.c_int32 * len(cu))(*cu)
+    pr = _lib.Problem(num_seqs=len(lens), seqlen=max(lens), cu_seqlens=FAKE,
+                      cu_seqlens_host=ctypes.cast(arr, ctypes.c_void_p).value, total_tokens=cu[-1],
+                      num_heads_q=hq, num_heads_kv=hkv, head_dim=64, window=window, prefix=prefix, causal=1,
+                      scale=0.125)
+    items = _decode_plan_items(lens, hq, hkv, n, window, prefix)
+    R = (hq // hkv) * n
+    r256 = lambda x: -(-x // 256) * 256  # noqa: E731
+    want = r256(len(lens) * hkv * 4) + r256(items * hkv * R * 64 * 4) + r256(items * hkv * ((R + 1) & ~1) * 8) + 256
+    assert lib.sinkattn_decode_workspace_size(ctypes.byref(pr), n) == want
