@@ -50,6 +50,12 @@ constexpr int NTHR = 128;
 constexpr int TILE = BN * D * 2;  // 16 KB
 constexpr int SMEM_DYN = NS * 2 * TILE + 1024;
 
+// The work list's capacity is a template parameter: a short list keeps the
+// kernel parameter block small (a 16 KB block costs ~1.3 us more per launch
+// than a small one, a few per cent of a short decode step).
+constexpr int kDecodeSmallItems = 256;
+
+template <int CAP>
 struct DecK {
   CUtensorMap tm_k, tm_v;
   const __nv_bfloat16* q;  // [B * n, Hq, 64]
@@ -69,9 +75,9 @@ struct DecK {
   int num_seqs;
   int tiles_per_split;  // chunks of a sequence: ceil(tiles / tiles_per_split), equal shares
   int n_items;
-  uint32_t items[kDecodeMaxItems];  // sequence | (chunk << 16), chunks of a sequence consecutive
+  uint32_t items[CAP];  // sequence | (chunk << 16), chunks of a sequence consecutive
 };
-static_assert(sizeof(DecK) < 32000, "kernel parameter block too large");
+static_assert(sizeof(DecK<kDecodeMaxItems>) < 32000, "kernel parameter block too large");
 
 // Key tiles that the query rows [L - n, L - 1] see: the prefix tiles below the
 // window, then the window/causal band (same arithmetic as the full forward).
@@ -99,8 +105,8 @@ SA_DEV float quad_sum(float x) {
 }
 
 // MB: 16-row blocks covering the R rows (1, 2, 4 or 8).
-template <int MB>
-__global__ void __launch_bounds__(NTHR, 3) decode_split_kernel(const __grid_constant__ DecK p) {
+template <int MB, int CAP>
+__global__ void __launch_bounds__(NTHR, 3) decode_split_kernel(const __grid_constant__ DecK<CAP> p) {
   constexpr int MBW = MB < 2 ? MB : 2;  // row blocks per warp
   constexpr int WR = MB / MBW;          // warps splitting the rows
   constexpr int WK = 4 / WR;            // warps splitting the keys of a tile
@@ -500,10 +506,12 @@ DecodePlan decode_plan(const Problem& p, int n) {
   return pl;
 }
 
-cudaError_t launch_decode(const Problem& pr, int n, const DecodeArgs& a, const DecodePlan& pl, int* status,
-                          cudaStream_t stream) {
-  if (pr.num_seqs == 0) return cudaSuccess;
-  thread_local DecK k;
+namespace {
+
+template <int CAP>
+cudaError_t launch_decode_cap(const Problem& pr, int n, const DecodeArgs& a, const DecodePlan& pl, int* status,
+                              cudaStream_t stream) {
+  thread_local DecK<CAP> k;
   if (!make_rows_map(&k.tm_k, a.k, pr.total_tokens, pr.hkv, BN) ||
       !make_rows_map(&k.tm_v, a.v, pr.total_tokens, pr.hkv, BN))
     return cudaErrorInvalidValue;
@@ -537,10 +545,10 @@ cudaError_t launch_decode(const Problem& pr, int n, const DecodeArgs& a, const D
   switch (mb) {
 #define SA_DECODE_CASE(MBV)                                                                                    \
   case MBV:                                                                                                    \
-    if ((e = cudaFuncSetAttribute(decode_split_kernel<MBV>, cudaFuncAttributeMaxDynamicSharedMemorySize,      \
+    if ((e = cudaFuncSetAttribute(decode_split_kernel<MBV, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                                   SMEM_DYN)) != cudaSuccess)                                                   \
       return e;                                                                                                \
-    decode_split_kernel<MBV><<<grid, NTHR, SMEM_DYN, stream>>>(k);                                             \
+    decode_split_kernel<MBV, CAP><<<grid, NTHR, SMEM_DYN, stream>>>(k);                                        \
     break;
     SA_DECODE_CASE(1)
     SA_DECODE_CASE(2)
@@ -550,6 +558,17 @@ cudaError_t launch_decode(const Problem& pr, int n, const DecodeArgs& a, const D
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return prof_end(g_prof_dec, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const Problem& pr, int n, const DecodeArgs& a, const DecodePlan& pl, int* status,
+                          cudaStream_t stream) {
+  if (pr.num_seqs == 0) return cudaSuccess;
+  if (pl.items.size() > static_cast<size_t>(kDecodeMaxItems)) return cudaErrorInvalidValue;
+  return pl.items.size() <= static_cast<size_t>(kDecodeSmallItems)
+             ? launch_decode_cap<kDecodeSmallItems>(pr, n, a, pl, status, stream)
+             : launch_decode_cap<kDecodeMaxItems>(pr, n, a, pl, status, stream);
 }
 
 }  // namespace sa
