@@ -51,7 +51,8 @@ DEFAULT_WORKLOAD = "causal_gqa_b2_s8192"
 FLOP_FWD_PER_PAIR = 4 * 64
 FLOP_BWD_PER_PAIR = 10 * 64
 L2_FLUSH_BYTES = 256 << 20
-LAUNCHES_PER_STEP = 4  # forward, backward preprocess, backward main, dQ convert
+# Attention: the library counts its launches per step (sinkattn_kernel_launches): forward, backward
+# preprocess, backward main, dK/dV conversion of split key tiles (when any), dQ convert.
 DECODE_METRIC = "sink-attn decode GB/s (bf16 KV-cache stream) and % of measured HBM copy bandwidth"
 DECODE_LAUNCHES_PER_STEP = 1  # key-chunk kernel (the last chunk of each sequence merges)
 GRPO_METRIC = "GRPO token loss GB/s (fp32 log-probs) and % of measured HBM copy bandwidth"
@@ -462,6 +463,8 @@ def run_gpu(args, world, rank, local):
     dsink = torch.empty_like(sink)
     ws = torch.empty(max(16, sa.bwd_workspace_bytes(q, k, **prob)), dtype=torch.uint8, device=dev)
     flush = L2Flush(dev)
+    # Our kernels per step, counted by the library from its own work lists.
+    launches_per_step = sa.kernel_launches(q, k, "fwd", **prob) + sa.kernel_launches(q, k, "bwd", **prob)
 
     def step():
         sa.sinkattn_fwd(q, k, v, sink, o=o, lse=lse, **prob)
@@ -601,7 +604,7 @@ def run_gpu(args, world, rank, local):
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": Ke, "mode": "pinned host buffers, double-buffered: step i+1's inputs up and step i-1's "
                                      "outputs down on two copy streams while step i computes; one timed region"},
-        "gpu_launches": K * LAUNCHES_PER_STEP,
+        "gpu_launches": K * launches_per_step,
         "clocks": clock_info,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -85,6 +85,13 @@ typedef struct {
 size_t sinkattn_fwd_workspace_size(const sinkattn_problem* prob);
 size_t sinkattn_bwd_workspace_size(const sinkattn_problem* prob);
 
+/* Number of kernel launches sinkattn_fwd (which = 1) or sinkattn_bwd /
+ * sinkattn_bwd_noalloc (which = 2) make for this problem, from host
+ * arithmetic alone (the same work lists the calls build); -1 for an invalid
+ * problem or `which`.  Lets a caller count the library's launches without a
+ * profiler. */
+int32_t sinkattn_kernel_launches(const sinkattn_problem* prob, int32_t which);
+
 /* Forward.  Reads q, k, v (bf16) and sink (fp32 [Hq]); writes
  * o = alpha * softmax_M(s) V (bf16 [T, Hq, 64]) and lse = l (fp32 [Hq, T]).
  * Rows of a sequence are never mixed with rows of another sequence. */

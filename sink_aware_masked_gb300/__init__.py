@@ -12,6 +12,7 @@ from .api import (  # noqa: F401
     decode_workspace_bytes,
     grpo_loss,
     grpo_workspace_bytes,
+    kernel_launches,
     make_problem,
     sink_attention,
     sinkattn_bwd,

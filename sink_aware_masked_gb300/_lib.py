@@ -56,6 +56,7 @@ _GP = ctypes.POINTER(GrpoProblem)
 SIGNATURES = {
     "sinkattn_fwd_workspace_size": (_sz, [_PP]),
     "sinkattn_bwd_workspace_size": (_sz, [_PP]),
+    "sinkattn_kernel_launches": (_i32, [_PP, _i32]),
     "sinkattn_fwd": (ctypes.c_int, [_PP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "sinkattn_bwd": (ctypes.c_int, [_PP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "sinkattn_bwd_noalloc": (ctypes.c_int, [_PP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),

@@ -83,6 +83,16 @@ def sinkattn_fwd(q, k, v, sink, *, o=None, lse=None, workspace=None, **problem):
     return o, lse
 
 
+def kernel_launches(q, k, which: str, **problem) -> int:
+    """Kernel launches sinkattn_fwd (which="fwd") or sinkattn_bwd ("bwd") makes for this problem."""
+    lib = _lib.load()
+    pr, keep = make_problem(q, k, **problem)
+    n = int(lib.sinkattn_kernel_launches(ctypes.byref(pr), {"fwd": 1, "bwd": 2}[which]))
+    if n < 0:
+        raise ValueError("kernel_launches: invalid problem")
+    return n
+
+
 def bwd_workspace_bytes(q, k, **problem) -> int:
     lib = _lib.load()
     pr, keep = make_problem(q, k, **problem)

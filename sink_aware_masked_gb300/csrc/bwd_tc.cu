@@ -664,6 +664,16 @@ size_t bwd_split_acc_bytes(const Problem& pr) {
   return static_cast<size_t>(pr.total_tokens) * pr.hkv * 2 * D * sizeof(float);
 }
 
+int bwd_tc_main_launches(const Problem& pr) {
+  if (pr.num_seqs == 0 || pr.total_tokens == 0 || pr.seqlen == 0) return 0;
+  const std::vector<BwdItem> items = bwd_work_list(pr, bwd_qchunk(pr));
+  constexpr size_t kMax = sizeof(BwdTcK::items) / sizeof(BwdTcK::items[0]);
+  constexpr size_t kMaxTiles = sizeof(DkvConvK::tiles) / sizeof(DkvConvK::tiles[0]);
+  size_t split_tiles = 0;
+  for (const BwdItem& it : items) split_tiles += (it.nchunks > 1 && it.chunk == 0) ? 1 : 0;
+  return static_cast<int>((items.size() + kMax - 1) / kMax + (split_tiles + kMaxTiles - 1) / kMaxTiles);
+}
+
 cudaError_t launch_bwd_tc_main(const Problem& pr, const BwdArgs& a, int* status, cudaStream_t stream) {
   if (pr.num_seqs == 0 || pr.total_tokens == 0 || pr.seqlen == 0) return cudaSuccess;
   thread_local BwdTcK k;  // 17 KB parameter block; host-side staging, one per host thread

@@ -490,6 +490,12 @@ int num_sms() {
 
 }  // namespace
 
+int fwd_tc_launches(const Problem& pr) {
+  if (pr.total_tokens == 0 || pr.num_seqs == 0 || pr.seqlen == 0) return 0;
+  constexpr size_t kMax = sizeof(FwdTcK::items) / sizeof(FwdTcK::items[0]);
+  return static_cast<int>((fwd_work_list(pr).size() + kMax - 1) / kMax);
+}
+
 cudaError_t launch_fwd_tc(const Problem& pr, const FwdArgs& a, int* status, cudaStream_t stream) {
   if (pr.total_tokens == 0 || pr.num_seqs == 0 || pr.seqlen == 0) return cudaSuccess;
   thread_local FwdTcK k;  // 17 KB parameter block; host-side staging, one per host thread
