@@ -251,3 +251,38 @@ def test_decode_plan_chunk_count(lib, lens, n, window, prefix):
     r256 = lambda x: -(-x // 256) * 256  # noqa: E731
     want = r256(len(lens) * hkv * 4) + r256(items * hkv * R * 64 * 4) + r256(items * hkv * ((R + 1) & ~1) * 8) + 256
     assert lib.sinkattn_decode_workspace_size(ctypes.byref(pr), n) == want
+
+
+@pytest.mark.parametrize("total", [9, 2048 * 4, 2048 * 4 + 3, 2_434_425])
+def test_grpo_workspace_layout(lib, total):
+    """Two 128-byte lines of barrier words, then one (sum J, sum k3,
+    clipped) partial per CTA, 256-byte aligned; the grid is at most one CTA
+    per 512-vector stage and two CTAs per SM (152 SMs without a device)."""
+    host = (ctypes.c_int32 * 3)(0, total // 2, total)
+    g, _ = grpo_problem(cu_tokens_host=ctypes.cast(host, ctypes.c_void_p).value, total_tokens=total)
+    ctas = min(max(1, -(-(total // 4) // 512)), 2 * 152)
+    assert lib.sinkattn_grpo_workspace_size(ctypes.byref(g)) == 256 + -(-(ctas * 16) // 256) * 256
+
+
+@pytest.mark.parametrize("name,fwd,bwd", [
+    ("causal_gqa_b2_s8192", 1, 3),              # preprocess, main, dQ convert
+    ("causal_gqa_s4096", 1, 4),                 # + the dK/dV conversion of split key tiles
+    ("window128_prefix4_gqa_b2_s8192", 1, 4),   # the always-visible prefix tiles are split
+    ("window128_gqa_s4096", 1, 3),
+])
+def test_kernel_launch_counts(lib, name, fwd, bwd):
+    """The launches the library reports for the benchmark's workloads (its
+    own work lists, host arithmetic only)."""
+    import workloads as W
+    from sink_aware_masked_gb300 import _lib
+
+    wl = W.WORKLOADS[name]
+    cu = wl.cu_seqlens()
+    arr = (ctypes.c_int32 * len(cu))(*[int(x) for x in cu])
+    pr = _lib.Problem(num_seqs=wl.num_seqs, seqlen=wl.max_seqlen, cu_seqlens=FAKE,
+                      cu_seqlens_host=ctypes.cast(arr, ctypes.c_void_p).value, total_tokens=wl.total_tokens,
+                      num_heads_q=wl.num_heads_q, num_heads_kv=wl.num_heads_kv, head_dim=64,
+                      window=wl.window, prefix=wl.prefix, causal=int(wl.causal), scale=wl.scale)
+    assert lib.sinkattn_kernel_launches(ctypes.byref(pr), 1) == fwd
+    assert lib.sinkattn_kernel_launches(ctypes.byref(pr), 2) == bwd
+    assert lib.sinkattn_kernel_launches(ctypes.byref(pr), 3) == -1
