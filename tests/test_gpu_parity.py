@@ -83,6 +83,9 @@ SMALL = [
     W.custom((1000,), 4, 2, window=10, prefix=150, seed=24, name="s1000_w10_p150_split"),
     W.custom((700, 1300, 5), 4, 1, window=64, prefix=40, seed=25, name="varlen_w64_p40_split"),
     W.custom((900,), 4, 2, window=20, prefix=3, causal=False, seed=26, name="s900_noncausal_w20_p3_split"),
+    # an odd GQA group larger than one (the forward pairs heads only for even groups)
+    W.custom((333, 70), 6, 2, window=50, prefix=7, seed=27, name="varlen_group3_w50_p7"),
+    W.custom((1100,), 6, 2, window=12, prefix=140, seed=28, name="s1100_group3_w12_p140_split"),
 ]
 
 
