@@ -58,6 +58,10 @@ DECODE_LAUNCHES_PER_STEP = 1  # key-chunk kernel (the last chunk of each sequenc
 GRPO_METRIC = "GRPO token loss GB/s (fp32 log-probs) and % of measured HBM copy bandwidth"
 GRPO_LAUNCHES_PER_STEP = 1  # one cooperative kernel: advantages, tokens, grid barrier, 1/N scaling
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_NAMES = {"fwd": "fwd_tc_kernel", "bwd_main": "bwd_tc_kernel"}
+# Attention workloads the default run also measures (one entry each under "configs").
+EXTRA_CONFIGS = ("causal_gqa_s4096", "window128_gqa_s4096", "window128_prefix4_gqa_b2_s8192", "varlen8_window128",
+                 "varlen8_causal")
 
 
 # ----------------------------------------------------------------- accounting
@@ -139,14 +143,15 @@ def load_peaks():
 
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi sampling (every 50 ms) while the timed region runs."""
+    """nvidia-smi sampling (every ``interval_ms``) while the timed region runs."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, interval_ms: int = 50):
         self.gpu = gpu_index
+        self.interval_ms = int(interval_ms)
         self.proc = None
         self.path = None
 
@@ -157,9 +162,18 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "50"], stdout=self.fh, stderr=subprocess.DEVNULL)
+                 "-lms", str(self.interval_ms)], stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        # nvidia-smi takes a moment to start: wait (up to 3 s) for its first
+        # sample so that the timed region that follows is sampled from its start.
+        t0 = time.monotonic()
+        while time.monotonic() - t0 < 3.0 and self.proc.poll() is None:
+            self.fh.flush()
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.01)
 
     def stop(self):
         if self.proc is None:
@@ -189,7 +203,8 @@ class ClockSampler:
                         reasons.add(name)
         os.unlink(self.path)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": max(power) if power else None}
+                "reasons": sorted(reasons), "samples": len(sm), "interval_ms": self.interval_ms,
+                "power_w_max": max(power) if power else None}
 
 
 # ----------------------------------------------------------------- oracle (CPU)
@@ -225,7 +240,8 @@ def oracle_sample_jobs(wl, n_heads):
 
 
 class OraclePool:
-    """A spawn pool of single-threaded oracle workers (one per host core, up to 16)."""
+    """A spawn pool of single-threaded oracle workers (one per host core, up to
+    16; the line reports the host's core count beside the worker count)."""
 
     def __init__(self):
         import multiprocessing as mp
@@ -255,6 +271,7 @@ def cpu_baseline(wl, pool=None):
         if own:
             pool.close()
     return {"value": rounds * flops / sec / 1e12, "unit": "TFLOP/s", "cores": pool.cores, "kind": "oracle",
+            "host_cpu_count": os.cpu_count(),
             "sample": f"{rounds} rounds of {len(jobs)} query heads x 1 sequence of {wl.seqlens[0]} tokens of "
                       f"{wl.name}, fwd+bwd, one single-threaded worker per head, {sec:.2f} s wall"}
 
@@ -296,6 +313,7 @@ def decode_cpu_baseline(wl, n, steps=3):
     finally:
         pool.close()
     return {"value": steps * nbytes / sec / 1e9, "unit": "GB/s", "cores": pool.cores, "kind": "oracle",
+            "host_cpu_count": os.cpu_count(),
             "sample": f"{steps} rounds of {nseq} sequences of {wl.name} (all heads, {n} query rows each), "
                       f"one single-threaded worker per sequence, {sec:.2f} s wall"}
 
@@ -432,6 +450,133 @@ def barrier(world):
         dist.barrier()
 
 
+def attention_setup(wl, dev):
+    """Device inputs, outputs and workspace of one attention workload."""
+    import torch
+
+    import sink_aware_masked_gb300 as sa
+
+    inp = W.make_inputs(wl)
+    q, k, v, do = (t.to(dev) for t in (inp.q_bf16, inp.k_bf16, inp.v_bf16, inp.do_bf16))
+    sink = inp.sink.to(dev)
+    if wl.uniform:
+        prob = dict(num_seqs=wl.num_seqs)
+    else:
+        cu = wl.cu_seqlens()
+        prob = dict(cu_seqlens=torch.tensor(cu, dtype=torch.int32, device=dev),
+                    cu_seqlens_host=[int(x) for x in cu], max_seqlen=wl.max_seqlen)
+    prob.update(window=wl.window, prefix=wl.prefix, causal=wl.causal, scale=wl.scale)
+    st = dict(q=q, k=k, v=v, do=do, sink=sink, prob=prob, o=torch.empty_like(q),
+              lse=torch.empty((wl.num_heads_q, wl.total_tokens), dtype=torch.float32, device=dev),
+              dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v), dsink=torch.empty_like(sink))
+    st["ws"] = torch.empty(max(16, sa.bwd_workspace_bytes(q, k, **prob)), dtype=torch.uint8, device=dev)
+    # Our kernels per step, counted by the library from its own work lists.
+    st["launches_per_step"] = (sa.kernel_launches(q, k, "fwd", **prob) + sa.kernel_launches(q, k, "bwd", **prob))
+    return st
+
+
+def attention_step(st):
+    import sink_aware_masked_gb300 as sa
+
+    sa.sinkattn_fwd(st["q"], st["k"], st["v"], st["sink"], o=st["o"], lse=st["lse"], **st["prob"])
+    sa.sinkattn_bwd(st["q"], st["k"], st["v"], st["o"], st["lse"], st["do"], st["sink"], dq=st["dq"], dk=st["dk"],
+                    dv=st["dv"], dsink=st["dsink"], workspace=st["ws"], **st["prob"])
+
+
+def time_attention(st, K, warmup, dev, flush, world, sample_ms=50):
+    """K timed steps (L2 flushed before each, outside its events); per step the
+    whole-step, forward-kernel and backward-main-kernel CUDA-event times, and
+    the clocks sampled while the steps ran."""
+    import torch
+
+    import sink_aware_masked_gb300 as sa
+
+    for _ in range(max(warmup, 0)):
+        flush(1.0)
+        attention_step(st)
+    torch.cuda.synchronize()
+    if sa.sinkattn_get_device_status() != 0:
+        raise RuntimeError("device status reported a timed-out wait during warm-up")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for e in ev:  # torch creates the CUDA event on first record(); the hook needs the handle
+        for x in e:
+            x.record()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index if dev.index is not None else 0, sample_ms)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    for i in range(K):
+        flush(float(i))
+        e = ev[i]
+        sa.sinkattn_set_profile_events(sa.PROFILE_FWD, e[2], e[3])
+        sa.sinkattn_set_profile_events(sa.PROFILE_BWD_MAIN, e[4], e[5])
+        e[0].record()
+        attention_step(st)
+        e[1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clock_info = clocks.stop()
+    sa.sinkattn_set_profile_events(sa.PROFILE_FWD)
+    sa.sinkattn_set_profile_events(sa.PROFILE_BWD_MAIN)
+    if sa.sinkattn_get_device_status() != 0:
+        raise RuntimeError("device status reported a timed-out wait")
+    return ([e[0].elapsed_time(e[1]) for e in ev], [e[2].elapsed_time(e[3]) for e in ev],
+            [e[4].elapsed_time(e[5]) for e in ev], clock_info)
+
+
+def roofline_of(wl, fwd_ms, bwd_main_ms, peaks, peak_src, workload_name):
+    """Roofline of the dominant kernel (the larger mean CUDA-event time): its
+    algorithmic FLOP per byte against the ridge point of the measured peaks
+    (278 FLOP/B on GB300) decides whether tensor or HBM bounds it."""
+    pairs = visible_pairs(wl)
+    fwd_b, bwd_b = algorithmic_bytes(wl)
+    avg_bwd, avg_fwd = statistics.mean(bwd_main_ms), statistics.mean(fwd_ms)
+    dom = "bwd_main" if avg_bwd >= avg_fwd else "fwd"
+    dom_ms = avg_bwd if dom == "bwd_main" else avg_fwd
+    dom_flop = pairs * (FLOP_BWD_PER_PAIR if dom == "bwd_main" else FLOP_FWD_PER_PAIR)
+    dom_bytes = bwd_b if dom == "bwd_main" else fwd_b
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if dom_flop / dom_bytes >= ridge:
+        roof = {"bound": "tensor", "achieved": dom_flop / (dom_ms / 1e3) / 1e12, "peak": peaks["bf16_tflops"],
+                "peak_source": f"{peak_src} bf16 burst", "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": dom_bytes / (dom_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
+                "peak_source": f"{peak_src} HBM copy", "unit": "GB/s"}
+    return {"bound": roof["bound"], "kernel": dom, "kernel_name": KERNEL_NAMES[dom], "achieved": roof["achieved"],
+            "peak": roof["peak"], "peak_source": roof["peak_source"], "unit": roof["unit"],
+            "frac": roof["achieved"] / roof["peak"], "traffic": _committed_traffic(workload_name, dom),
+            "flop_per_byte": dom_flop / dom_bytes, "ridge_flop_per_byte": ridge, "algorithmic_bytes": dom_bytes,
+            "kernel_ms": dom_ms, "tflops": dom_flop / (dom_ms / 1e3) / 1e12,
+            "hbm_gbs_equiv": dom_bytes / (dom_ms / 1e3) / 1e9}
+
+
+def measure_config(name, dev, flush, peaks, peak_src, target_s=0.3):
+    """One extra workload at N = 1: enough timed steps to span about
+    ``target_s`` seconds (so the 20 ms clock sampler sees the load), with its
+    TFLOP/s, the dominant kernel against its roof, and the clocks."""
+    import torch
+
+    wl = W.WORKLOADS[name]
+    st = attention_setup(wl, dev)
+    probe, _, _, _ = time_attention(st, 3, 3, dev, flush, 1)
+    K = int(min(2000, max(20, math.ceil(target_s * 1e3 / (statistics.median(probe) + 0.1)))))
+    step_ms, fwd_ms, bwd_ms, clocks = time_attention(st, K, 3, dev, flush, 1, sample_ms=20)
+    flop = visible_pairs(wl) * (FLOP_FWD_PER_PAIR + FLOP_BWD_PER_PAIR)
+    tot = sum(step_ms)
+    value = flop * K / (tot / 1e3) / 1e12
+    roof = roofline_of(wl, fwd_ms, bwd_ms, peaks, peak_src, name)
+    out = {"tflops": value, "pct_of_peak": 100.0 * value / peaks["bf16_tflops"], "ms_per_step": tot / K, "steps": K,
+           "dominant_kernel": roof["kernel_name"], "dominant_ms": roof["kernel_ms"],
+           "breakdown_ms": {"fwd_kernel": statistics.mean(fwd_ms), "bwd_main_kernel": statistics.mean(bwd_ms),
+                            "rest": statistics.mean(step_ms) - statistics.mean(fwd_ms) - statistics.mean(bwd_ms)},
+           "roofline": roof, "gpu_launches": K * st["launches_per_step"], "clocks": clocks,
+           "flop_per_step": flop, "algorithmic_bytes_per_step": sum(algorithmic_bytes(wl))}
+    del st
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_gpu(args, world, rank, local):
     import torch
 
@@ -447,64 +592,11 @@ def run_gpu(args, world, rank, local):
     torch.cuda.set_device(dev)
     base = W.WORKLOADS[args.workload]
     wl = base.with_(seed=base.seed + 1000 * rank)  # each rank: its own batch
-    inp = W.make_inputs(wl)
-    q, k, v, do = (t.to(dev) for t in (inp.q_bf16, inp.k_bf16, inp.v_bf16, inp.do_bf16))
-    sink = inp.sink.to(dev)
-    if wl.uniform:
-        prob = dict(num_seqs=wl.num_seqs)
-    else:
-        cu = wl.cu_seqlens()
-        prob = dict(cu_seqlens=torch.tensor(cu, dtype=torch.int32, device=dev),
-                    cu_seqlens_host=[int(x) for x in cu], max_seqlen=wl.max_seqlen)
-    prob.update(window=wl.window, prefix=wl.prefix, causal=wl.causal, scale=wl.scale)
-    o = torch.empty_like(q)
-    lse = torch.empty((wl.num_heads_q, wl.total_tokens), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    dsink = torch.empty_like(sink)
-    ws = torch.empty(max(16, sa.bwd_workspace_bytes(q, k, **prob)), dtype=torch.uint8, device=dev)
+    st = attention_setup(wl, dev)
+    q, k, v, do, sink, o, lse, ws, prob = (st[n] for n in ("q", "k", "v", "do", "sink", "o", "lse", "ws", "prob"))
     flush = L2Flush(dev)
-    # Our kernels per step, counted by the library from its own work lists.
-    launches_per_step = sa.kernel_launches(q, k, "fwd", **prob) + sa.kernel_launches(q, k, "bwd", **prob)
-
-    def step():
-        sa.sinkattn_fwd(q, k, v, sink, o=o, lse=lse, **prob)
-        sa.sinkattn_bwd(q, k, v, o, lse, do, sink, dq=dq, dk=dk, dv=dv, dsink=dsink, workspace=ws, **prob)
-
-    for _ in range(max(args.warmup, 0)):
-        flush(1.0)
-        step()
-    torch.cuda.synchronize()
-    if sa.sinkattn_get_device_status() != 0:
-        raise RuntimeError("device status reported a timed-out wait during warm-up")
-
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
-    for e in ev:  # torch creates the CUDA event on first record(); the hook needs the handle
-        for x in e:
-            x.record()
-    torch.cuda.synchronize()
-    clocks = ClockSampler(dev.index if dev.index is not None else 0)
-    barrier(world)
-    torch.cuda.synchronize()
-    clocks.start()
-    for i in range(K):
-        flush(float(i))
-        e = ev[i]
-        sa.sinkattn_set_profile_events(sa.PROFILE_FWD, e[2], e[3])
-        sa.sinkattn_set_profile_events(sa.PROFILE_BWD_MAIN, e[4], e[5])
-        e[0].record()
-        step()
-        e[1].record()
-    torch.cuda.synchronize()
-    barrier(world)
-    clock_info = clocks.stop()
-    sa.sinkattn_set_profile_events(sa.PROFILE_FWD)
-    sa.sinkattn_set_profile_events(sa.PROFILE_BWD_MAIN)
-    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    fwd_ms = [e[2].elapsed_time(e[3]) for e in ev]
-    bwd_main_ms = [e[4].elapsed_time(e[5]) for e in ev]
-    if sa.sinkattn_get_device_status() != 0:
-        raise RuntimeError("device status reported a timed-out wait")
+    step_ms, fwd_ms, bwd_main_ms, clock_info = time_attention(st, K, args.warmup, dev, flush, world, sample_ms=20)
 
     # ---- end to end through host buffers (pinned), copies inside the timed
     # region.  Double-buffered, as a training loop feeding the library would
@@ -515,7 +607,7 @@ def run_gpu(args, world, rank, local):
     sets = []
     for _ in range(2):
         din = [torch.empty_like(t) for t in (q, k, v, do, sink)]
-        dout = [torch.empty_like(t) for t in (o, lse, dq, dk, dv, dsink)]
+        dout = [torch.empty_like(t) for t in (o, lse, st["dq"], st["dk"], st["dv"], st["dsink"])]
         sets.append((din, dout, [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dout]))
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in sets[0][2])
@@ -556,6 +648,7 @@ def run_gpu(args, world, rank, local):
     e2e_ms = [e2e_start.elapsed_time(e2e_end)]
     if sa.sinkattn_get_device_status() != 0:
         raise RuntimeError("device status reported a timed-out wait")
+    del sets, host_in
 
     # ---- reduce over ranks (max) and report
     tot, e2e_tot = reduce_max([sum(step_ms), sum(e2e_ms)], world, dev)
@@ -564,23 +657,8 @@ def run_gpu(args, world, rank, local):
     value = world * flop_step * K / (tot / 1e3) / 1e12
     e2e_value = world * flop_step * Ke / (e2e_tot / 1e3) / 1e12
     peaks, peak_src = load_peaks()
-    fwd_b, bwd_b = algorithmic_bytes(wl)
-    avg_bwd = statistics.mean(bwd_main_ms)
-    avg_fwd = statistics.mean(fwd_ms)
-    dom = "bwd_main" if avg_bwd >= avg_fwd else "fwd"
-    dom_ms = avg_bwd if dom == "bwd_main" else avg_fwd
-    dom_flop = pairs * (FLOP_BWD_PER_PAIR if dom == "bwd_main" else FLOP_FWD_PER_PAIR)
-    dom_bytes = bwd_b if dom == "bwd_main" else fwd_b
-    # Which roof bounds the dominant kernel: its algorithmic FLOP per byte
-    # against the ridge point of the measured peaks (278 FLOP/B on GB300).
-    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    if dom_flop / dom_bytes >= ridge:
-        roof = {"bound": "tensor", "achieved": dom_flop / (dom_ms / 1e3) / 1e12, "peak": peaks["bf16_tflops"],
-                "peak_source": f"{peak_src} bf16 burst", "unit": "TFLOP/s"}
-    else:
-        roof = {"bound": "hbm", "achieved": dom_bytes / (dom_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
-                "peak_source": f"{peak_src} HBM copy", "unit": "GB/s"}
-    traffic = _committed_traffic(args.workload, dom)
+    roof = roofline_of(wl, fwd_ms, bwd_main_ms, peaks, peak_src, args.workload)
+    avg_fwd, avg_bwd = statistics.mean(fwd_ms), statistics.mean(bwd_main_ms)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": tot / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
@@ -594,19 +672,20 @@ def run_gpu(args, world, rank, local):
         "pct_of_peak": 100.0 * value / world / peaks["bf16_tflops"],
         "breakdown_ms": {"fwd_kernel": avg_fwd, "bwd_main_kernel": avg_bwd,
                          "rest": statistics.mean(step_ms) - avg_fwd - avg_bwd},
-        "roofline": {"bound": roof["bound"], "kernel": dom, "achieved": roof["achieved"], "peak": roof["peak"],
-                     "peak_source": roof["peak_source"], "unit": roof["unit"],
-                     "frac": roof["achieved"] / roof["peak"], "traffic": traffic,
-                     "flop_per_byte": dom_flop / dom_bytes, "ridge_flop_per_byte": ridge,
-                     "algorithmic_bytes": dom_bytes,
-                     "tflops": dom_flop / (dom_ms / 1e3) / 1e12,
-                     "hbm_gbs_equiv": dom_bytes / (dom_ms / 1e3) / 1e9},
+        "roofline": roof,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": Ke, "mode": "pinned host buffers, double-buffered: step i+1's inputs up and step i-1's "
                                      "outputs down on two copy streams while step i computes; one timed region"},
-        "gpu_launches": K * launches_per_step,
+        "gpu_launches": K * st["launches_per_step"],
         "clocks": clock_info,
     }
+    del st, q, k, v, do, sink, o, lse, ws
+    torch.cuda.empty_cache()
+    if world == 1 and not args.no_configs:
+        # The other attention workloads at N = 1, each timed the same way
+        # (not part of the line's value): causal and windowed, uniform and packed.
+        line["configs"] = {name: measure_config(name, dev, flush, peaks, peak_src)
+                           for name in EXTRA_CONFIGS if name != args.workload}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl)
     if rank == 0:
@@ -914,6 +993,7 @@ def main(argv=None):
                     choices=sorted(W.WORKLOADS) + sorted(W.DECODE_WORKLOADS) + sorted(W.GRPO_WORKLOADS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU baseline leg")
+    ap.add_argument("--no-configs", action="store_true", help="skip the extra attention workloads (configs)")
     args = ap.parse_args(argv)
     world, rank, local = dist_setup()
     if args.impl == "reference":

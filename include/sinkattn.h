@@ -39,6 +39,12 @@
  * Errors: argument checks run on the host before anything is launched; a
  * failing check returns its status and launches nothing.  A failed launch
  * returns SINKATTN_ERR_CUDA.  Nothing aborts, exits or traps on the device.
+ *
+ * First call on a device: the calls that launch kernels (fwd, bwd, decode,
+ * GRPO, the wait self-test) look up the device address of the library's
+ * status word once per device, with that device current, through
+ * cudaGetSymbolAddress (thread-safe).  Make the first such call on each
+ * device outside any stream capture; later calls only launch kernels.
  */
 #ifndef SINKATTN_H
 #define SINKATTN_H

@@ -27,6 +27,51 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
+HEAD_DIM = 64
+
+
+def _check(name: str, t: Optional[torch.Tensor], dtype: torch.dtype, shape=None, device=None) -> None:
+    """Reject what the C ABI cannot see: it receives only a raw pointer, so a
+    tensor of another dtype, layout, size or device would be read as
+    garbage.  Checked in this order: shape, dtype, contiguity, same device as
+    the call's first tensor (``device``); ``_on_gpu`` then checks that this
+    device is a GPU."""
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if shape is not None:
+        if t.dim() != len(shape) or any(s is not None and int(a) != int(s) for a, s in zip(t.shape, shape)):
+            want = "[" + ", ".join("*" if s is None else str(int(s)) for s in shape) + "]"
+            raise ValueError(f"{name} has shape {list(t.shape)}, expected {want}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _on_gpu(name: str, t: torch.Tensor) -> None:
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+
+
+def _check_qkv(q, k, v, sink):
+    """q [T, Hq, 64], k and v [T_kv, Hkv, 64] bf16 with Hq % Hkv == 0, sink [Hq] fp32, one CUDA device."""
+    if q is None or k is None or q.dim() != 3 or k.dim() != 3:
+        raise ValueError("q and k must be 3-D tensors [tokens, heads, head_dim]")
+    if q.shape[2] != HEAD_DIM or k.shape[2] != HEAD_DIM:
+        raise ValueError(f"head_dim must be {HEAD_DIM} (q: {q.shape[2]}, k: {k.shape[2]})")
+    hq, hkv = q.shape[1], k.shape[1]
+    if hkv < 1 or hq % hkv != 0:
+        raise ValueError(f"query heads ({hq}) must be a multiple of key/value heads ({hkv})")
+    dev = q.device
+    _check("q", q, torch.bfloat16, (None, hq, HEAD_DIM), dev)
+    _check("k", k, torch.bfloat16, (None, hkv, HEAD_DIM), dev)
+    _check("v", v, torch.bfloat16, tuple(k.shape), dev)
+    _check("sink", sink, torch.float32, (hq,), dev)
+    return dev
+
+
 def _stream() -> int:
     return torch.cuda.current_stream().cuda_stream
 
@@ -65,15 +110,30 @@ def make_problem(q: torch.Tensor, k: torch.Tensor, *, num_seqs: Optional[int] = 
     return pr, keep
 
 
+def _check_cu(problem: dict, dev) -> None:
+    cu = problem.get("cu_seqlens")
+    if cu is not None:
+        host = problem.get("cu_seqlens_host")
+        n = None if host is None else len(host)
+        _check("cu_seqlens", cu, torch.int32, (n,), dev)
+
+
 def sinkattn_fwd(q, k, v, sink, *, o=None, lse=None, workspace=None, **problem):
     """Forward: returns (o, lse).  ``problem`` keys as in make_problem."""
-    lib = _lib.load()
-    pr, keep = make_problem(q, k, **problem)
+    dev = _check_qkv(q, k, v, sink)
     T, hq, d = q.shape
+    if k.shape[0] != T:
+        raise ValueError(f"k and v hold {k.shape[0]} tokens, q holds {T}")
     if o is None:
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((hq, T), dtype=torch.float32, device=q.device)
+    _check("o", o, torch.bfloat16, tuple(q.shape), dev)
+    _check("lse", lse, torch.float32, (hq, T), dev)
+    _check_cu(problem, dev)
+    _on_gpu("q", q)
+    lib = _lib.load()
+    pr, keep = make_problem(q, k, **problem)
     ws_bytes = lib.sinkattn_fwd_workspace_size(ctypes.byref(pr))
     if workspace is None and ws_bytes > 0:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
@@ -102,12 +162,27 @@ def bwd_workspace_bytes(q, k, **problem) -> int:
 def sinkattn_bwd(q, k, v, o, lse, dout, sink, *, dq=None, dk=None, dv=None, dsink=None, workspace=None,
                  **problem):
     """Backward: returns (dq, dk, dv, dsink)."""
-    lib = _lib.load()
-    pr, keep = make_problem(q, k, **problem)
+    dev = _check_qkv(q, k, v, sink)
+    T, hq, _ = q.shape
+    if k.shape[0] != T:
+        raise ValueError(f"k and v hold {k.shape[0]} tokens, q holds {T}")
+    _check("o", o, torch.bfloat16, tuple(q.shape), dev)
+    _check("dout", dout, torch.bfloat16, tuple(q.shape), dev)
+    _check("lse", lse, torch.float32, (hq, T), dev)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     dsink = torch.empty_like(sink) if dsink is None else dsink
+    _check("dq", dq, torch.bfloat16, tuple(q.shape), dev)
+    _check("dk", dk, torch.bfloat16, tuple(k.shape), dev)
+    _check("dv", dv, torch.bfloat16, tuple(k.shape), dev)
+    _check("dsink", dsink, torch.float32, (hq,), dev)
+    if workspace is not None:
+        _check("workspace", workspace, torch.uint8, (None,), dev)
+    _check_cu(problem, dev)
+    _on_gpu("q", q)
+    lib = _lib.load()
+    pr, keep = make_problem(q, k, **problem)
     ws_bytes = int(lib.sinkattn_bwd_workspace_size(ctypes.byref(pr)))
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
@@ -133,13 +208,20 @@ def sinkattn_decode_fwd(q, k, v, sink, *, q_per_seq: int, o=None, lse=None, work
     of the last q_per_seq positions of each sequence in order.  Each output
     row equals the same row of sinkattn_fwd over the whole sequence.
     """
-    lib = _lib.load()
-    pr, keep = make_problem(q, k, total_tokens=k.shape[0], **problem)
+    dev = _check_qkv(q, k, v, sink)
     R, hq, d = q.shape
     if o is None:
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((hq, R), dtype=torch.float32, device=q.device)
+    _check("o", o, torch.bfloat16, tuple(q.shape), dev)
+    _check("lse", lse, torch.float32, (hq, R), dev)
+    if workspace is not None:
+        _check("workspace", workspace, torch.uint8, (None,), dev)
+    _check_cu(problem, dev)
+    _on_gpu("q", q)
+    lib = _lib.load()
+    pr, keep = make_problem(q, k, total_tokens=k.shape[0], **problem)
     ws_bytes = int(lib.sinkattn_decode_workspace_size(ctypes.byref(pr), int(q_per_seq)))
     if workspace is None:
         # zero-filled: the chunk counters at its start must be zero (each call leaves them so)
@@ -170,7 +252,8 @@ def grpo_workspace_bytes(cu_tokens, cu_tokens_host, *, group_size: int) -> int:
 
 
 def grpo_loss(logp, logp_old, mask, rewards, cu_tokens, cu_tokens_host, *, group_size: int, clip_eps: float = 0.2,
-              adv_eps: float = 1e-6, kl_beta: float = 0.0, logp_ref=None, dlogp=None, workspace=None):
+              adv_eps: float = 1e-6, kl_beta: float = 0.0, logp_ref=None, dlogp=None, workspace=None, stats=None,
+              advantages=None):
     """GRPO token loss: returns (stats [4] fp32, dlogp [T] fp32, advantages [R] fp32).
 
     stats = (loss, policy term, KL term, clipped fraction); all tensors on the
@@ -180,12 +263,30 @@ def grpo_loss(logp, logp_old, mask, rewards, cu_tokens, cu_tokens_host, *, group
     once; each completed call leaves it reusable.  Without one, a zero-filled
     workspace is allocated per call.
     """
-    lib = _lib.load()
     R = len(cu_tokens_host) - 1
+    dev = logp.device if isinstance(logp, torch.Tensor) else None
+    _check("logp", logp, torch.float32, (None,), dev)
+    T = logp.shape[0]
+    _check("logp_old", logp_old, torch.float32, (T,), dev)
+    if kl_beta:
+        _check("logp_ref", logp_ref, torch.float32, (T,), dev)
+    _check("mask", mask, torch.uint8, (T,), dev)
+    _check("rewards", rewards, torch.float32, (R,), dev)
+    _check("cu_tokens", cu_tokens, torch.int32, (R + 1,), dev)
+    if dlogp is not None:
+        _check("dlogp", dlogp, torch.float32, (T,), dev)
+    if stats is not None:
+        _check("stats", stats, torch.float32, (4,), dev)
+    if advantages is not None:
+        _check("advantages", advantages, torch.float32, (R,), dev)
+    if workspace is not None:
+        _check("workspace", workspace, torch.uint8, (None,), dev)
+    _on_gpu("logp", logp)
+    lib = _lib.load()
     g, keep = _grpo_problem(cu_tokens, cu_tokens_host, group_size, clip_eps, adv_eps, kl_beta)
-    stats = torch.empty(4, dtype=torch.float32, device=logp.device)
+    stats = torch.empty(4, dtype=torch.float32, device=logp.device) if stats is None else stats
     dlogp = torch.empty_like(logp) if dlogp is None else dlogp
-    adv = torch.empty(R, dtype=torch.float32, device=logp.device)
+    adv = torch.empty(R, dtype=torch.float32, device=logp.device) if advantages is None else advantages
     ws_bytes = int(lib.sinkattn_grpo_workspace_size(ctypes.byref(g)))
     if workspace is None:
         workspace = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=logp.device)
@@ -197,6 +298,8 @@ def grpo_loss(logp, logp_old, mask, rewards, cu_tokens, cu_tokens_host, *, group
 
 def sinkattn_varlen_plan(seqlens: torch.Tensor) -> torch.Tensor:
     """Device int32 lengths [B] -> device int32 offsets [B + 1]."""
+    _check("seqlens", seqlens, torch.int32, (None,))
+    _on_gpu("seqlens", seqlens)
     lib = _lib.load()
     cu = torch.empty(seqlens.numel() + 1, dtype=torch.int32, device=seqlens.device)
     _lib.check("sinkattn_varlen_plan",
@@ -206,8 +309,11 @@ def sinkattn_varlen_plan(seqlens: torch.Tensor) -> torch.Tensor:
 
 def sinkattn_pack(padded: torch.Tensor, cu_seqlens: torch.Tensor, total_tokens: int) -> torch.Tensor:
     """[B, Smax, H, D] bf16 -> [T, H, D] (rows past each length dropped)."""
-    lib = _lib.load()
+    _check("padded", padded, torch.bfloat16, (None, None, None, None))
     B, Smax, H, D = padded.shape
+    _check("cu_seqlens", cu_seqlens, torch.int32, (B + 1,), padded.device)
+    _on_gpu("padded", padded)
+    lib = _lib.load()
     packed = torch.empty((total_tokens, H, D), dtype=padded.dtype, device=padded.device)
     _lib.check("sinkattn_pack", lib.sinkattn_pack(_ptr(padded), _ptr(cu_seqlens), B, Smax, H, D,
                                                   _ptr(packed), _stream()))
@@ -216,8 +322,11 @@ def sinkattn_pack(padded: torch.Tensor, cu_seqlens: torch.Tensor, total_tokens: 
 
 def sinkattn_unpack(packed: torch.Tensor, cu_seqlens: torch.Tensor, B: int, Smax: int) -> torch.Tensor:
     """[T, H, D] -> [B, Smax, H, D] with zero padding rows."""
-    lib = _lib.load()
+    _check("packed", packed, torch.bfloat16, (None, None, None))
     T, H, D = packed.shape
+    _check("cu_seqlens", cu_seqlens, torch.int32, (int(B) + 1,), packed.device)
+    _on_gpu("packed", packed)
+    lib = _lib.load()
     padded = torch.empty((B, Smax, H, D), dtype=packed.dtype, device=packed.device)
     _lib.check("sinkattn_unpack", lib.sinkattn_unpack(_ptr(packed), _ptr(cu_seqlens), B, Smax, H, D,
                                                       _ptr(padded), _stream()))

@@ -210,7 +210,8 @@ cudaError_t launch_bwd(const Problem& pr, const BwdArgs& a, int* status, cudaStr
     ConvK k{a.dq_accum, static_cast<__nv_bfloat16*>(a.dq), T * pr.hq * D / 8, pr.scale, a.dsink_part,
             a.preprocess_blocks, pr.hq, a.dsink};
     long long blocks = (k.n8 + 255) / 256;
-    if (blocks > 152 * 16) blocks = 152 * 16;
+    const long long cap = 16LL * device_sms();
+    if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     dq_convert_kernel<<<static_cast<int>(blocks) + (pr.hq + 7) / 8, 256, 0, stream>>>(k);
   }

@@ -54,19 +54,6 @@
 
 #include <algorithm>
 
-// Optional timeline instrumentation for performance work: compiled in only
-// when SA_BWD_TRACE is defined (never in the library build).
-#ifdef SA_BWD_TRACE
-__device__ long long* g_bwd_trace;
-#define SA_TRACE(role, step, ev)                                                                       \
-  do {                                                                                                \
-    if (trace_p != nullptr && (step) < 1024) trace_p[((role) * 1024 + (step)) * 8 + (ev)] = clock64(); \
-  } while (0)
-#else
-#define SA_TRACE(role, step, ev) \
-  do {                           \
-  } while (0)
-#endif
 
 namespace sa {
 namespace {
@@ -114,9 +101,10 @@ struct BwdTcK {
   MaskParams mask;
   float scale, scale_log2;
   // Work list slice (longest first).  A key tile whose query range is longer
-  // than `qchunk` query tiles is split into chunks, one item each; their
-  // partial dK/dV are added into the fp32 accumulator dkv_acc
-  // ([T][Hkv][2][64]: dV then unscaled dK) and converted afterwards.
+  // than `qchunk` query tiles is split into chunks, one item each; each chunk
+  // writes its partial dK/dV to its own fp32 slot of dkv_acc
+  // ([slot][Hkv][2][128 keys][64]: dV, then unscaled dK) and a conversion
+  // pass sums the slots of a tile in chunk order.
   int qchunk;
   float* dkv_acc;
   int n_items;
@@ -143,12 +131,6 @@ SA_DEV uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
   return v;
-}
-
-// Vector fp32 atomic add (no return value).
-SA_DEV void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
 }
 
 SA_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -229,9 +211,6 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x;
-#ifdef SA_BWD_TRACE
-  long long* const trace_p = (blockIdx.x == 0 && blockIdx.y == 0) ? g_bwd_trace : nullptr;
-#endif
   const BwdItem item = p.items[blockIdx.y];  // longest first
   const SeqSpan sp = seq_span(p.cu, p.seqlen, item.b);
   const int k0 = static_cast<int>(item.kt) * BN;
@@ -317,7 +296,6 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
     for (int t = 0; t < nsteps; ++t) {
       const int s = t % NS;
       if (t >= NS && !mbar_wait_warp(b_qe(s), ((t / NS) - 1) & 1, ab)) break;
-      if (lane == 0) SA_TRACE(0, t, 0);
       const int h = step_head(t), q0 = step_q0(t);
       // Bias rows of the 128 query rows: asynchronous 16-byte copies that
       // complete on the stage's full barrier (rows past the sequence end read
@@ -333,7 +311,6 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
         mbar_expect_tx(b_qf(s), 2 * TILE);
         tma_load_2d(sb + OFF_Q + s * TILE, &p.tm_q, h * D, sp.start + q0, b_qf(s));
         tma_load_2d(sb + OFF_DO + s * TILE, &p.tm_do, h * D, sp.start + q0, b_qf(s));
-        SA_TRACE(0, t, 1);
       }
       issued = t + 1;
     }
@@ -393,13 +370,11 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
       for (int t = 0; ok && t < nsteps; ++t) {
         const int s = t % NS, db = t & 1;
         const bool more = t + 1 < nsteps;
-        if (lane == 0) SA_TRACE(1, t, 0);
         // Phase 1 of each half is done (packed P^T in the S^T columns):
         // dV += P_h^T dO_h, then the next step's S_h^T over those columns
         // (the tensor core runs MMAs in issue order).
         for (int h = 0; h < 2 && ok; ++h) {
           if (!(ok = mbar_wait_warp(b_pt(h), t & 1, ab))) break;
-          if (lane == 0) SA_TRACE(1, t, 1 + h);
           fence_after_sync();
           const uint64_t o = sdesc_add(d_o, s * TILE + h * HALF * 128);
 #pragma unroll
@@ -421,7 +396,6 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
         // dK += dS_h^T Q_h, then the next step's dP_h^T over those columns.
         for (int h = 0; h < 2 && ok; ++h) {
           if (!(ok = mbar_wait_warp(b_ds(h), t & 1, ab))) break;
-          if (lane == 0) SA_TRACE(1, t, 3 + h);
           fence_after_sync();
           const uint64_t q = sdesc_add(d_q, s * TILE + h * HALF * 128);
 #pragma unroll
@@ -440,7 +414,6 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
           if (!(ok = mbar_wait_warp(b_dqe, (t - 1) & 1, ab))) break;
           fence_after_sync();
         }
-        if (lane == 0) SA_TRACE(1, t, 5);
         const uint64_t dsm = sdesc_add(d_dsm, db * 2 * TILE);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
@@ -480,10 +453,8 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
       if (lane == 0) mbar_arrive(b_kvt);
     }
     for (int t = 0; ok && t < nsteps; ++t) {
-      if (tid == 128 || tid == 256) SA_TRACE(2 + (tid == 256 ? 2 : 0), t, 0);
       ok = mbar_wait_warp(b_s(half), t & 1, ab);
       if (!ok) break;
-      if (tid == 128 || tid == 256) SA_TRACE(2 + (tid == 256 ? 2 : 0), t, 1);
       fence_after_sync();
       const int qh = step_q0(t) + HALF * half;
       const bool full = block_full(qh, HALF, k0, BN, sp.len, p.mask);
@@ -497,7 +468,6 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_pt(half));
-      if (tid == 128 || tid == 256) SA_TRACE(2 + (tid == 256 ? 2 : 0), t, 2);
       if (!(ok = mbar_wait_warp(b_dp(half), t & 1, ab))) break;
       fence_after_sync();
       ew_phase2(tDP, rowb, kr, pv);
@@ -506,7 +476,6 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_ds(half));
-      if (tid == 128 || tid == 256) SA_TRACE(2 + (tid == 256 ? 2 : 0), t, 4);
     }
     ok = ok && mbar_wait_warp(b_done, 0, ab);
     if (ok) {
@@ -520,17 +489,20 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
       reg_fence32(a);
       reg_fence32(b2);
       const float mul = half ? p.scale : 1.f;
-      if (key < sp.len && split) {
-        // Partial sums of a split tile: add into the fp32 accumulator.
-        float* dst = p.dkv_acc + (static_cast<size_t>(sp.start + key) * p.hkv + g) * 2 * D + half * D;
+      if (split) {
+        // Partial sums of one chunk of a split tile: this thread's key row of
+        // the chunk's own slot (rows past the sequence end are written too and
+        // never read).
+        float4* dst = reinterpret_cast<float4*>(
+            p.dkv_acc + ((static_cast<size_t>(item.slot) * p.hkv + g) * 2 + half) * (BN * D) + kr * D);
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-          red_add_v4(dst + 4 * c, __uint_as_float(a[4 * c]), __uint_as_float(a[4 * c + 1]),
-                     __uint_as_float(a[4 * c + 2]), __uint_as_float(a[4 * c + 3]));
+          dst[c] = make_float4(__uint_as_float(a[4 * c]), __uint_as_float(a[4 * c + 1]),
+                               __uint_as_float(a[4 * c + 2]), __uint_as_float(a[4 * c + 3]));
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-          red_add_v4(dst + 32 + 4 * c, __uint_as_float(b2[4 * c]), __uint_as_float(b2[4 * c + 1]),
-                     __uint_as_float(b2[4 * c + 2]), __uint_as_float(b2[4 * c + 3]));
+          dst[8 + c] = make_float4(__uint_as_float(b2[4 * c]), __uint_as_float(b2[4 * c + 1]),
+                                   __uint_as_float(b2[4 * c + 2]), __uint_as_float(b2[4 * c + 3]));
       } else if (key < sp.len) {
         __nv_bfloat16* dst = (half ? p.dk : p.dv) + (static_cast<size_t>(sp.start + key) * p.hkv + g) * D;
         uint4* d4 = reinterpret_cast<uint4*>(dst);
@@ -557,10 +529,8 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
     const uint32_t stg = sb + OFF_STG;
     bool ok = true;
     for (int t = 0; t < nsteps; ++t) {
-      if (leader) SA_TRACE(3, t, 0);
       ok = mbar_wait_warp(b_dqf, t & 1, ab);
       if (!ok) break;
-      if (leader) SA_TRACE(3, t, 1);
       fence_after_sync();
       uint32_t a[32], b2[32];
       tmem_ld32(tQ, a);
@@ -574,7 +544,6 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
       const int h = step_head(t), q0 = step_q0(t);
       const bool valid = q0 + qr < sp.len;
       if (leader) bulk_wait_read0();
-      if (leader) SA_TRACE(3, t, 2);
       named_sync(1, 128);
       // Columns 0-31, then 32-63, through the one 16 KB staging tile.
 #pragma unroll
@@ -602,7 +571,6 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
       if (leader) {
         tma_reduce_add_2d(&p.tm_dq, h * D + 32, sp.start + q0, stg);
         bulk_commit();
-        SA_TRACE(3, t, 3);
       }
     }
     if (leader) bulk_wait0();
@@ -616,10 +584,17 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
   }
 }
 
-// dK, dV of split key tiles: fp32 accumulator -> bf16 (dK scaled).  A flat
-// grid-stride pass over every 8-element group of the split tiles' rows, so
-// that many loads are in flight (the work is a few MB spread over a few
-// tiles: one block per tile would leave most SMs idle).
+// dK, dV of split key tiles: the sum of the tile's per-chunk fp32 slots, in
+// chunk order (deterministic), -> bf16 (dK scaled).  A flat grid-stride pass
+// over every 8-element group of the split tiles' rows, so that many loads are
+// in flight (the work is a few MB spread over a few tiles: one block per tile
+// would leave most SMs idle).
+struct DkvTile {
+  uint32_t code;   // sequence | key tile << 16
+  uint32_t slot0;  // slot of chunk 0
+  uint32_t nchunks;
+};
+
 struct DkvConvK {
   const float* acc;
   __nv_bfloat16* dk;
@@ -627,41 +602,59 @@ struct DkvConvK {
   const int32_t* cu;
   int seqlen, hkv, n_tiles;
   float scale;
-  uint32_t tiles[2048];  // split key tiles: sequence | key tile << 16
+  DkvTile tiles[2048];
 };
+static_assert(sizeof(DkvConvK) < 32000, "kernel parameter block too large");
 
 __global__ void __launch_bounds__(256) dkv_convert_kernel(const __grid_constant__ DkvConvK p) {
   const int per_row = p.hkv * 2 * (D / 8);  // 8-element groups per key row
   const long long per_tile = static_cast<long long>(BN) * per_row;
   const long long total = per_tile * p.n_tiles;
+  const size_t slot_floats = static_cast<size_t>(p.hkv) * 2 * BN * D;
   for (long long i = blockIdx.x * 256LL + threadIdx.x; i < total; i += static_cast<long long>(gridDim.x) * 256) {
     const int s = static_cast<int>(i / per_tile);
     const int rem0 = static_cast<int>(i - s * per_tile);
     const int r = rem0 / per_row, rem = rem0 - r * per_row;
-    const uint32_t code = p.tiles[s];
-    const SeqSpan sp = seq_span(p.cu, p.seqlen, static_cast<int>(code & 0xFFFFu));
-    const int k0 = static_cast<int>(code >> 16) * BN;
+    const DkvTile tile = p.tiles[s];
+    const SeqSpan sp = seq_span(p.cu, p.seqlen, static_cast<int>(tile.code & 0xFFFFu));
+    const int k0 = static_cast<int>(tile.code >> 16) * BN;
     if (k0 + r >= sp.len) continue;
     const int g = rem / (2 * (D / 8)), which = (rem / (D / 8)) & 1, c8 = rem % (D / 8);
-    const size_t row = static_cast<size_t>(sp.start + k0 + r);
-    const float* src = p.acc + ((row * p.hkv + g) * 2 + which) * D + 8 * c8;
+    const float4* src = reinterpret_cast<const float4*>(
+        p.acc + tile.slot0 * slot_floats + ((static_cast<size_t>(g) * 2 + which) * BN + r) * D + 8 * c8);
+    float4 x = __ldcs(src), y = __ldcs(src + 1);
+    for (uint32_t c = 1; c < tile.nchunks; ++c) {
+      const float4* sc = src + c * (slot_floats / 4);
+      const float4 xc = __ldcs(sc), yc = __ldcs(sc + 1);
+      x = make_float4(x.x + xc.x, x.y + xc.y, x.z + xc.z, x.w + xc.w);
+      y = make_float4(y.x + yc.x, y.y + yc.y, y.z + yc.z, y.w + yc.w);
+    }
     const float mul = which ? p.scale : 1.f;
-    const float4 x = __ldcs(reinterpret_cast<const float4*>(src)), y = __ldcs(reinterpret_cast<const float4*>(src) + 1);
     uint4 o;
     o.x = pack_bf16(x.x * mul, x.y * mul);
     o.y = pack_bf16(x.z * mul, x.w * mul);
     o.z = pack_bf16(y.x * mul, y.y * mul);
     o.w = pack_bf16(y.z * mul, y.w * mul);
+    const size_t row = static_cast<size_t>(sp.start + k0 + r);
     *reinterpret_cast<uint4*>((which ? p.dk : p.dv) + (row * p.hkv + g) * D + 8 * c8) = o;
   }
+}
+
+// Split tiles of a work list (each tile once, from its chunk 0).
+std::vector<DkvTile> split_tiles(const std::vector<BwdItem>& items) {
+  std::vector<DkvTile> tiles;
+  for (const BwdItem& it : items)
+    if (it.nchunks > 1 && it.chunk == 0)
+      tiles.push_back({static_cast<uint32_t>(it.b) | (static_cast<uint32_t>(it.kt) << 16), it.slot, it.nchunks});
+  return tiles;
 }
 
 }  // namespace
 
 size_t bwd_split_acc_bytes(const Problem& pr) {
   if (pr.total_tokens == 0 || pr.num_seqs == 0) return 0;
-  if (!bwd_any_split(bwd_work_list(pr, bwd_qchunk(pr)))) return 0;
-  return static_cast<size_t>(pr.total_tokens) * pr.hkv * 2 * D * sizeof(float);
+  const int slots = bwd_split_slots(bwd_work_list(pr, bwd_qchunk(pr)));
+  return static_cast<size_t>(slots) * pr.hkv * 2 * BN * D * sizeof(float);
 }
 
 int bwd_tc_main_launches(const Problem& pr) {
@@ -669,14 +662,13 @@ int bwd_tc_main_launches(const Problem& pr) {
   const std::vector<BwdItem> items = bwd_work_list(pr, bwd_qchunk(pr));
   constexpr size_t kMax = sizeof(BwdTcK::items) / sizeof(BwdTcK::items[0]);
   constexpr size_t kMaxTiles = sizeof(DkvConvK::tiles) / sizeof(DkvConvK::tiles[0]);
-  size_t split_tiles = 0;
-  for (const BwdItem& it : items) split_tiles += (it.nchunks > 1 && it.chunk == 0) ? 1 : 0;
-  return static_cast<int>((items.size() + kMax - 1) / kMax + (split_tiles + kMaxTiles - 1) / kMaxTiles);
+  const size_t n_split = split_tiles(items).size();
+  return static_cast<int>((items.size() + kMax - 1) / kMax + (n_split + kMaxTiles - 1) / kMaxTiles);
 }
 
 cudaError_t launch_bwd_tc_main(const Problem& pr, const BwdArgs& a, int* status, cudaStream_t stream) {
   if (pr.num_seqs == 0 || pr.total_tokens == 0 || pr.seqlen == 0) return cudaSuccess;
-  thread_local BwdTcK k;  // 17 KB parameter block; host-side staging, one per host thread
+  thread_local BwdTcK k;  // 25 KB parameter block; host-side staging, one per host thread
   if (!make_rows_map(&k.tm_q, a.q, pr.total_tokens, pr.hq, BM) ||
       !make_rows_map(&k.tm_do, a.dout, pr.total_tokens, pr.hq, BM) ||
       !make_rows_map(&k.tm_k, a.k, pr.total_tokens, pr.hkv, BN) ||
@@ -699,12 +691,9 @@ cudaError_t launch_bwd_tc_main(const Problem& pr, const BwdArgs& a, int* status,
   k.qchunk = bwd_qchunk(pr);
   k.dkv_acc = a.dkv_acc;
   const std::vector<BwdItem> items = bwd_work_list(pr, k.qchunk);
-  const bool any_split = bwd_any_split(items);
+  const std::vector<DkvTile> tiles = split_tiles(items);
+  if (!tiles.empty() && a.dkv_acc == nullptr) return cudaErrorInvalidValue;
   cudaError_t e;
-  if (any_split) {
-    if (a.dkv_acc == nullptr) return cudaErrorInvalidValue;
-    if ((e = cudaMemsetAsync(a.dkv_acc, 0, bwd_split_acc_bytes(pr), stream)) != cudaSuccess) return e;
-  }
   if ((e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_DYN)) !=
       cudaSuccess)
     return e;
@@ -718,7 +707,7 @@ cudaError_t launch_bwd_tc_main(const Problem& pr, const BwdArgs& a, int* status,
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if ((e = prof_end(g_prof_bwd, stream)) != cudaSuccess) return e;
-  if (any_split) {
+  if (!tiles.empty()) {
     thread_local DkvConvK c;
     c.acc = a.dkv_acc;
     c.dk = static_cast<__nv_bfloat16*>(a.dk);
@@ -727,16 +716,13 @@ cudaError_t launch_bwd_tc_main(const Problem& pr, const BwdArgs& a, int* status,
     c.seqlen = pr.seqlen;
     c.hkv = pr.hkv;
     c.scale = pr.scale;
-    std::vector<uint32_t> tiles;  // each split tile once (its chunk 0)
-    for (const BwdItem& it : items)
-      if (it.nchunks > 1 && it.chunk == 0) tiles.push_back(static_cast<uint32_t>(it.b) | (static_cast<uint32_t>(it.kt) << 16));
     constexpr int kMaxTiles = static_cast<int>(sizeof(c.tiles) / sizeof(c.tiles[0]));
     for (size_t first = 0; first < tiles.size(); first += kMaxTiles) {
       const int n = static_cast<int>(std::min<size_t>(kMaxTiles, tiles.size() - first));
       std::copy(tiles.begin() + first, tiles.begin() + first + n, c.tiles);
       c.n_tiles = n;
       const long long groups = static_cast<long long>(n) * BN * pr.hkv * 2 * (D / 8);
-      const int blocks = static_cast<int>(std::min<long long>((groups + 255) / 256, 152LL * 8));
+      const int blocks = static_cast<int>(std::min<long long>((groups + 255) / 256, 8LL * device_sms()));
       dkv_convert_kernel<<<blocks, 256, 0, stream>>>(c);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }

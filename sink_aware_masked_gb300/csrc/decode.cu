@@ -444,22 +444,11 @@ __global__ void __launch_bounds__(NTHR, 3) decode_split_kernel(const __grid_cons
   if (tid == 0) p.counters[b * p.hkv + g] = 0;  // every chunk of this call has counted
 }
 
-// SMs of the current device; 152 (a GB300) when no device answers, so that
-// the host-side plan (and the workspace size it implies) is the same with or
-// without a GPU.
-int num_sms() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      n <= 0)
-    return 152;
-  return n;
-}
-
 }  // namespace
 
 DecodePlan decode_plan(const Problem& p, int n) {
   DecodePlan pl;
-  const int sms = num_sms();
+  const int sms = device_sms();
   std::vector<int> tiles(p.num_seqs);
   long long total = 0;
   for (int b = 0; b < p.num_seqs; ++b) {

@@ -62,19 +62,6 @@
 
 #include <algorithm>
 
-// Optional timeline instrumentation for performance work: compiled in only
-// when SA_FWD_TRACE is defined (never in the library build).
-#ifdef SA_FWD_TRACE
-__device__ long long* g_fwd_trace;
-#define SA_TRACE(role, step, ev)                                                         \
-  do {                                                                                  \
-    if (trace_p != nullptr && (step) < 256) trace_p[((role) * 256 + (step)) * 8 + (ev)] = clock64(); \
-  } while (0)
-#else
-#define SA_TRACE(role, step, ev) \
-  do {                           \
-  } while (0)
-#endif
 
 namespace sa {
 namespace {
@@ -168,9 +155,6 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nh = p.nh;
-#ifdef SA_FWD_TRACE
-  long long* const trace_p = blockIdx.x == 0 ? g_fwd_trace : nullptr;
-#endif
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
@@ -276,7 +260,6 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
               for (int kk = 0; kk < D / 16; ++kk)
                 if (leader) mma_ss(tmem + TM_S + 128 * i, sdesc_add(qd, kk * 32), sdesc_add(kd, kk * 32), id_s, kk > 0);
               if (leader) mma_commit(b_s(i));
-              if (lane == 0) SA_TRACE(0, nt, 1 + i);
             }
             if (leader) {
               if (j == u.n_tiles - 1) mma_commit(b_qe(qb));
@@ -308,7 +291,6 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
                 }
               }
               if (leader) mma_commit(b_pv(hf));
-              if (lane == 0) SA_TRACE(0, nt, 3 + hf);
             }
             if (ok && leader) mma_commit(b_e(s));
           }
@@ -336,9 +318,7 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
         const int q = u.q0 + row;
         float m_ref = -INFINITY, l = 0.f;
         for (int j = 0; j < u.n_tiles; ++j, ++nt) {
-          if ((warp & 3) == 0 && lane == 0) SA_TRACE(1 + i, nt, 0);
           if (!(ok = wait_all(b_s(i), nt & 1))) break;
-          if ((warp & 3) == 0 && lane == 0) SA_TRACE(1 + i, nt, 1);
           fence_after_sync();
           uint32_t r_[4][32];
 #pragma unroll
@@ -346,7 +326,6 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
           tmem_ld_wait();
 #pragma unroll
           for (int c = 0; c < 4; ++c) reg_fence32(r_[c]);
-          if ((warp & 3) == 0 && lane == 0) SA_TRACE(1 + i, nt, 4);
           // S_i is in registers: the tensor core may overwrite it.
           fence_before_sync();
           __syncwarp();
@@ -387,7 +366,6 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
             m_ref = m_new;
             l *= factor;
           }
-          if ((warp & 3) == 0 && lane == 0) SA_TRACE(1 + i, nt, 5);
           if (__any_sync(0xffffffffu, resc)) {
             // O_i must hold every P.V of the previous steps (the second
             // half's commit covers the first half's MMAs).
@@ -406,7 +384,6 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
             tmem_st32(tO, o[0]);
             tmem_st32(tO + 32, o[1]);
           }
-          if ((warp & 3) == 0 && lane == 0) SA_TRACE(1 + i, nt, 2);
           const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
           const float2 sl2x2 = make_float2(sl2, sl2), negx2 = make_float2(neg, neg);
           float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
@@ -432,14 +409,12 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(b_p(hh));
-            if (hh == 0 && (warp & 3) == 0 && lane == 0) SA_TRACE(1 + i, nt, 7);
           }
           if (!ok) break;
 #undef S_
           const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
           const float2 at = fadd2(a01, a23);
           l += at.x + at.y;
-          if ((warp & 3) == 0 && lane == 0) SA_TRACE(1 + i, nt, 3);
         }
         if (!ok) break;
         // ------------------------------------------------------ epilogue
@@ -481,13 +456,6 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
   }
 }
 
-int num_sms() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return 0;
-  return n;
-}
-
 }  // namespace
 
 int fwd_tc_launches(const Problem& pr) {
@@ -503,8 +471,7 @@ cudaError_t launch_fwd_tc(const Problem& pr, const FwdArgs& a, int* status, cuda
       !make_rows_map(&k.tm_k, a.k, pr.total_tokens, pr.hkv, BN) ||
       !make_rows_map(&k.tm_v, a.v, pr.total_tokens, pr.hkv, BN))
     return cudaErrorInvalidValue;
-  const int sms = num_sms();
-  if (sms <= 0) return cudaErrorInvalidDevice;
+  const int sms = device_sms();
   k.sink = a.sink;
   k.o = static_cast<__nv_bfloat16*>(a.o);
   k.lse = a.lse;

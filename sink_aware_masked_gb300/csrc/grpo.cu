@@ -532,14 +532,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) grpo_kernel(const GrpoK 
 // Grid bound: one CTA per stage of vectors (2048 tokens) at most, and at
 // most kCtasPerSm per SM.
 int max_ctas(int T) {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0, s = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&s, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        s <= 0)
-      s = 152;
-    sms = s;
-  }
+  const int sms = device_sms();
   const int by_work = std::max(1, (T / 4 + kStageVec - 1) / kStageVec);
   return std::min(by_work, kCtasPerSm * sms);
 }
@@ -567,9 +560,7 @@ cudaError_t launch_grpo(const GrpoArgs& a, cudaStream_t stream) {
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, grpo_kernel, kThreads, dyn);
   if (e != cudaSuccess) return e;
   if (per_sm <= 0) return cudaErrorInvalidConfiguration;
-  int sms = 0, dev = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess || (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-    return e;
+  const int sms = device_sms();
   const int grid = std::min(max_ctas(a.total_tokens), per_sm * sms);
   if (grid >= (1 << kArriveBits)) return cudaErrorInvalidConfiguration;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);

@@ -53,26 +53,37 @@ struct BwdArgs {
   // the main kernel adds them to S^T and dP^T through one K=16 MMA.
   void* bias;
   float* dsink_part;  // [preprocess blocks, Hq]
-  float* dkv_acc;     // fp32 dK/dV partial sums of split prefix key tiles (or nullptr)
+  float* dkv_acc;     // fp32 dK/dV partial sums of split key tiles, one slot per chunk (or nullptr)
   int preprocess_blocks;
 };
 
 // Preprocess tokens per block (bounds the number of dsink partial rows).
 constexpr int kPreTokens = 8;
 
+// Streaming multiprocessors of the current device, cached per device; 152
+// (a GB300) when no device answers, so that host-side plans and the
+// workspace sizes they imply are the same with or without a GPU.
+int device_sms();
+
 inline int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
 // One backward work item: key tile `kt` of sequence `b`, query chunk `chunk`
-// of `nchunks` (nchunks > 1: partial dK/dV go to the fp32 accumulator).
+// of `nchunks`.  When nchunks > 1 the item's partial dK/dV go to fp32 slot
+// `slot` of the workspace (one slot per chunk; the chunks of one tile hold
+// consecutive slots, chunk c at slot - chunk + c), and a conversion pass
+// sums a tile's slots in chunk order, so the result does not depend on the
+// order in which the chunks ran.
 struct BwdItem {
   uint16_t b, kt, chunk, nchunks;
+  uint32_t slot;
 };
 
 // Work lists (schedule.cu), longest first.
 std::vector<uint32_t> fwd_work_list(const Problem& p);  // b | (query tile << 16)
 int bwd_qchunk(const Problem& p);
 std::vector<BwdItem> bwd_work_list(const Problem& p, int qchunk);
-bool bwd_any_split(const std::vector<BwdItem>& items);
+// Partial-sum slots the items of a list use (items with nchunks > 1).
+int bwd_split_slots(const std::vector<BwdItem>& items);
 
 // Decode forward (decode.cu): the last n query rows of each sequence against
 // its whole key/value history, split over the keys and merged afterwards.

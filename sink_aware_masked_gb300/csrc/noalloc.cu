@@ -18,8 +18,10 @@
 //     Make that first call before any stream capture.
 //   * All calls share the one array, and it keeps whatever the last call left
 //     there.  Nothing in it has to start at zero: the backward preprocess
-//     kernel clears the dQ accumulator itself and every other part is fully
-//     overwritten before it is read.  Calls whose kernels overlap on the GPU
+//     kernel clears the fp32 dQ accumulator before the main kernel adds into
+//     it, and every other part (the per-row bias terms, the dsink partial
+//     sums, the per-chunk dK/dV partial sums of split key tiles) is written
+//     in full before it is read.  Calls whose kernels overlap on the GPU
 //     (different streams, or several host threads) race on the array and give
 //     wrong results: serialise them.
 #include <mutex>

@@ -13,6 +13,7 @@
 //   one SM's average share of the work, and never below 4 (short chunks
 //   waste the pipeline fill).  Split tiles accumulate dK/dV in fp32.
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <vector>
 
@@ -22,7 +23,8 @@ namespace sa {
 namespace {
 
 constexpr int TILE_ROWS = 128;
-constexpr int kNumSMs = 152;
+constexpr int kMaxDevices = 256;
+constexpr int kFallbackSms = 152;  // a GB300, when no device answers
 
 struct Span {
   int start, len;
@@ -59,6 +61,17 @@ int bwd_query_tiles(const Problem& p, int k0, int len) {
 
 }  // namespace
 
+int device_sms() {
+  static std::atomic<int> cache[kMaxDevices];  // zero until the first query of a device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return kFallbackSms;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return kFallbackSms;
+  cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
 std::vector<uint32_t> fwd_work_list(const Problem& p) {
   struct It {
     int cost;
@@ -87,7 +100,8 @@ int bwd_qchunk(const Problem& p) {
       longest = std::max(longest, nq);
     }
   // Per-SM average of query tiles (x kv heads, every CTA covers one kv head).
-  const long long per_sm = (total * p.hkv + kNumSMs - 1) / kNumSMs;
+  const int sms = device_sms();
+  const long long per_sm = (total * p.hkv + sms - 1) / sms;
   const int cap = static_cast<int>(std::max<long long>(4, per_sm / 2));
   return std::max(1, std::min(cap, longest));
 }
@@ -99,6 +113,7 @@ std::vector<BwdItem> bwd_work_list(const Problem& p, int qchunk) {
   };
   std::vector<It> items;
   const auto s = spans(p);
+  uint32_t slot = 0;  // chunks of split tiles, in tile then chunk order
   for (int b = 0; b < p.num_seqs; ++b)
     for (int k0 = 0; k0 < s[b].len; k0 += TILE_ROWS) {
       const int nq = bwd_query_tiles(p, k0, s[b].len);
@@ -106,7 +121,8 @@ std::vector<BwdItem> bwd_work_list(const Problem& p, int qchunk) {
       for (int c = 0; c < chunks; ++c) {
         const int cost = std::min(qchunk, nq - c * qchunk);
         items.push_back({cost, BwdItem{static_cast<uint16_t>(b), static_cast<uint16_t>(k0 / TILE_ROWS),
-                                       static_cast<uint16_t>(c), static_cast<uint16_t>(chunks)}});
+                                       static_cast<uint16_t>(c), static_cast<uint16_t>(chunks),
+                                       chunks > 1 ? slot++ : 0u}});
       }
     }
   std::stable_sort(items.begin(), items.end(), [](const It& a, const It& c) { return a.cost > c.cost; });
@@ -115,10 +131,10 @@ std::vector<BwdItem> bwd_work_list(const Problem& p, int qchunk) {
   return out;
 }
 
-bool bwd_any_split(const std::vector<BwdItem>& items) {
-  for (const auto& it : items)
-    if (it.nchunks > 1) return true;
-  return false;
+int bwd_split_slots(const std::vector<BwdItem>& items) {
+  int n = 0;
+  for (const auto& it : items) n += it.nchunks > 1 ? 1 : 0;
+  return n;
 }
 
 }  // namespace sa

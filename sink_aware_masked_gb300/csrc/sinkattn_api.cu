@@ -1,9 +1,11 @@
 // C ABI of the sink-aware attention library: argument checks, problem
 // normalisation, workspace layout and kernel dispatch.  Declarations and the
 // contract of every entry point are in include/sinkattn.h.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/sinkattn.h"
 #include "internal.h"
@@ -18,17 +20,28 @@ namespace {
 // Device status word raised by kernels that give up a bounded wait.
 __device__ int g_device_status = 0;
 
-// Device address of g_device_status for the current device (looked up once).
+// Device address of g_device_status for the current device, looked up once
+// per device (cudaGetSymbolAddress, under a lock; later calls read the cached
+// pointer).  The first lookup on a device is a CUDA runtime call that stream
+// capture does not record: make the first call of the library on each device
+// outside any capture.
 int* status_word() {
-  static int* ptr[256] = {};
+  constexpr int kMaxDevices = 256;
+  static std::atomic<int*> ptr[kMaxDevices];
+  static std::mutex setup;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return nullptr;
-  if (ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
-    ptr[dev] = static_cast<int*>(p);
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  int* p = ptr[dev].load(std::memory_order_acquire);
+  if (p != nullptr) return p;
+  std::lock_guard<std::mutex> lock(setup);
+  p = ptr[dev].load(std::memory_order_relaxed);
+  if (p == nullptr) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_device_status) != cudaSuccess || a == nullptr) return nullptr;
+    p = static_cast<int*>(a);
+    ptr[dev].store(p, std::memory_order_release);
   }
-  return ptr[dev];
+  return p;
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

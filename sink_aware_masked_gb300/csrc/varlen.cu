@@ -92,7 +92,8 @@ cudaError_t launch_pack(const void* src, const int32_t* cu, int B, int Smax, int
   const long long total = static_cast<long long>(B) * Smax * k.vec_per_row;
   if (total == 0) return cudaSuccess;
   long long blocks = (total + 255) / 256;
-  if (blocks > 152 * 32) blocks = 152 * 32;
+  const long long cap = 32LL * device_sms();
+  if (blocks > cap) blocks = cap;
   pack_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(k);
   return cudaGetLastError();
 }

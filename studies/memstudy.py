@@ -14,7 +14,7 @@ O = P[..., :S] V (the zero-value sink contributes nothing to O), followed by
 autograd's backward.  Its memory is quadratic in S; the library keeps every
 buffer linear in S.
 
-Run:  python -m sink_aware_masked_gb300.memstudy [--seqlens 4096 8192 16384]
+Run:  python -m studies.memstudy [--seqlens 4096 8192 16384]
 """
 from __future__ import annotations
 
@@ -25,7 +25,7 @@ from typing import Dict, Optional
 
 import torch
 
-from . import api
+from sink_aware_masked_gb300 import api
 
 
 def eager_reference_layer(q, k, v, sink, dout, *, window: int = api.WINDOW_INF, prefix: int = 0,

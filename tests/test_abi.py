@@ -97,14 +97,25 @@ def test_null_and_misaligned_pointers(lib):
 
 
 def test_workspace_sizes_are_linear_in_tokens(lib):
+    """The backward workspace is the fp32 dQ accumulator and one 16-byte bias
+    row per (head, token), both linear in T, plus the per-chunk dK/dV slots of
+    split key tiles: at most 2 * SMs + (key tiles) * Hkv slot-heads of 64 KB
+    (chunks hold at least half an SM's share of the work, so there are at most
+    2 * SMs / Hkv more chunks than tiles).  No term grows faster than T."""
+    sms = 152  # the host-side plan without a device assumes a GB300
     sizes = []
-    for S in (1024, 2048, 4096, 8192):
-        pr = problem(seqlen=S, total_tokens=S, num_heads_q=64, num_heads_kv=8)
-        sizes.append(lib.sinkattn_bwd_workspace_size(ctypes.byref(pr)))
-        # dQ accumulator fp32 + two [Hq, T] fp32 rows + dsink partials: linear in T
-        assert sizes[-1] >= S * 64 * 64 * 4 + 2 * S * 64 * 4
-    d1, d2, d3 = sizes[1] - sizes[0], sizes[2] - sizes[1], sizes[3] - sizes[2]
-    assert abs(d2 - 2 * d1) <= 1024 and abs(d3 - 2 * d2) <= 2048
+    for S in (1024, 2048, 4096, 8192, 16384, 32768):
+        for window in (-1, 128):
+            pr = problem(seqlen=S, total_tokens=S, num_heads_q=64, num_heads_kv=8, window=window)
+            ws = lib.sinkattn_bwd_workspace_size(ctypes.byref(pr))
+            linear = S * 64 * 64 * 4 + S * 64 * 16
+            assert ws >= linear
+            tiles = (S + 127) // 128
+            assert ws <= linear + (2 * sms + tiles * 8) * 65536 + S * 64 + 4096, (S, window)
+            if window == -1:
+                sizes.append(ws)
+    # Large problems split few tiles: doubling T doubles the workspace.
+    assert abs(sizes[-1] - 2 * sizes[-2]) <= 0.01 * sizes[-1]
     assert lib.sinkattn_fwd_workspace_size(ctypes.byref(problem())) == 0
 
 

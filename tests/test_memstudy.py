@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle.sinkattn_ref as ref
-from sink_aware_masked_gb300 import memstudy
+from studies import memstudy
 
 
 @pytest.mark.parametrize("window,prefix", [(-1, 0), (5, 3)])
