@@ -11,8 +11,9 @@
 //   bwd_pre   : one pass over O and dO: the bias rows (-l'/scale and -D as
 //               bf16 hi/mid/lo triples) the main kernel folds into its S^T and
 //               dP^T MMAs, per-block partial dsink sums, zeroes the fp32 dQ
-//               accumulator.  HBM-bound; every thread issues the loads of four
-//               tokens before using them.
+//               accumulator and the main kernel's unit-claim counters.
+//               HBM-bound; every thread issues the loads of four tokens
+//               before using them.
 //   dq_convert: dQ = scale * accumulator -> bf16; ceil(Hq / 8) extra blocks
 //               reduce the dsink partials in a fixed order (deterministic),
 //               one warp per head.
@@ -33,6 +34,8 @@ struct PreK {
   uint4* bias;
   float* dq_accum;
   float* dsink_part;
+  int* counters;  // the main kernel's unit-claim counters, cleared here
+  int n_counters;
   long long T;
   int hq;
   float scale;
@@ -74,6 +77,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreK p) {
   const int hs = threadIdx.x >> 3;   // 0..31
   const long long t0 = static_cast<long long>(blockIdx.x) * kPreTokens;
   const long long t1 = min(t0 + kPreTokens, p.T);
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < p.n_counters; i += blockDim.x) p.counters[i] = 0;
   for (int h = hs; h < ((p.hq + 31) & ~31); h += 32) {
     const bool ok = h < p.hq;
     const float sk = ok ? __ldg(p.sink + h) : 0.f;
@@ -197,7 +202,8 @@ cudaError_t launch_bwd(const Problem& pr, const BwdArgs& a, int* status, cudaStr
   const long long T = pr.total_tokens;
   {
     PreK k{static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.sink,
-           static_cast<uint4*>(a.bias), a.dq_accum, a.dsink_part, T, pr.hq, pr.scale};
+           static_cast<uint4*>(a.bias), a.dq_accum, a.dsink_part, a.unit_counters, a.n_unit_counters, T, pr.hq,
+           pr.scale};
     if (a.preprocess_blocks > 0) bwd_pre_kernel<<<a.preprocess_blocks, 256, 0, stream>>>(k);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

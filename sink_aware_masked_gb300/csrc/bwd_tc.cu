@@ -10,17 +10,27 @@
 //   dV  += P^T dO,  dK += dS^T Q (scale applied at the end),  dQ = dS K
 // Nothing of size S x S is stored: P and dS live one 128 x 128 tile at a time.
 //
-// Work unit (one CTA): 128 keys of one sequence and one kv head; the CTA
-// loops over the query heads of the GQA group x the 128-row query tiles that
-// can see those keys ("steps"), so dK and dV accumulate in Tensor Memory
-// without atomics.  Each step's 128 query rows are split into two 64-row
-// halves A and B, each with its own S^T / dP^T buffers and its own
-// element-wise warpgroup, so the tensor core works on one half while the
-// other half's element-wise pass runs.
+// Persistent: one CTA per SM takes work units from a list sorted longest
+// first, claiming the next one from a global counter when its loader has
+// issued the last loads of the current one (greedy list scheduling: an SM
+// that finishes early takes the next unit, whatever the units' costs; the
+// claim comes a few steps before the unit is needed, so the loads run on
+// across the boundary).  A unit is 128 keys of one sequence and one
+// kv head (possibly one query chunk of them); the CTA loops over the query
+// heads of the GQA group x the 128-row query tiles that see those keys
+// ("steps"), so dK and dV accumulate in Tensor Memory without atomics.  Each
+// step's 128 query rows are split into two 64-row halves A and B, each with
+// its own S^T / dP^T buffers and element-wise warpgroup, so the tensor core
+// works on one half while the other half's element-wise pass runs.  Steps
+// are numbered across units, so the Q/dO ring, the per-step barriers and the
+// dQ drain run on without a break at unit boundaries.
 // Warp roles (16 warps, four warpgroups):
-//   warp 0      loader: K, V once; per step Q and dO tiles by TMA (3-stage
-//               ring) and the 128 l' and D values of the query tile by
-//               cp.async, all completing on the stage's full barrier.
+//   warp 0      unit claimer and Q/dO loader: claims the next unit (atomic
+//               add on the launch's counter) once it has issued the loads of
+//               the current one and publishes the claim in a 4-entry shared
+//               ring that every other role reads; per step Q and dO tiles by
+//               TMA (NS-stage ring) and the 128 bias rows of the query tile
+//               by cp.async, all completing on the stage's full barrier.
 //   warp 1      MMA issuer and TMEM owner (whole warp, one elected lane
 //               issues).  Per half h of step t, as the element-wise warps
 //               hand their results over:
@@ -30,16 +40,24 @@
 //               next step's S^T and dP^T overwrite the columns the
 //               preceding MMA read, which the tensor core runs first), then
 //               for the whole step dQ(t) = dS(t) K (A = the dS^T tile in
-//               shared memory read MN-major, B = K MN-major).
+//               shared memory read MN-major, B = K MN-major).  The first dV
+//               product of a unit (which overwrites dV) waits until the
+//               element-wise warps have read the previous unit's dK, dV.
+//   warp 2      K/V loader: K and V of each unit by TMA into one of KVB
+//               buffers, a buffer once every MMA of the unit that used it
+//               has completed; the tiles are prefetched into L2 as soon as
+//               the unit is claimed.
 //   warps 4-7   element-wise for half A, warps 8-11 for half B; thread = key
 //               row.  Phase 1: P^T = exp(S^T - l'), packed over the S^T
 //               columns just read, then signalled, so dV and the next S^T
 //               run while phase 2 computes dS^T = P^T (dP^T - D), packed
 //               over the dP^T columns and into a double-buffered 128 x 128
 //               bf16 shared tile (128-byte swizzle) for the dQ product.
-//               At start they copy K and V into TMEM; at the end one
-//               warpgroup writes dV, the other dK.  Fully visible tiles
-//               take a path without the mask predicate.
+//               At a unit's start they copy its K and V into TMEM, then read
+//               the previous unit's dV (half A) and dK (half B) out of TMEM
+//               and write them while the new unit's first products run.
+//               Partial tiles clear masked entries with a per-key bit mask
+//               of the visible queries (one interval per key).
 //   warps 12-15 dQ drain: thread = query row; TMEM -> swizzled fp32 staging
 //               tile (32 columns at a time) -> TMA reduce-add into the fp32
 //               dQ accumulator.
@@ -54,39 +72,49 @@
 
 #include <algorithm>
 
-
 namespace sa {
 namespace {
 
 using namespace tc;
 
 constexpr int D = kHeadDim;
-constexpr int BN = 128;  // keys per CTA (TMEM lanes)
+constexpr int BN = 128;  // keys per unit (TMEM lanes)
 constexpr int BM = 128;  // query rows per step
-constexpr int NS = 3;    // Q/dO (and l', D) stages
 constexpr int NTHR = 512;
 // setmaxnreg split of the 512 x 128 launch registers: 128 x 56 (loader/MMA
 // warpgroup) + 256 x 168 (two element-wise warpgroups) + 128 x 96 (dQ drain)
 // = 62,464 <= 65,536.
 constexpr int REGS_LOW = 56, REGS_EW = 168, REGS_DQ = 96;
 constexpr int TILE = 128 * D * 2;  // 16 KB
-constexpr int OFF_K = 0;
-constexpr int OFF_V = OFF_K + TILE;
-constexpr int OFF_Q = OFF_V + TILE;
-constexpr int OFF_DO = OFF_Q + NS * TILE;
-constexpr int OFF_DS = OFF_DO + NS * TILE;     // 2 buffers x 32 KB
-constexpr int OFF_STG = OFF_DS + 2 * 2 * TILE;  // 16 KB fp32 dQ staging (32 of the 64 columns at a time)
-// Bias rows of the stage's 128 queries (16 bytes each: -l'/scale and -D as
-// bf16 hi/mid/lo, two zeros), the two 0/1 selector tiles that pick one triple
-// or the other (128 keys x 16 bytes), and a zero block that serves as the
-// upper K half (elements 8-15) of all of them.  All K-major, no swizzle.
-constexpr int OFF_BIAS = OFF_STG + TILE;           // NS x 2 KB
-constexpr int OFF_SEL = OFF_BIAS + NS * BM * 16;   // 2 x 2 KB
-constexpr int OFF_ZERO = OFF_SEL + 2 * BN * 16;    // 2 KB
-constexpr int SMEM_DYN = OFF_ZERO + BN * 16 + 1024;
+
+// Shared memory of a configuration with NS Q/dO stages and KVB K/V buffers.
+// Three stages and one K/V buffer fill the 227 KB of a CTA; measured against
+// two stages and two K/V buffers (the next unit's K and V loading while the
+// current one runs), the third stage is worth more on every workload, the
+// short windowed units included.
+template <int NS, int KVB>
+struct Layout {
+  static constexpr int OFF_K = 0;                     // buffer b: + 2 b TILE
+  static constexpr int OFF_V = TILE;                  // buffer b: + 2 b TILE
+  static constexpr int OFF_Q = 2 * KVB * TILE;
+  static constexpr int OFF_DO = OFF_Q + NS * TILE;
+  static constexpr int OFF_DS = OFF_DO + NS * TILE;      // 2 buffers x 32 KB
+  static constexpr int OFF_STG = OFF_DS + 2 * 2 * TILE;  // 16 KB fp32 dQ staging (32 of the 64 columns at a time)
+  // Bias rows of the stage's 128 queries (16 bytes each: -l'/scale and -D as
+  // bf16 hi/mid/lo, two zeros), the two 0/1 selector tiles that pick one
+  // triple or the other (128 keys x 16 bytes), and a zero block that serves
+  // as the upper K half (elements 8-15) of all of them.  All K-major, no
+  // swizzle.
+  static constexpr int OFF_BIAS = OFF_STG + TILE;          // NS x 2 KB
+  static constexpr int OFF_SEL = OFF_BIAS + NS * BM * 16;  // 2 x 2 KB
+  static constexpr int OFF_ZERO = OFF_SEL + 2 * BN * 16;   // 2 KB
+  static constexpr int SMEM_DYN = OFF_ZERO + BN * 16 + 1024;
+  static_assert(SMEM_DYN <= 227 * 1024 - 512, "shared memory");
+};
 
 constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 320, TM_DQ = 384, TM_K = 448, TM_V = 480;
 constexpr int HALF = BM / 2;
+constexpr int kMaxItems = 2048;
 
 struct BwdTcK {
   CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dq;
@@ -100,25 +128,76 @@ struct BwdTcK {
   int hq, hkv, group;
   MaskParams mask;
   float scale, scale_log2;
-  // Work list slice (longest first).  A key tile whose query range is longer
-  // than `qchunk` query tiles is split into chunks, one item each; each chunk
-  // writes its partial dK/dV to its own fp32 slot of dkv_acc
-  // ([slot][Hkv][2][128 keys][64]: dV, then unscaled dK) and a conversion
-  // pass sums the slots of a tile in chunk order.
+  // Work list slice (longest first); unit u = item u / Hkv, kv head u % Hkv,
+  // claimed in increasing u.
+  // A key tile whose query range is longer than `qchunk` query tiles is split
+  // into chunks, one item each; each chunk writes its partial dK/dV to its
+  // own fp32 slot of dkv_acc ([slot][Hkv][2][128 keys][64]: dV, then
+  // unscaled dK) and a conversion pass sums the slots of a tile in chunk
+  // order.
   int qchunk;
   float* dkv_acc;
+  int* unit_counter;  // zero at launch (the preprocess kernel clears it)
   int n_items;
-  BwdItem items[2048];
+  int n_units;
+  BwdItem items[kMaxItems];
 };
 static_assert(sizeof(BwdTcK) < 32000, "kernel parameter block too large");
 
+// Claimed units in flight: the claimer runs at most NS steps ahead of the
+// MMA issuer, and every reader is within a unit of it.
+constexpr int kUnitRing = 4;
+constexpr int kUnitReaders = 14;  // warps 1, 2 and 4-15 read every claim
+
+template <int NS, int KVB>
 struct Bars {
-  uint64_t kv_full, kv_tmem;
+  uint64_t unit_full[kUnitRing], unit_empty[kUnitRing];
+  uint64_t kv_full[KVB], kv_empty[KVB];
+  uint64_t kv_tmem;                 // K, V of the unit copied into TMEM (8 element-wise warps)
+  uint64_t kv_done;                 // every MMA of the unit has completed
+  uint64_t dkv_free;                // the unit's dK, dV read out of TMEM (8 element-wise warps)
   uint64_t q_full[NS], q_empty[NS];
   uint64_t s_full[2], dp_full[2];   // per half: S^T / dP^T of the step ready
   uint64_t pt_full[2], ds_full[2];  // per half: packed P^T / dS^T written by the element-wise warps
-  uint64_t dq_full, dq_free, kv_done, drain;
+  uint64_t dq_full, dq_free, drain;
 };
+
+// One work unit as every role sees it.
+struct Unit {
+  BwdItem item;
+  int g;  // kv head
+  SeqSpan sp;
+  int k0;
+  int qt_lo, nq, nsteps;
+  SA_DEV bool split() const { return item.nchunks > 1; }
+};
+
+// Unit number `idx` of the launch; false past the end of the list.
+SA_DEV bool decode_unit(const BwdTcK& p, int idx, Unit& u) {
+  if (idx < 0 || idx >= p.n_units) return false;
+  u.item = p.items[idx / p.hkv];
+  u.g = idx % p.hkv;
+  u.sp = seq_span(p.cu, p.seqlen, u.item.b);
+  u.k0 = static_cast<int>(u.item.kt) * BN;
+  if (u.k0 >= u.sp.len) {  // never produced by the host's work list
+    u.qt_lo = u.nq = u.nsteps = 0;
+    return true;
+  }
+  const int k1 = min(u.k0 + BN, u.sp.len) - 1;
+  int qlo, qhi;
+  query_range(u.k0, k1, u.sp.len, p.mask, qlo, qhi);
+  u.qt_lo = qlo / BM;
+  u.nq = qhi / BM - u.qt_lo + 1;
+  if (u.split()) {
+    u.qt_lo += u.item.chunk * p.qchunk;
+    u.nq = min(p.qchunk, u.nq - u.item.chunk * p.qchunk);
+  }
+  u.nsteps = u.nq > 0 ? p.group * u.nq : 0;
+  return true;
+}
+
+SA_DEV int step_head(const BwdTcK& p, const Unit& u, int t) { return u.g * p.group + t / u.nq; }
+SA_DEV int step_q0(const Unit& u, int t) { return (u.qt_lo + t % u.nq) * BM; }
 
 SA_DEV void wait_drain(uint32_t bar, uint32_t parity) {
   const long long t0 = clock64();
@@ -145,10 +224,11 @@ SA_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint
 // multiply per phase and nothing is read from shared memory.
 //
 // Phase 1: P^T = exp2((S^T - l'/scale) * scale * log2(e)), masked on partial
-// tiles (FULL skips the predicate); packed P^T overwrites the S^T columns
-// already read; fp32 P stays in registers for phase 2.
+// tiles (FULL skips the mask) with the key's visible-query bits; packed P^T
+// overwrites the S^T columns already read; fp32 P stays in registers for
+// phase 2.
 template <bool FULL>
-SA_DEV void ew_phase1(uint32_t tS, float sl2, int qh, int key, int len, const MaskParams& mask, float (&pv)[4][16]) {
+SA_DEV void ew_phase1(uint32_t tS, float sl2, uint32_t vis0, uint32_t vis1, float (&pv)[4][16]) {
   const float2 sl2x2 = make_float2(sl2, sl2);
   uint32_t sr[4][16];
 #pragma unroll
@@ -159,15 +239,16 @@ SA_DEV void ew_phase1(uint32_t tS, float sl2, int qh, int key, int len, const Ma
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const uint32_t (&sc)[16] = sr[c];
+    const uint32_t vis = c < 2 ? vis0 : vis1;
     uint32_t pp[8];
 #pragma unroll
     for (int e = 0; e < 16; e += 2) {
       const float2 x = fmul2(make_float2(__uint_as_float(sc[e]), __uint_as_float(sc[e + 1])), sl2x2);
       float2 pe = make_float2(ex2(x.x), ex2(x.y));
       if (!FULL) {
-        const int q = qh + 16 * c + e;
-        if (!(q < len && visible(q, key, len, mask))) pe.x = 0.f;
-        if (!(q + 1 < len && visible(q + 1, key, len, mask))) pe.y = 0.f;
+        const int bit = (16 * c + e) & 31;
+        if (!(vis & (1u << bit))) pe.x = 0.f;
+        if (!(vis & (2u << bit))) pe.y = 0.f;
       }
       pv[c][e] = pe.x;
       pv[c][e + 1] = pe.y;
@@ -203,51 +284,87 @@ SA_DEV void ew_phase2(uint32_t tDP, uint32_t rowb, int kr, const float (&pv)[4][
   }
 }
 
+// This thread's key row of a finished unit's dV (half 0) or dK (half 1, with
+// the softmax scale), from registers: bf16 into dv / dk, or the fp32 partial
+// sums of one chunk of a split tile into the chunk's slot.
+SA_DEV void write_dkv(const BwdTcK& p, const Unit& u, int half, int kr, const uint32_t (&a)[32],
+                      const uint32_t (&b2)[32]) {
+  const int key = u.k0 + kr;
+  if (u.split()) {
+    // Rows past the sequence end are written too and never read.
+    float4* dst = reinterpret_cast<float4*>(
+        p.dkv_acc + ((static_cast<size_t>(u.item.slot) * p.hkv + u.g) * 2 + half) * (BN * D) + kr * D);
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      dst[c] = make_float4(__uint_as_float(a[4 * c]), __uint_as_float(a[4 * c + 1]), __uint_as_float(a[4 * c + 2]),
+                           __uint_as_float(a[4 * c + 3]));
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      dst[8 + c] = make_float4(__uint_as_float(b2[4 * c]), __uint_as_float(b2[4 * c + 1]),
+                               __uint_as_float(b2[4 * c + 2]), __uint_as_float(b2[4 * c + 3]));
+  } else if (key < u.sp.len) {
+    const float mul = half ? p.scale : 1.f;
+    __nv_bfloat16* dst = (half ? p.dk : p.dv) + (static_cast<size_t>(u.sp.start + key) * p.hkv + u.g) * D;
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      d4[c] = make_uint4(pack_bf16(__uint_as_float(a[8 * c]) * mul, __uint_as_float(a[8 * c + 1]) * mul),
+                         pack_bf16(__uint_as_float(a[8 * c + 2]) * mul, __uint_as_float(a[8 * c + 3]) * mul),
+                         pack_bf16(__uint_as_float(a[8 * c + 4]) * mul, __uint_as_float(a[8 * c + 5]) * mul),
+                         pack_bf16(__uint_as_float(a[8 * c + 6]) * mul, __uint_as_float(a[8 * c + 7]) * mul));
+      d4[4 + c] = make_uint4(pack_bf16(__uint_as_float(b2[8 * c]) * mul, __uint_as_float(b2[8 * c + 1]) * mul),
+                             pack_bf16(__uint_as_float(b2[8 * c + 2]) * mul, __uint_as_float(b2[8 * c + 3]) * mul),
+                             pack_bf16(__uint_as_float(b2[8 * c + 4]) * mul, __uint_as_float(b2[8 * c + 5]) * mul),
+                             pack_bf16(__uint_as_float(b2[8 * c + 6]) * mul, __uint_as_float(b2[8 * c + 7]) * mul));
+    }
+  }
+}
+
+template <int NS, int KVB>
 __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__ BwdTcK p) {
+  using L = Layout<NS, KVB>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ Bars bars;
+  __shared__ Bars<NS, KVB> bars;
+  __shared__ int unit_slot[kUnitRing];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = blockIdx.x;
-  const BwdItem item = p.items[blockIdx.y];  // longest first
-  const SeqSpan sp = seq_span(p.cu, p.seqlen, item.b);
-  const int k0 = static_cast<int>(item.kt) * BN;
-  if (k0 >= sp.len) return;
-  const int k1 = min(k0 + BN, sp.len) - 1;
-  const bool split = item.nchunks > 1;
-  int qlo, qhi;
-  query_range(k0, k1, sp.len, p.mask, qlo, qhi);
-  int qt_lo = qlo / BM, nq = qhi / BM - qt_lo + 1;
-  if (split) {
-    qt_lo += item.chunk * p.qchunk;
-    nq = min(p.qchunk, nq - item.chunk * p.qchunk);
-  }
-  const int nsteps = p.group * nq;
-  auto step_head = [&](int t) { return g * p.group + t / nq; };
-  auto step_q0 = [&](int t) { return (qt_lo + t % nq) * BM; };
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
-  const uint32_t b_kv = smem_u32(&bars.kv_full), b_kvt = smem_u32(&bars.kv_tmem);
+  auto b_uf = [&](int j) { return smem_u32(&bars.unit_full[j]); };
+  auto b_ue = [&](int j) { return smem_u32(&bars.unit_empty[j]); };
+  auto b_kvf = [&](int b) { return smem_u32(&bars.kv_full[b]); };
+  auto b_kve = [&](int b) { return smem_u32(&bars.kv_empty[b]); };
+  const uint32_t b_kvt = smem_u32(&bars.kv_tmem), b_done = smem_u32(&bars.kv_done);
+  const uint32_t b_dkv = smem_u32(&bars.dkv_free);
   const uint32_t b_dqf = smem_u32(&bars.dq_full), b_dqe = smem_u32(&bars.dq_free);
   auto b_s = [&](int h) { return smem_u32(&bars.s_full[h]); };
   auto b_dp = [&](int h) { return smem_u32(&bars.dp_full[h]); };
   auto b_pt = [&](int h) { return smem_u32(&bars.pt_full[h]); };
   auto b_ds = [&](int h) { return smem_u32(&bars.ds_full[h]); };
-  const uint32_t b_done = smem_u32(&bars.kv_done), b_dr = smem_u32(&bars.drain);
+  const uint32_t b_dr = smem_u32(&bars.drain);
   auto b_qf = [&](int s) { return smem_u32(&bars.q_full[s]); };
   auto b_qe = [&](int s) { return smem_u32(&bars.q_empty[s]); };
 
   if (tid == 0) {
     abort_flag = 0;
-    mbar_init(b_kv, 1);
+    for (int j = 0; j < kUnitRing; ++j) {
+      mbar_init(b_uf(j), 1);
+      mbar_init(b_ue(j), kUnitReaders);
+    }
+    for (int b = 0; b < KVB; ++b) {
+      mbar_init(b_kvf(b), 1);
+      mbar_init(b_kve(b), 1);
+    }
     for (int s = 0; s < NS; ++s) {
       mbar_init(b_qf(s), 33);  // 32 cp.async arrivals + the TMA expect-tx arrival
       mbar_init(b_qe(s), 1);
     }
     mbar_init(b_kvt, 8);
+    mbar_init(b_done, 1);
+    mbar_init(b_dkv, 8);
     for (int h = 0; h < 2; ++h) {
       mbar_init(b_s(h), 1);
       mbar_init(b_dp(h), 1);
@@ -256,7 +373,6 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
     }
     mbar_init(b_dqf, 1);
     mbar_init(b_dqe, 4);
-    mbar_init(b_done, 1);
     mbar_init(b_dr, 1);
     fence_mbar_init();
   }
@@ -268,9 +384,9 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
     // Selector rows [1,1,1,0,...] (picks -l'/scale) and [0,0,0,1,1,1,0,0]
     // (picks -D) in bf16, and the zero block.
     constexpr uint32_t one = 0x3F80u;
-    st_shared_v4(sb + OFF_SEL + tid * 16, one | (one << 16), one, 0u, 0u);
-    st_shared_v4(sb + OFF_SEL + BN * 16 + tid * 16, 0u, one << 16, one | (one << 16), 0u);
-    st_shared_v4(sb + OFF_ZERO + tid * 16, 0u, 0u, 0u, 0u);
+    st_shared_v4(sb + L::OFF_SEL + tid * 16, one | (one << 16), one, 0u, 0u);
+    st_shared_v4(sb + L::OFF_SEL + BN * 16 + tid * 16, 0u, one << 16, one | (one << 16), 0u);
+    st_shared_v4(sb + L::OFF_ZERO + tid * 16, 0u, 0u, 0u, 0u);
     fence_async_smem();  // generic-proxy writes, read by the tensor core
   }
   fence_before_sync();
@@ -278,69 +394,121 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
   fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
   const Abort ab{&abort_flag, p.status};
+  // This warp's r-th unit from the claim ring (whole warp): 1 = a unit, 0 =
+  // the end of the list, -1 = a wait gave up.
+  auto take = [&](int r, Unit& u) -> int {
+    const int j = r % kUnitRing;
+    if (!mbar_wait_warp(b_uf(j), (r / kUnitRing) & 1, ab)) return -1;
+    const int idx = *static_cast<volatile int*>(&unit_slot[j]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(b_ue(j));
+    return decode_unit(p, idx, u) ? 1 : 0;
+  };
 
   if (warp < 4) {
     regs_dec<REGS_LOW>();
     if (warp == 0) {
-    // ------------------------------------------------------------ loader
-    if (lane == 0) {
-      tma_prefetch_map(&p.tm_q);
-      tma_prefetch_map(&p.tm_k);
-      tma_prefetch_map(&p.tm_v);
-      tma_prefetch_map(&p.tm_do);
-      mbar_expect_tx(b_kv, 2 * TILE);
-      tma_load_2d(sb + OFF_K, &p.tm_k, g * D, sp.start + k0, b_kv);
-      tma_load_2d(sb + OFF_V, &p.tm_v, g * D, sp.start + k0, b_kv);
-    }
-    int issued = 0;
-    for (int t = 0; t < nsteps; ++t) {
-      const int s = t % NS;
-      if (t >= NS && !mbar_wait_warp(b_qe(s), ((t / NS) - 1) & 1, ab)) break;
-      const int h = step_head(t), q0 = step_q0(t);
-      // Bias rows of the 128 query rows: asynchronous 16-byte copies that
-      // complete on the stage's full barrier (rows past the sequence end read
-      // row 0 and are masked by the element-wise warps).
-#pragma unroll
-      for (int r = lane; r < BM; r += 32) {
-        const int qq = q0 + r;
-        const size_t idx = static_cast<size_t>(h) * p.T + sp.start + (qq < sp.len ? qq : 0);
-        cp_async16(sb + OFF_BIAS + (s * BM + r) * 16, p.bias + idx, true);
-      }
-      cp_async_arrive_noinc(b_qf(s));
+      // ---------------------------------------------------------- Q/dO loader
       if (lane == 0) {
-        mbar_expect_tx(b_qf(s), 2 * TILE);
-        tma_load_2d(sb + OFF_Q + s * TILE, &p.tm_q, h * D, sp.start + q0, b_qf(s));
-        tma_load_2d(sb + OFF_DO + s * TILE, &p.tm_do, h * D, sp.start + q0, b_qf(s));
+        tma_prefetch_map(&p.tm_q);
+        tma_prefetch_map(&p.tm_do);
       }
-      issued = t + 1;
-    }
-    if (lane == 0 && abort_flag) {
-      wait_drain(b_kv, 0);
-      for (int t = max(0, issued - NS); t < issued; ++t) wait_drain(b_qf(t % NS), (t / NS) & 1);
-    }
+      bool ok = true;
+      int n = 0;  // steps issued
+      Unit u;
+      for (int r = 0; ok; ++r) {
+        // Claim the CTA's r-th unit and publish it (whole warp, lane 0
+        // claims); the slot is free once every reader took claim r - 4.
+        const int j = r % kUnitRing;
+        if (r >= kUnitRing && !(ok = mbar_wait_warp(b_ue(j), ((r / kUnitRing) - 1) & 1, ab))) break;
+        int idx = 0;
+        if (lane == 0) {
+          idx = atomicAdd(p.unit_counter, 1);
+          unit_slot[j] = idx;
+          mbar_arrive(b_uf(j));  // release: the readers see the slot with the phase
+        }
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+        if (!decode_unit(p, idx, u)) break;
+        for (int t = 0; t < u.nsteps; ++t, ++n) {
+          const int s = n % NS;
+          if (n >= NS && !(ok = mbar_wait_warp(b_qe(s), ((n / NS) - 1) & 1, ab))) break;
+          const int h = step_head(p, u, t), q0 = step_q0(u, t);
+          // Bias rows of the 128 query rows: asynchronous 16-byte copies that
+          // complete on the stage's full barrier (rows past the sequence end
+          // read row 0 and are masked by the element-wise warps).
+#pragma unroll
+          for (int r2 = lane; r2 < BM; r2 += 32) {
+            const int qq = q0 + r2;
+            const size_t idx = static_cast<size_t>(h) * p.T + u.sp.start + (qq < u.sp.len ? qq : 0);
+            cp_async16(sb + L::OFF_BIAS + (s * BM + r2) * 16, p.bias + idx, true);
+          }
+          cp_async_arrive_noinc(b_qf(s));
+          if (lane == 0) {
+            mbar_expect_tx(b_qf(s), 2 * TILE);
+            tma_load_2d(sb + L::OFF_Q + s * TILE, &p.tm_q, h * D, u.sp.start + q0, b_qf(s));
+            tma_load_2d(sb + L::OFF_DO + s * TILE, &p.tm_do, h * D, u.sp.start + q0, b_qf(s));
+          }
+        }
+      }
+      if (lane == 0 && abort_flag)
+        for (int m = max(0, n - NS); m < n; ++m) wait_drain(b_qf(m % NS), (m / NS) & 1);
+    } else if (warp == 2) {
+      // ---------------------------------------------------------- K/V loader
+      // The whole warp takes the claims; lane 0 issues the loads.
+      if (lane == 0) {
+        tma_prefetch_map(&p.tm_k);
+        tma_prefetch_map(&p.tm_v);
+      }
+      bool ok = true;
+      int ru = 0;  // units loaded
+      Unit u;
+      for (int r = 0; ok; ++r) {
+        const int got = take(r, u);
+        if (got <= 0) {
+          ok = got == 0;
+          break;
+        }
+        if (u.nsteps == 0) continue;
+        const int kb = ru % KVB;
+        // The claim comes a few steps before the buffer frees: bring the
+        // tiles into L2 now, so that the load at the boundary is short.
+        if (lane == 0 && ru >= KVB) {
+          tma_prefetch_l2_2d(&p.tm_k, u.g * D, u.sp.start + u.k0);
+          tma_prefetch_l2_2d(&p.tm_v, u.g * D, u.sp.start + u.k0);
+        }
+        if (ru >= KVB && !(ok = mbar_wait_warp(b_kve(kb), ((ru / KVB) - 1) & 1, ab))) break;
+        if (lane == 0) {
+          mbar_expect_tx(b_kvf(kb), 2 * TILE);
+          tma_load_2d(sb + L::OFF_K + 2 * kb * TILE, &p.tm_k, u.g * D, u.sp.start + u.k0, b_kvf(kb));
+          tma_load_2d(sb + L::OFF_V + 2 * kb * TILE, &p.tm_v, u.g * D, u.sp.start + u.k0, b_kvf(kb));
+        }
+        ++ru;
+      }
+      if (lane == 0 && abort_flag)
+        for (int m = max(0, ru - KVB); m < ru; ++m) wait_drain(b_kvf(m % KVB), (m / KVB) & 1);
     } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs this code so every descriptor is warp-uniform; one
-    // elected lane issues the MMAs and the commits that track them.
-    {
+      // ------------------------------------------------------------ MMA issuer
+      // The whole warp runs this code so every descriptor is warp-uniform; one
+      // elected lane issues the MMAs and the commits that track them.
       const bool leader = elect_one();
       const uint32_t id_s = idesc_bf16(BN, HALF, false, false);  // S_h^T, dP_h^T: 128 keys x 64 queries
       const uint32_t id_kv = idesc_bf16(BN, D, false, true);     // dV, dK: 128 keys x 64
       const uint32_t id_q = idesc_bf16(BM, D, true, true);       // dQ: 128 queries x 64
-      const uint64_t d_k = sdesc_sw128(sb + OFF_K, 16, 1024);    // MN-major B of dQ
-      const uint64_t d_q = sdesc_sw128(sb + OFF_Q, 16, 1024);    // stage s: + s * TILE, half h: + h * 8 KB
-      const uint64_t d_o = sdesc_sw128(sb + OFF_DO, 16, 1024);
-      const uint64_t d_dsm = sdesc_sw128(sb + OFF_DS, TILE, 1024);  // MN-major A of dQ (two 64-query blocks)
+      const uint64_t d_k = sdesc_sw128(sb + L::OFF_K, 16, 1024);   // MN-major B of dQ; buffer b: + 2 b TILE
+      const uint64_t d_q = sdesc_sw128(sb + L::OFF_Q, 16, 1024);   // stage s: + s * TILE, half h: + h * 8 KB
+      const uint64_t d_o = sdesc_sw128(sb + L::OFF_DO, 16, 1024);
+      const uint64_t d_dsm = sdesc_sw128(sb + L::OFF_DS, TILE, 1024);  // MN-major A of dQ (two 64-query blocks)
       // S_h^T = K Q_h^T and dP_h^T = V dO_h^T of the step held in stage s
       // (A = K or V in Tensor Memory, B = the half's 64 query rows, K-major).
       // Bias product first (overwrites): a selector tile times the stage's
       // bias rows of the half adds -l'/scale to S^T and -D to dP^T.
       auto bias_desc = [&](int h, int s) {
-        const uint32_t off = OFF_BIAS + (s * BM + h * HALF) * 16;
-        return sdesc_nosw(sb + off, OFF_ZERO - off, 128);
+        const uint32_t off = L::OFF_BIAS + (s * BM + h * HALF) * 16;
+        return sdesc_nosw(sb + off, L::OFF_ZERO - off, 128);
       };
-      const uint64_t d_sel_s = sdesc_nosw(sb + OFF_SEL, OFF_ZERO - OFF_SEL, 128);
-      const uint64_t d_sel_dp = sdesc_nosw(sb + OFF_SEL + BN * 16, OFF_ZERO - (OFF_SEL + BN * 16), 128);
+      const uint64_t d_sel_s = sdesc_nosw(sb + L::OFF_SEL, L::OFF_ZERO - L::OFF_SEL, 128);
+      const uint64_t d_sel_dp =
+          sdesc_nosw(sb + L::OFF_SEL + BN * 16, L::OFF_ZERO - (L::OFF_SEL + BN * 16), 128);
       auto issue_s = [&](int h, int s) {
         const uint64_t q = sdesc_add(d_q, s * TILE + h * HALF * 128);
         if (leader) mma_ss(tmem + TM_S + HALF * h, d_sel_s, bias_desc(h, s), id_s, 0);
@@ -355,170 +523,190 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
         for (int kk = 0; kk < D / 16; ++kk)
           if (leader) mma_ts(tmem + TM_DP + HALF * h, tmem + TM_V + kk * 8, sdesc_add(o, kk * 32), id_s, 1);
       };
-      bool ok = mbar_wait_warp(b_kvt, 0, ab) && mbar_wait_warp(b_qf(0), 0, ab);
-      if (ok) {
+      bool ok = true;
+      int n = 0, ru = 0;
+      Unit u;
+      for (int r = 0; ok; ++r) {
+        const int got = take(r, u);
+        if (got <= 0) {
+          ok = got == 0;
+          break;
+        }
+        if (u.nsteps == 0) continue;
+        const int kb = ru % KVB;
+        // K and V of the unit are in TMEM (the element-wise warps copied them
+        // after their TMA landed, which this wait also acquires), and the
+        // first stage of the unit has landed.
+        if (!(ok = mbar_wait_warp(b_kvt, ru & 1, ab) && mbar_wait_warp(b_kvf(kb), (ru / KVB) & 1, ab) &&
+                   mbar_wait_warp(b_qf(n % NS), (n / NS) & 1, ab)))
+          break;
         fence_after_sync();
         for (int h = 0; h < 2; ++h) {
-          issue_s(h, 0);
+          issue_s(h, n % NS);
           if (leader) mma_commit(b_s(h));
         }
         for (int h = 0; h < 2; ++h) {
-          issue_dp(h, 0);
+          issue_dp(h, n % NS);
           if (leader) mma_commit(b_dp(h));
         }
-      }
-      for (int t = 0; ok && t < nsteps; ++t) {
-        const int s = t % NS, db = t & 1;
-        const bool more = t + 1 < nsteps;
-        // Phase 1 of each half is done (packed P^T in the S^T columns):
-        // dV += P_h^T dO_h, then the next step's S_h^T over those columns
-        // (the tensor core runs MMAs in issue order).
-        for (int h = 0; h < 2 && ok; ++h) {
-          if (!(ok = mbar_wait_warp(b_pt(h), t & 1, ab))) break;
-          fence_after_sync();
-          const uint64_t o = sdesc_add(d_o, s * TILE + h * HALF * 128);
+        const uint64_t dk_b = sdesc_add(d_k, 2 * kb * TILE);
+        for (int t = 0; ok && t < u.nsteps; ++t, ++n) {
+          const int s = n % NS, db = n & 1;
+          const bool more = t + 1 < u.nsteps;
+          // Phase 1 of each half is done (packed P^T in the S^T columns):
+          // dV += P_h^T dO_h, then the next step's S_h^T over those columns
+          // (the tensor core runs MMAs in issue order).
+          for (int h = 0; h < 2 && ok; ++h) {
+            if (!(ok = mbar_wait_warp(b_pt(h), n & 1, ab))) break;
+            // The first dV product overwrites dV: the previous unit's dK, dV
+            // must have left Tensor Memory.
+            if (t == 0 && h == 0 && ru > 0 && !(ok = mbar_wait_warp(b_dkv, (ru - 1) & 1, ab))) break;
+            fence_after_sync();
+            const uint64_t o = sdesc_add(d_o, s * TILE + h * HALF * 128);
 #pragma unroll
-          for (int kk = 0; kk < HALF / 16; ++kk)
-            if (leader)
-              mma_ts(tmem + TM_DV, tmem + TM_S + HALF * h + kk * 8, sdesc_add(o, kk * 2048), id_kv,
-                     (t > 0 || h > 0 || kk > 0) ? 1u : 0u);
-          if (more) {
-            if (h == 0) {
-              if (!(ok = mbar_wait_warp(b_qf((t + 1) % NS), ((t + 1) / NS) & 1, ab))) break;
-              fence_after_sync();
+            for (int kk = 0; kk < HALF / 16; ++kk)
+              if (leader)
+                mma_ts(tmem + TM_DV, tmem + TM_S + HALF * h + kk * 8, sdesc_add(o, kk * 2048), id_kv,
+                       (t > 0 || h > 0 || kk > 0) ? 1u : 0u);
+            if (more) {
+              if (h == 0) {
+                if (!(ok = mbar_wait_warp(b_qf((n + 1) % NS), ((n + 1) / NS) & 1, ab))) break;
+                fence_after_sync();
+              }
+              issue_s(h, (n + 1) % NS);
+              if (leader) mma_commit(b_s(h));
             }
-            issue_s(h, (t + 1) % NS);
-            if (leader) mma_commit(b_s(h));
           }
+          if (!ok) break;
+          // Phase 2 of each half is done (packed dS^T in the dP^T columns):
+          // dK += dS_h^T Q_h, then the next step's dP_h^T over those columns.
+          for (int h = 0; h < 2 && ok; ++h) {
+            if (!(ok = mbar_wait_warp(b_ds(h), n & 1, ab))) break;
+            fence_after_sync();
+            const uint64_t q = sdesc_add(d_q, s * TILE + h * HALF * 128);
+#pragma unroll
+            for (int kk = 0; kk < HALF / 16; ++kk)
+              if (leader)
+                mma_ts(tmem + TM_DK, tmem + TM_DP + HALF * h + kk * 8, sdesc_add(q, kk * 2048), id_kv,
+                       (t > 0 || h > 0 || kk > 0) ? 1u : 0u);
+            if (more) {
+              issue_dp(h, (n + 1) % NS);
+              if (leader) mma_commit(b_dp(h));
+            }
+          }
+          if (!ok) break;
+          if (leader) mma_commit(b_qe(s));  // Q(n), dO(n), l'(n), D(n) have no later reader
+          if (n > 0) {
+            if (!(ok = mbar_wait_warp(b_dqe, (n - 1) & 1, ab))) break;
+            fence_after_sync();
+          }
+          const uint64_t dsm = sdesc_add(d_dsm, db * 2 * TILE);
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            if (leader) mma_ss(tmem + TM_DQ, sdesc_add(dsm, kk * 2048), sdesc_add(dk_b, kk * 2048), id_q, kk > 0);
+          if (leader) mma_commit(b_dqf);
         }
         if (!ok) break;
-        // Phase 2 of each half is done (packed dS^T in the dP^T columns):
-        // dK += dS_h^T Q_h, then the next step's dP_h^T over those columns.
-        for (int h = 0; h < 2 && ok; ++h) {
-          if (!(ok = mbar_wait_warp(b_ds(h), t & 1, ab))) break;
-          fence_after_sync();
-          const uint64_t q = sdesc_add(d_q, s * TILE + h * HALF * 128);
-#pragma unroll
-          for (int kk = 0; kk < HALF / 16; ++kk)
-            if (leader)
-              mma_ts(tmem + TM_DK, tmem + TM_DP + HALF * h + kk * 8, sdesc_add(q, kk * 2048), id_kv,
-                     (t > 0 || h > 0 || kk > 0) ? 1u : 0u);
-          if (more) {
-            issue_dp(h, (t + 1) % NS);
-            if (leader) mma_commit(b_dp(h));
-          }
+        // Every MMA of the unit: dK, dV are final and the K/V buffer is free.
+        if (leader) {
+          mma_commit(b_done);
+          mma_commit(b_kve(kb));
         }
-        if (!ok) break;
-        if (leader) mma_commit(b_qe(s));  // Q(t), dO(t), l'(t), D(t) have no later reader
-        if (t > 0) {
-          if (!(ok = mbar_wait_warp(b_dqe, (t - 1) & 1, ab))) break;
-          fence_after_sync();
-        }
-        const uint64_t dsm = sdesc_add(d_dsm, db * 2 * TILE);
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          if (leader) mma_ss(tmem + TM_DQ, sdesc_add(dsm, kk * 2048), sdesc_add(d_k, kk * 2048), id_q, kk > 0);
-        if (leader) mma_commit(b_dqf);
+        ++ru;
       }
-      if (ok && leader) mma_commit(b_done);
       if (leader) mma_commit(b_dr);
       __syncwarp();
       wait_drain(b_dr, 0);
-    }
     }
   } else if (warp < 12) {
     // ------------------------------------------------------------ element-wise
     regs_inc<REGS_EW>();
     const int half = (warp - 4) >> 2;  // query rows [64 * half, 64 * half + 64) of each step
     const int kr = (warp & 3) * 32 + lane;
-    const int key = k0 + kr;
     const uint32_t lb = lane_base(warp);
     const uint32_t tS = tmem + TM_S + HALF * half + lb, tDP = tmem + TM_DP + HALF * half + lb;
+    const uint32_t tKV = tmem + (half ? TM_V : TM_K) + lb;
+    const uint32_t tAcc = tmem + (half ? TM_DK : TM_DV) + lb;
     const float sl2 = p.scale_log2;
-    bool ok = mbar_wait_warp(b_kv, 0, ab);
-    if (ok) {
-      // Copy this thread's row of K (first half) or V (second half) into TMEM,
-      // where it is the A operand of S^T = K Q^T / dP^T = V dO^T.
-      const uint32_t src = sb + (half ? OFF_V : OFF_K) + kr * 128;
-      uint32_t r[32];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 v = ld_shared_v4(src + ((c ^ (kr & 7)) << 4));
-        r[4 * c] = v.x, r[4 * c + 1] = v.y, r[4 * c + 2] = v.z, r[4 * c + 3] = v.w;
-      }
-      tmem_st32(tmem + (half ? TM_V : TM_K) + lb, r);
-      tmem_st_wait();
-      fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_kvt);
-    }
-    for (int t = 0; ok && t < nsteps; ++t) {
-      ok = mbar_wait_warp(b_s(half), t & 1, ab);
-      if (!ok) break;
-      fence_after_sync();
-      const int qh = step_q0(t) + HALF * half;
-      const bool full = block_full(qh, HALF, k0, BN, sp.len, p.mask);
-      const uint32_t rowb = sb + OFF_DS + (t & 1) * 2 * TILE + half * TILE + kr * 128;
-      float pv[4][16];
-      if (full)
-        ew_phase1<true>(tS, sl2, qh, key, sp.len, p.mask, pv);
-      else
-        ew_phase1<false>(tS, sl2, qh, key, sp.len, p.mask, pv);
-      tmem_st_wait();
-      fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_pt(half));
-      if (!(ok = mbar_wait_warp(b_dp(half), t & 1, ab))) break;
-      fence_after_sync();
-      ew_phase2(tDP, rowb, kr, pv);
-      tmem_st_wait();
-      fence_before_sync();
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_ds(half));
-    }
-    ok = ok && mbar_wait_warp(b_done, 0, ab);
-    if (ok) {
-      // First warpgroup writes dV, second writes dK (scaled).
+    bool ok = true;
+    int n = 0, ru = 0;
+    Unit u, prev;
+    // Reads the finished unit number `idx` (its dV / dK) out of TMEM,
+    // releases the columns to the next unit's products, writes it.
+    auto drain_unit = [&](const Unit& done, int idx) -> bool {
+      if (!mbar_wait_warp(b_done, idx & 1, ab)) return false;
       fence_after_sync();
       uint32_t a[32], b2[32];
-      const uint32_t src = tmem + (half ? TM_DK : TM_DV) + lb;
-      tmem_ld32(src, a);
-      tmem_ld32(src + 32, b2);
+      tmem_ld32(tAcc, a);
+      tmem_ld32(tAcc + 32, b2);
       tmem_ld_wait();
       reg_fence32(a);
       reg_fence32(b2);
-      const float mul = half ? p.scale : 1.f;
-      if (split) {
-        // Partial sums of one chunk of a split tile: this thread's key row of
-        // the chunk's own slot (rows past the sequence end are written too and
-        // never read).
-        float4* dst = reinterpret_cast<float4*>(
-            p.dkv_acc + ((static_cast<size_t>(item.slot) * p.hkv + g) * 2 + half) * (BN * D) + kr * D);
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          dst[c] = make_float4(__uint_as_float(a[4 * c]), __uint_as_float(a[4 * c + 1]),
-                               __uint_as_float(a[4 * c + 2]), __uint_as_float(a[4 * c + 3]));
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          dst[8 + c] = make_float4(__uint_as_float(b2[4 * c]), __uint_as_float(b2[4 * c + 1]),
-                                   __uint_as_float(b2[4 * c + 2]), __uint_as_float(b2[4 * c + 3]));
-      } else if (key < sp.len) {
-        __nv_bfloat16* dst = (half ? p.dk : p.dv) + (static_cast<size_t>(sp.start + key) * p.hkv + g) * D;
-        uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          d4[c] = make_uint4(pack_bf16(__uint_as_float(a[8 * c]) * mul, __uint_as_float(a[8 * c + 1]) * mul),
-                             pack_bf16(__uint_as_float(a[8 * c + 2]) * mul, __uint_as_float(a[8 * c + 3]) * mul),
-                             pack_bf16(__uint_as_float(a[8 * c + 4]) * mul, __uint_as_float(a[8 * c + 5]) * mul),
-                             pack_bf16(__uint_as_float(a[8 * c + 6]) * mul, __uint_as_float(a[8 * c + 7]) * mul));
-          d4[4 + c] = make_uint4(pack_bf16(__uint_as_float(b2[8 * c]) * mul, __uint_as_float(b2[8 * c + 1]) * mul),
-                                 pack_bf16(__uint_as_float(b2[8 * c + 2]) * mul, __uint_as_float(b2[8 * c + 3]) * mul),
-                                 pack_bf16(__uint_as_float(b2[8 * c + 4]) * mul, __uint_as_float(b2[8 * c + 5]) * mul),
-                                 pack_bf16(__uint_as_float(b2[8 * c + 6]) * mul, __uint_as_float(b2[8 * c + 7]) * mul));
-        }
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_dkv);
+      write_dkv(p, done, half, kr, a, b2);
+      return true;
+    };
+    for (int r = 0; ok; ++r) {
+      const int got = take(r, u);
+      if (got <= 0) {
+        ok = got == 0;
+        break;
       }
+      if (u.nsteps == 0) continue;
+      const int kb = ru % KVB;
+      if (!(ok = mbar_wait_warp(b_kvf(kb), (ru / KVB) & 1, ab))) break;
+      {
+        // This thread's row of K (first half) or V (second half) into TMEM,
+        // where it is the A operand of S^T = K Q^T / dP^T = V dO^T.  The
+        // previous unit's products that read these columns have completed:
+        // their results were consumed by this warpgroup's last phase.
+        const uint32_t src = sb + (half ? L::OFF_V : L::OFF_K) + 2 * kb * TILE + kr * 128;
+        uint32_t rr[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = ld_shared_v4(src + ((c ^ (kr & 7)) << 4));
+          rr[4 * c] = v.x, rr[4 * c + 1] = v.y, rr[4 * c + 2] = v.z, rr[4 * c + 3] = v.w;
+        }
+        tmem_st32(tKV, rr);
+        tmem_st_wait();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_kvt);
+      }
+      if (ru > 0 && !(ok = drain_unit(prev, ru - 1))) break;
+      for (int t = 0; t < u.nsteps; ++t, ++n) {
+        if (!(ok = mbar_wait_warp(b_s(half), n & 1, ab))) break;
+        fence_after_sync();
+        const int qh = step_q0(u, t) + HALF * half;
+        const bool full = block_full(qh, HALF, u.k0, BN, u.sp.len, p.mask);
+        const uint32_t rowb = sb + L::OFF_DS + (n & 1) * 2 * TILE + half * TILE + kr * 128;
+        float pv[4][16];
+        if (full) {
+          ew_phase1<true>(tS, sl2, 0u, 0u, pv);
+        } else {
+          const int key = u.k0 + kr;
+          ew_phase1<false>(tS, sl2, query_bits(key, qh, u.sp.len, p.mask), query_bits(key, qh + 32, u.sp.len, p.mask),
+                           pv);
+        }
+        tmem_st_wait();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_pt(half));
+        if (!(ok = mbar_wait_warp(b_dp(half), n & 1, ab))) break;
+        fence_after_sync();
+        ew_phase2(tDP, rowb, kr, pv);
+        tmem_st_wait();
+        fence_before_sync();
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_ds(half));
+      }
+      prev = u;
+      ++ru;
     }
+    if (ok && ru > 0) drain_unit(prev, ru - 1);
   } else {
     // ------------------------------------------------------------ dQ drain
     regs_dec<REGS_DQ>();
@@ -526,51 +714,59 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
     const bool leader = (warp == 12 && lane == 0);
     const uint32_t lb = lane_base(warp);
     const uint32_t tQ = tmem + TM_DQ + lb;
-    const uint32_t stg = sb + OFF_STG;
+    const uint32_t stg = sb + L::OFF_STG;
     bool ok = true;
-    for (int t = 0; t < nsteps; ++t) {
-      ok = mbar_wait_warp(b_dqf, t & 1, ab);
-      if (!ok) break;
-      fence_after_sync();
-      uint32_t a[32], b2[32];
-      tmem_ld32(tQ, a);
-      tmem_ld32(tQ + 32, b2);
-      tmem_ld_wait();
-      reg_fence32(a);
-      reg_fence32(b2);
-      fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_dqe);
-      const int h = step_head(t), q0 = step_q0(t);
-      const bool valid = q0 + qr < sp.len;
-      if (leader) bulk_wait_read0();
-      named_sync(1, 128);
-      // Columns 0-31, then 32-63, through the one 16 KB staging tile.
+    int n = 0;
+    Unit u;
+    for (int r = 0; ok; ++r) {
+      const int got = take(r, u);
+      if (got <= 0) {
+        ok = got == 0;
+        break;
+      }
+      for (int t = 0; t < u.nsteps; ++t, ++n) {
+        if (!(ok = mbar_wait_warp(b_dqf, n & 1, ab))) break;
+        fence_after_sync();
+        uint32_t a[32], b2[32];
+        tmem_ld32(tQ, a);
+        tmem_ld32(tQ + 32, b2);
+        tmem_ld_wait();
+        reg_fence32(a);
+        reg_fence32(b2);
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_dqe);
+        const int h = step_head(p, u, t), q0 = step_q0(u, t);
+        const bool valid = q0 + qr < u.sp.len;
+        if (leader) bulk_wait_read0();
+        named_sync(1, 128);
+        // Columns 0-31, then 32-63, through the one 16 KB staging tile.
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t sw = ((i ^ (qr & 7)) << 4) + qr * 128;
-        st_shared_v4(stg + sw, valid ? a[4 * i] : 0u, valid ? a[4 * i + 1] : 0u, valid ? a[4 * i + 2] : 0u,
-                     valid ? a[4 * i + 3] : 0u);
-      }
-      fence_async_smem();
-      named_sync(1, 128);
-      if (leader) {
-        tma_reduce_add_2d(&p.tm_dq, h * D, sp.start + q0, stg);
-        bulk_commit();
-        bulk_wait_read0();
-      }
-      named_sync(1, 128);
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t sw = ((i ^ (qr & 7)) << 4) + qr * 128;
+          st_shared_v4(stg + sw, valid ? a[4 * i] : 0u, valid ? a[4 * i + 1] : 0u, valid ? a[4 * i + 2] : 0u,
+                       valid ? a[4 * i + 3] : 0u);
+        }
+        fence_async_smem();
+        named_sync(1, 128);
+        if (leader) {
+          tma_reduce_add_2d(&p.tm_dq, h * D, u.sp.start + q0, stg);
+          bulk_commit();
+          bulk_wait_read0();
+        }
+        named_sync(1, 128);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t sw = ((i ^ (qr & 7)) << 4) + qr * 128;
-        st_shared_v4(stg + sw, valid ? b2[4 * i] : 0u, valid ? b2[4 * i + 1] : 0u, valid ? b2[4 * i + 2] : 0u,
-                     valid ? b2[4 * i + 3] : 0u);
-      }
-      fence_async_smem();
-      named_sync(1, 128);
-      if (leader) {
-        tma_reduce_add_2d(&p.tm_dq, h * D + 32, sp.start + q0, stg);
-        bulk_commit();
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t sw = ((i ^ (qr & 7)) << 4) + qr * 128;
+          st_shared_v4(stg + sw, valid ? b2[4 * i] : 0u, valid ? b2[4 * i + 1] : 0u, valid ? b2[4 * i + 2] : 0u,
+                       valid ? b2[4 * i + 3] : 0u);
+        }
+        fence_async_smem();
+        named_sync(1, 128);
+        if (leader) {
+          tma_reduce_add_2d(&p.tm_dq, h * D + 32, u.sp.start + q0, stg);
+          bulk_commit();
+        }
       }
     }
     if (leader) bulk_wait0();
@@ -657,14 +853,31 @@ size_t bwd_split_acc_bytes(const Problem& pr) {
   return static_cast<size_t>(slots) * pr.hkv * 2 * BN * D * sizeof(float);
 }
 
+int bwd_tc_main_slices(const Problem& pr) {
+  if (pr.num_seqs == 0 || pr.total_tokens == 0 || pr.seqlen == 0) return 0;
+  return static_cast<int>((bwd_work_list(pr, bwd_qchunk(pr)).size() + kMaxItems - 1) / kMaxItems);
+}
+
 int bwd_tc_main_launches(const Problem& pr) {
   if (pr.num_seqs == 0 || pr.total_tokens == 0 || pr.seqlen == 0) return 0;
   const std::vector<BwdItem> items = bwd_work_list(pr, bwd_qchunk(pr));
-  constexpr size_t kMax = sizeof(BwdTcK::items) / sizeof(BwdTcK::items[0]);
   constexpr size_t kMaxTiles = sizeof(DkvConvK::tiles) / sizeof(DkvConvK::tiles[0]);
   const size_t n_split = split_tiles(items).size();
-  return static_cast<int>((items.size() + kMax - 1) / kMax + (n_split + kMaxTiles - 1) / kMaxTiles);
+  return static_cast<int>((items.size() + kMaxItems - 1) / kMaxItems + (n_split + kMaxTiles - 1) / kMaxTiles);
 }
+
+namespace {
+
+template <int NS, int KVB>
+cudaError_t launch_main(const BwdTcK& k, int grid, cudaStream_t stream) {
+  constexpr int smem = Layout<NS, KVB>::SMEM_DYN;
+  cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<NS, KVB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  bwd_tc_kernel<NS, KVB><<<grid, NTHR, smem, stream>>>(k);
+  return cudaGetLastError();
+}
+
+}  // namespace
 
 cudaError_t launch_bwd_tc_main(const Problem& pr, const BwdArgs& a, int* status, cudaStream_t stream) {
   if (pr.num_seqs == 0 || pr.total_tokens == 0 || pr.seqlen == 0) return cudaSuccess;
@@ -693,18 +906,18 @@ cudaError_t launch_bwd_tc_main(const Problem& pr, const BwdArgs& a, int* status,
   const std::vector<BwdItem> items = bwd_work_list(pr, k.qchunk);
   const std::vector<DkvTile> tiles = split_tiles(items);
   if (!tiles.empty() && a.dkv_acc == nullptr) return cudaErrorInvalidValue;
+  const int sms = device_sms();
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_DYN)) !=
-      cudaSuccess)
-    return e;
-  constexpr int kMax = static_cast<int>(sizeof(k.items) / sizeof(k.items[0]));
   if ((e = prof_begin(g_prof_bwd, stream)) != cudaSuccess) return e;
-  for (size_t first = 0; first < items.size(); first += kMax) {
-    const int n = static_cast<int>(std::min<size_t>(kMax, items.size() - first));
+  for (size_t first = 0; first < items.size(); first += kMaxItems) {
+    const int n = static_cast<int>(std::min<size_t>(kMaxItems, items.size() - first));
     std::copy(items.begin() + first, items.begin() + first + n, k.items);
     k.n_items = n;
-    bwd_tc_kernel<<<dim3(pr.hkv, n), NTHR, SMEM_DYN, stream>>>(k);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    k.n_units = n * pr.hkv;
+    k.unit_counter = a.unit_counters + first / kMaxItems;
+    const int grid = std::min(sms, k.n_units);
+    e = launch_main<3, 1>(k, grid, stream);
+    if (e != cudaSuccess) return e;
   }
   if ((e = prof_end(g_prof_bwd, stream)) != cudaSuccess) return e;
   if (!tiles.empty()) {

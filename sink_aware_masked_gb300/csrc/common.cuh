@@ -92,6 +92,18 @@ SA_DEV uint32_t visible_bits(int q, int kbase, int len, const MaskParams& m) {
   return r;
 }
 
+// visible(qbase + e, key, len, m) and qbase + e < len for e = 0..31 as a bit
+// mask: the queries that see one key form a single interval, from the key
+// itself (causal) up to the sequence end or, for a key outside the prefix,
+// key + w.
+SA_DEV uint32_t query_bits(int key, int qbase, int len, const MaskParams& m) {
+  if (key >= len) return 0u;
+  const int lo = m.causal ? key - qbase : -64;
+  int hi = len - 1 - qbase;
+  if (m.window >= 0 && key >= m.prefix) hi = min(hi, key + m.window - qbase);
+  return bits_below(hi + 1) & ~bits_below(lo);
+}
+
 // ---------------------------------------------------------------- PTX helpers
 SA_DEV uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 

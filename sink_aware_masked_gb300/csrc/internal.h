@@ -54,6 +54,8 @@ struct BwdArgs {
   void* bias;
   float* dsink_part;  // [preprocess blocks, Hq]
   float* dkv_acc;     // fp32 dK/dV partial sums of split key tiles, one slot per chunk (or nullptr)
+  int* unit_counters; // one claim counter per main-kernel launch, cleared by the preprocess kernel
+  int n_unit_counters;
   int preprocess_blocks;
 };
 
@@ -147,6 +149,7 @@ cudaError_t launch_fwd_tc(const Problem& p, const FwdArgs& a, int* status, cudaS
 // Kernel launches launch_fwd_tc / launch_bwd_tc_main make for a problem (host arithmetic).
 int fwd_tc_launches(const Problem& p);
 int bwd_tc_main_launches(const Problem& p);
+int bwd_tc_main_slices(const Problem& p);  // launches of the main kernel itself (work-list slices)
 cudaError_t launch_bwd(const Problem& p, const BwdArgs& a, int* status, cudaStream_t s);
 cudaError_t launch_bwd_tc_main(const Problem& p, const BwdArgs& a, int* status, cudaStream_t s);
 size_t bwd_split_acc_bytes(const Problem& p);

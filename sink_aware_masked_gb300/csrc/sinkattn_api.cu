@@ -113,18 +113,24 @@ __global__ void selftest_wait_kernel(int* status, long long limit) {
 }
 
 struct BwdLayout {
-  size_t dq_accum, bias, part, dkv, total;
-  int pre_blocks;
+  size_t dq_accum, bias, part, counters, dkv, total;
+  int pre_blocks, n_counters;
 };
 
+// Backward workspace: fp32 dQ accumulator [T, Hq, 64], bias rows [Hq, T]
+// (16 bytes), dsink partial sums [preprocess blocks, Hq], the main kernel's
+// unit-claim counters (one int per launch), then the per-chunk dK/dV slots of
+// split key tiles.  Every part starts at a 256-byte boundary.
 BwdLayout bwd_layout(const sa::Problem& p) {
   BwdLayout l;
   const size_t T = static_cast<size_t>(p.total_tokens), H = static_cast<size_t>(p.hq);
   l.pre_blocks = sa::ceil_div(p.total_tokens, sa::kPreTokens);
+  l.n_counters = sa::bwd_tc_main_slices(p);
   l.dq_accum = 0;
   l.bias = l.dq_accum + round_up(T * H * sa::kHeadDim * 4, 256);
   l.part = l.bias + round_up(T * H * 16, 256);
-  l.dkv = l.part + round_up(static_cast<size_t>(l.pre_blocks) * H * 4, 256);
+  l.counters = l.part + round_up(static_cast<size_t>(l.pre_blocks) * H * 4, 256);
+  l.dkv = l.counters + round_up(static_cast<size_t>(l.n_counters) * 4, 256);
   l.total = l.dkv + round_up(sa::bwd_split_acc_bytes(p), 256) + 256;
   return l;
 }
@@ -208,6 +214,8 @@ sinkattn_status sinkattn_bwd(const sinkattn_problem* prob, const void* q, const 
   a.bias = ws + L.bias;
   a.dsink_part = reinterpret_cast<float*>(ws + L.part);
   a.dkv_acc = sa::bwd_split_acc_bytes(p) ? reinterpret_cast<float*>(ws + L.dkv) : nullptr;
+  a.unit_counters = reinterpret_cast<int*>(ws + L.counters);
+  a.n_unit_counters = L.n_counters;
   a.preprocess_blocks = L.pre_blocks;
   int* status = status_word();
   if (status == nullptr) return SINKATTN_ERR_CUDA;

@@ -106,6 +106,14 @@ SA_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, ui
       : "memory");
 }
 
+// Brings a tile into L2 ahead of its load (no shared memory, no barrier).
+SA_DEV void tma_prefetch_l2_2d(const CUtensorMap* map, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+
 // Contiguous bulk copy global -> shared on the TMA unit, completing on `bar`
 // (both addresses 16-byte aligned, bytes a multiple of 16).
 SA_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {

@@ -246,8 +246,11 @@ def test_peak_memory_linear_in_sequence_length():
         torch.cuda.synchronize()
         peaks.append(torch.cuda.max_memory_allocated() - base)
     d = np.diff(peaks) / np.diff([2048, 4096, 8192, 16384])
-    # Bytes per extra token stay constant (no S^2 term).  torch's caching
-    # allocator rounds large blocks up to 2 MiB, which moves the smallest case
-    # by a few percent; an S x S buffer of even one head would double the
-    # slope between the last two sizes.
-    assert np.max(d) / np.min(d) < 1.15, peaks
+    # Bytes per extra token never grow (no S^2 term): an S x S buffer of even
+    # one head would double the slope between the last two sizes.  The slope
+    # may shrink: the per-chunk dK/dV slots of split key tiles are a bounded
+    # term on top of the linear buffers, and fewer tiles split as S grows.
+    # torch's caching allocator rounds large blocks up to 2 MiB, which moves
+    # the smallest case by a few percent.
+    assert np.all(d[1:] <= 1.15 * d[:-1]), peaks
+    assert peaks[-1] <= 16384 * 16 * 2048, peaks  # well under 2 KB per token and head
