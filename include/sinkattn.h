@@ -111,8 +111,12 @@ sinkattn_status sinkattn_fwd(const sinkattn_problem* prob,
  * dsink[h] = -sum over all rows of (1 - alpha_q) * <dout_q, o_q>.
  * The workspace holds an fp32 dQ accumulator [T, Hq, 64], one 16-byte row
  * per (head, token) with the per-row terms -D and -l'/scale, where
- * l' = l + softplus(sink - l), as three bf16 summands each ([Hq, T]), and
- * per-block partial sums of dsink. */
+ * l' = l + softplus(sink - l), as three bf16 summands each ([Hq, T]),
+ * per-block partial sums of dsink, and, when key tiles are split over
+ * several work items, per-chunk dK/dV partial sums.
+ * Its contents on entry do not matter (the call clears what it accumulates
+ * into).  dK, dV and dsink are bitwise reproducible run to run; dQ is summed
+ * in arrival order and reproducible to fp32 rounding. */
 sinkattn_status sinkattn_bwd(const sinkattn_problem* prob,
                              const void* q, const void* k, const void* v, const void* o,
                              const float* lse, const void* dout, const float* sink,

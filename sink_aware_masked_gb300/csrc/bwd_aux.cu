@@ -11,7 +11,9 @@
 //   bwd_pre   : one pass over O and dO: the bias rows (-l'/scale and -D as
 //               bf16 hi/mid/lo triples) the main kernel folds into its S^T and
 //               dP^T MMAs, per-block partial dsink sums, zeroes the fp32 dQ
-//               accumulator and the main kernel's unit-claim counters.
+//               accumulator (which also brings it into L2 for the main
+//               kernel's reduce-adds when it fits) and the main kernel's
+//               unit-claim counters.
 //               HBM-bound; every thread issues the loads of four tokens
 //               before using them.
 //   dq_convert: dQ = scale * accumulator -> bf16; ceil(Hq / 8) extra blocks
@@ -202,8 +204,8 @@ cudaError_t launch_bwd(const Problem& pr, const BwdArgs& a, int* status, cudaStr
   const long long T = pr.total_tokens;
   {
     PreK k{static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.sink,
-           static_cast<uint4*>(a.bias), a.dq_accum, a.dsink_part, a.unit_counters, a.n_unit_counters, T, pr.hq,
-           pr.scale};
+           static_cast<uint4*>(a.bias), a.dq_accum, a.dsink_part, a.unit_counters, a.n_unit_counters,
+           T, pr.hq, pr.scale};
     if (a.preprocess_blocks > 0) bwd_pre_kernel<<<a.preprocess_blocks, 256, 0, stream>>>(k);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -719,13 +719,16 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
     int n = 0;
     Unit u;
     for (int r = 0; ok; ++r) {
+      // The four drain warps decide together: they meet at named barriers,
+      // so none may leave the loop while the others go on.
       const int got = take(r, u);
-      if (got <= 0) {
-        ok = got == 0;
+      if (!named_sync_and(1, 128, got >= 0)) {
+        ok = false;
         break;
       }
+      if (got == 0) break;
       for (int t = 0; t < u.nsteps; ++t, ++n) {
-        if (!(ok = mbar_wait_warp(b_dqf, n & 1, ab))) break;
+        if (!(ok = named_sync_and(1, 128, mbar_wait_warp(b_dqf, n & 1, ab)))) break;
         fence_after_sync();
         uint32_t a[32], b2[32];
         tmem_ld32(tQ, a);

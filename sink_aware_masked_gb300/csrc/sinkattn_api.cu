@@ -120,7 +120,9 @@ struct BwdLayout {
 // Backward workspace: fp32 dQ accumulator [T, Hq, 64], bias rows [Hq, T]
 // (16 bytes), dsink partial sums [preprocess blocks, Hq], the main kernel's
 // unit-claim counters (one int per launch), then the per-chunk dK/dV slots of
-// split key tiles.  Every part starts at a 256-byte boundary.
+// split key tiles.  Every part starts at a 256-byte boundary.  Nothing needs
+// to be zero on entry: the preprocess kernel clears the accumulator and the
+// counters.
 BwdLayout bwd_layout(const sa::Problem& p) {
   BwdLayout l;
   const size_t T = static_cast<size_t>(p.total_tokens), H = static_cast<size_t>(p.hq);

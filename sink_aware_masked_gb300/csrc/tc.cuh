@@ -154,6 +154,19 @@ SA_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;\n
 // Wait until every committed bulk group has completed.
 SA_DEV void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
 
+// Named barrier over `n` threads that also returns whether `v` holds for all
+// of them: a group that decides together after a bounded wait leaves (or
+// stays) together, so none of its threads is left at a later barrier.
+SA_DEV bool named_sync_and(int id, int n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, %2, %3, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
 // Named barrier over `n` threads (id 1..15; id 0 is __syncthreads).
 SA_DEV void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory"); }
 

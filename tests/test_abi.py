@@ -280,6 +280,7 @@ def test_grpo_workspace_layout(lib, total):
     ("causal_gqa_s4096", 1, 4),                 # + the dK/dV conversion of split key tiles
     ("window128_prefix4_gqa_b2_s8192", 1, 4),   # the always-visible prefix tiles are split
     ("window128_gqa_s4096", 1, 3),
+    ("varlen8_causal", 1, 3),
 ])
 def test_kernel_launch_counts(lib, name, fwd, bwd):
     """The launches the library reports for the benchmark's workloads (its

@@ -100,13 +100,22 @@ def test_attention_writes_stay_inside_outputs(wl):
     dv = Guarded((T, hkv, 64), torch.bfloat16)
     dsink = Guarded((hq,), torch.float32)
     ws_bytes = sa.bwd_workspace_bytes(q, k, **kw)
-    ws = Guarded((ws_bytes,), torch.uint8)
+    ws = Guarded((ws_bytes,), torch.uint8)  # its inside holds the sentinel too: nothing needs to be zero
+    first = None
     for rep in range(2):  # the second call reuses the workspace as the first left it
         sa.sinkattn_bwd(q, k, v, o.t, lse.t, do, sink, dq=dq.t, dk=dk.t, dv=dv.t, dsink=dsink.t, workspace=ws.t,
                         **kw)
         assert sa.sinkattn_get_device_status() == 0
         for name, g in (("dq", dq), ("dk", dk), ("dv", dv), ("dsink", dsink), ("workspace", ws)):
             g.check(f"{name} (call {rep + 1})")
+        if first is None:
+            first = [t.clone() for t in (dk.t, dv.t, dsink.t)]
+        else:
+            for a, b in zip(first, (dk.t, dv.t, dsink.t)):
+                assert torch.equal(a, b), "dk, dv and dsink are reproducible"
+    ref = pu.oracle_heads(inp, wl, list(range(hq)), parallel=False)
+    pu.assert_within(pu.errors(dict(o=o.t, lse=lse.t, dq=dq.t, dk=dk.t, dv=dv.t, dsink=dsink.t), ref,
+                               list(range(hq)), list(range(hkv))), wl.name)
     for name, t in ins.items():
         assert torch.equal(t, dict(q=q, k=k, v=v, do=do, sink=sink)[name]), f"input {name} was modified"
     assert torch.equal(o_in, o.t) and torch.equal(lse_in, lse.t), "o or lse was modified by the backward"
