@@ -95,7 +95,8 @@ size_t sinkattn_bwd_workspace_size(const sinkattn_problem* prob);
  * sinkattn_bwd_noalloc (which = 2) make for this problem, from host
  * arithmetic alone (the same work lists the calls build); -1 for an invalid
  * problem or `which`.  Lets a caller count the library's launches without a
- * profiler. */
+ * profiler.  The calls make no other stream operation, except the backward
+ * of a problem without tokens, which sets dsink to zero with one memset. */
 int32_t sinkattn_kernel_launches(const sinkattn_problem* prob, int32_t which);
 
 /* Forward.  Reads q, k, v (bf16) and sink (fp32 [Hq]); writes

@@ -1,5 +1,5 @@
-// Backward helper kernels of sink-aware attention (the main kernel is
-// bwd_tc.cu).
+// Backward preprocess of sink-aware attention (the main kernel and the
+// conversion pass are in bwd_tc.cu).
 //
 // Math (explicit sink column with zero value; SinkFlex-RL section 5 and the
 // summary page's alpha = sigmoid(l - s_h); per-head sink gradient from the
@@ -16,9 +16,6 @@
 //               unit-claim counters.
 //               HBM-bound; every thread issues the loads of four tokens
 //               before using them.
-//   dq_convert: dQ = scale * accumulator -> bf16; ceil(Hq / 8) extra blocks
-//               reduce the dsink partials in a fixed order (deterministic),
-//               one warp per head.
 #include "common.cuh"
 #include "internal.h"
 
@@ -142,88 +139,20 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreK p) {
   }
 }
 
-// ------------------------------------------------------------------ convert
-struct ConvK {
-  const float* acc;
-  __nv_bfloat16* dq;
-  long long n8;  // number of 8-element groups
-  float scale;
-  const float* part;
-  int nparts;
-  int hq;
-  float* dsink;
-};
-
-__global__ void __launch_bounds__(256) dq_convert_kernel(const ConvK p) {
-  const int nred = (p.hq + 7) / 8;
-  const int conv_blocks = static_cast<int>(gridDim.x) - nred;
-  if (static_cast<int>(blockIdx.x) >= conv_blocks) {
-    // Fixed-order reduction of the dsink partials: one warp per head.
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int h = (static_cast<int>(blockIdx.x) - conv_blocks) * 8 + warp;
-    if (h >= p.hq) return;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    int i = lane;
-    for (; i + 7 * 32 < p.nparts; i += 8 * 32) {
-#pragma unroll
-      for (int u = 0; u < 8; ++u) acc[u] += p.part[static_cast<size_t>(i + 32 * u) * p.hq + h];
-    }
-    for (; i < p.nparts; i += 32) acc[0] += p.part[static_cast<size_t>(i) * p.hq + h];
-    float s = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) p.dsink[h] = s;
-    return;
-  }
-  // Two groups of 8 accumulator values per thread in flight, read with
-  // streaming loads (the accumulator is dead after this pass).
-  const long long stride = static_cast<long long>(conv_blocks) * blockDim.x;
-  auto emit = [&](long long i, const float4& a, const float4& c) {
-    uint4 o;
-    o.x = pack_bf16(a.x * p.scale, a.y * p.scale);
-    o.y = pack_bf16(a.z * p.scale, a.w * p.scale);
-    o.z = pack_bf16(c.x * p.scale, c.y * p.scale);
-    o.w = pack_bf16(c.z * p.scale, c.w * p.scale);
-    reinterpret_cast<uint4*>(p.dq)[i] = o;
-  };
-  const float4* acc4 = reinterpret_cast<const float4*>(p.acc);
-  long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  for (; i + stride < p.n8; i += 2 * stride) {
-    const float4 a0 = __ldcs(acc4 + 2 * i), c0 = __ldcs(acc4 + 2 * i + 1);
-    const float4 a1 = __ldcs(acc4 + 2 * (i + stride)), c1 = __ldcs(acc4 + 2 * (i + stride) + 1);
-    emit(i, a0, c0);
-    emit(i + stride, a1, c1);
-  }
-  if (i < p.n8) emit(i, __ldcs(acc4 + 2 * i), __ldcs(acc4 + 2 * i + 1));
-}
-
 }  // namespace
 
-// Preprocess, main kernel (bwd_tc.cu), then dQ conversion and dsink reduction.
+// Preprocess, then the main kernel and the conversion pass (bwd_tc.cu).
 cudaError_t launch_bwd(const Problem& pr, const BwdArgs& a, int* status, cudaStream_t stream) {
   const long long T = pr.total_tokens;
-  {
-    PreK k{static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.sink,
-           static_cast<uint4*>(a.bias), a.dq_accum, a.dsink_part, a.unit_counters, a.n_unit_counters,
-           T, pr.hq, pr.scale};
-    if (a.preprocess_blocks > 0) bwd_pre_kernel<<<a.preprocess_blocks, 256, 0, stream>>>(k);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  {
-    cudaError_t e = launch_bwd_tc_main(pr, a, status, stream);
-    if (e != cudaSuccess) return e;
-  }
-  {
-    ConvK k{a.dq_accum, static_cast<__nv_bfloat16*>(a.dq), T * pr.hq * D / 8, pr.scale, a.dsink_part,
-            a.preprocess_blocks, pr.hq, a.dsink};
-    long long blocks = (k.n8 + 255) / 256;
-    const long long cap = 16LL * device_sms();
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
-    dq_convert_kernel<<<static_cast<int>(blocks) + (pr.hq + 7) / 8, 256, 0, stream>>>(k);
-  }
-  return cudaGetLastError();
+  // No rows: every gradient is empty and dsink is zero.
+  if (T == 0 || pr.num_seqs == 0 || pr.seqlen == 0) return cudaMemsetAsync(a.dsink, 0, sizeof(float) * pr.hq, stream);
+  PreK k{static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.sink,
+         static_cast<uint4*>(a.bias), a.dq_accum, a.dsink_part, a.unit_counters, a.n_unit_counters,
+         T, pr.hq, pr.scale};
+  if (a.preprocess_blocks > 0) bwd_pre_kernel<<<a.preprocess_blocks, 256, 0, stream>>>(k);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_bwd_tc_main(pr, a, status, stream);
 }
 
 }  // namespace sa

@@ -783,60 +783,117 @@ __global__ void __launch_bounds__(NTHR, 1) bwd_tc_kernel(const __grid_constant__
   }
 }
 
-// dK, dV of split key tiles: the sum of the tile's per-chunk fp32 slots, in
-// chunk order (deterministic), -> bf16 (dK scaled).  A flat grid-stride pass
-// over every 8-element group of the split tiles' rows, so that many loads are
-// in flight (the work is a few MB spread over a few tiles: one block per tile
-// would leave most SMs idle).
+// The conversion pass after the main kernel, one launch with three kinds of
+// blocks:
+//   dQ     dQ = scale * accumulator -> bf16, two groups of eight values per
+//          thread in flight, streaming loads (the accumulator is dead after);
+//   dK, dV of split key tiles: the sum of the tile's per-chunk fp32 slots, in
+//          chunk order (deterministic), -> bf16 (dK scaled), a flat
+//          grid-stride pass over every 8-element group of the split tiles'
+//          rows (a few MB spread over a few tiles: one block per tile would
+//          leave most SMs idle);
+//   dsink  the fixed-order sum of the preprocess partials, one warp per head
+//          (deterministic).
 struct DkvTile {
   uint32_t code;   // sequence | key tile << 16
   uint32_t slot0;  // slot of chunk 0
   uint32_t nchunks;
 };
 
-struct DkvConvK {
-  const float* acc;
+struct ConvK {
+  // dQ
+  const float* dq_acc;
+  __nv_bfloat16* dq;
+  long long n8;  // 8-element groups of dQ
+  int q_blocks;
+  // split tiles
+  const float* dkv_acc;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   const int32_t* cu;
-  int seqlen, hkv, n_tiles;
+  int seqlen, hkv, n_tiles, kv_blocks;
+  // dsink
+  const float* part;
+  int nparts, hq;
+  float* dsink;
   float scale;
   DkvTile tiles[2048];
 };
-static_assert(sizeof(DkvConvK) < 32000, "kernel parameter block too large");
+static_assert(sizeof(ConvK) < 32000, "kernel parameter block too large");
 
-__global__ void __launch_bounds__(256) dkv_convert_kernel(const __grid_constant__ DkvConvK p) {
-  const int per_row = p.hkv * 2 * (D / 8);  // 8-element groups per key row
-  const long long per_tile = static_cast<long long>(BN) * per_row;
-  const long long total = per_tile * p.n_tiles;
-  const size_t slot_floats = static_cast<size_t>(p.hkv) * 2 * BN * D;
-  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < total; i += static_cast<long long>(gridDim.x) * 256) {
-    const int s = static_cast<int>(i / per_tile);
-    const int rem0 = static_cast<int>(i - s * per_tile);
-    const int r = rem0 / per_row, rem = rem0 - r * per_row;
-    const DkvTile tile = p.tiles[s];
-    const SeqSpan sp = seq_span(p.cu, p.seqlen, static_cast<int>(tile.code & 0xFFFFu));
-    const int k0 = static_cast<int>(tile.code >> 16) * BN;
-    if (k0 + r >= sp.len) continue;
-    const int g = rem / (2 * (D / 8)), which = (rem / (D / 8)) & 1, c8 = rem % (D / 8);
-    const float4* src = reinterpret_cast<const float4*>(
-        p.acc + tile.slot0 * slot_floats + ((static_cast<size_t>(g) * 2 + which) * BN + r) * D + 8 * c8);
-    float4 x = __ldcs(src), y = __ldcs(src + 1);
-    for (uint32_t c = 1; c < tile.nchunks; ++c) {
-      const float4* sc = src + c * (slot_floats / 4);
-      const float4 xc = __ldcs(sc), yc = __ldcs(sc + 1);
-      x = make_float4(x.x + xc.x, x.y + xc.y, x.z + xc.z, x.w + xc.w);
-      y = make_float4(y.x + yc.x, y.y + yc.y, y.z + yc.z, y.w + yc.w);
+__global__ void __launch_bounds__(256) convert_kernel(const __grid_constant__ ConvK p) {
+  const int bid = static_cast<int>(blockIdx.x);
+  if (bid < p.q_blocks) {
+    const long long stride = static_cast<long long>(p.q_blocks) * blockDim.x;
+    auto emit = [&](long long i, const float4& a, const float4& c) {
+      uint4 o;
+      o.x = pack_bf16(a.x * p.scale, a.y * p.scale);
+      o.y = pack_bf16(a.z * p.scale, a.w * p.scale);
+      o.z = pack_bf16(c.x * p.scale, c.y * p.scale);
+      o.w = pack_bf16(c.z * p.scale, c.w * p.scale);
+      reinterpret_cast<uint4*>(p.dq)[i] = o;
+    };
+    const float4* acc4 = reinterpret_cast<const float4*>(p.dq_acc);
+    long long i = static_cast<long long>(bid) * blockDim.x + threadIdx.x;
+    for (; i + stride < p.n8; i += 2 * stride) {
+      const float4 a0 = __ldcs(acc4 + 2 * i), c0 = __ldcs(acc4 + 2 * i + 1);
+      const float4 a1 = __ldcs(acc4 + 2 * (i + stride)), c1 = __ldcs(acc4 + 2 * (i + stride) + 1);
+      emit(i, a0, c0);
+      emit(i + stride, a1, c1);
     }
-    const float mul = which ? p.scale : 1.f;
-    uint4 o;
-    o.x = pack_bf16(x.x * mul, x.y * mul);
-    o.y = pack_bf16(x.z * mul, x.w * mul);
-    o.z = pack_bf16(y.x * mul, y.y * mul);
-    o.w = pack_bf16(y.z * mul, y.w * mul);
-    const size_t row = static_cast<size_t>(sp.start + k0 + r);
-    *reinterpret_cast<uint4*>((which ? p.dk : p.dv) + (row * p.hkv + g) * D + 8 * c8) = o;
+    if (i < p.n8) emit(i, __ldcs(acc4 + 2 * i), __ldcs(acc4 + 2 * i + 1));
+    return;
   }
+  if (bid < p.q_blocks + p.kv_blocks) {
+    const int per_row = p.hkv * 2 * (D / 8);  // 8-element groups per key row
+    const long long per_tile = static_cast<long long>(BN) * per_row;
+    const long long total = per_tile * p.n_tiles;
+    const size_t slot_floats = static_cast<size_t>(p.hkv) * 2 * BN * D;
+    for (long long i = (bid - p.q_blocks) * 256LL + threadIdx.x; i < total;
+         i += static_cast<long long>(p.kv_blocks) * 256) {
+      const int s = static_cast<int>(i / per_tile);
+      const int rem0 = static_cast<int>(i - s * per_tile);
+      const int r = rem0 / per_row, rem = rem0 - r * per_row;
+      const DkvTile tile = p.tiles[s];
+      const SeqSpan sp = seq_span(p.cu, p.seqlen, static_cast<int>(tile.code & 0xFFFFu));
+      const int k0 = static_cast<int>(tile.code >> 16) * BN;
+      if (k0 + r >= sp.len) continue;
+      const int g = rem / (2 * (D / 8)), which = (rem / (D / 8)) & 1, c8 = rem % (D / 8);
+      const float4* src = reinterpret_cast<const float4*>(
+          p.dkv_acc + tile.slot0 * slot_floats + ((static_cast<size_t>(g) * 2 + which) * BN + r) * D + 8 * c8);
+      float4 x = __ldcs(src), y = __ldcs(src + 1);
+      for (uint32_t c = 1; c < tile.nchunks; ++c) {
+        const float4* sc = src + c * (slot_floats / 4);
+        const float4 xc = __ldcs(sc), yc = __ldcs(sc + 1);
+        x = make_float4(x.x + xc.x, x.y + xc.y, x.z + xc.z, x.w + xc.w);
+        y = make_float4(y.x + yc.x, y.y + yc.y, y.z + yc.z, y.w + yc.w);
+      }
+      const float mul = which ? p.scale : 1.f;
+      uint4 o;
+      o.x = pack_bf16(x.x * mul, x.y * mul);
+      o.y = pack_bf16(x.z * mul, x.w * mul);
+      o.z = pack_bf16(y.x * mul, y.y * mul);
+      o.w = pack_bf16(y.z * mul, y.w * mul);
+      const size_t row = static_cast<size_t>(sp.start + k0 + r);
+      *reinterpret_cast<uint4*>((which ? p.dk : p.dv) + (row * p.hkv + g) * D + 8 * c8) = o;
+    }
+    return;
+  }
+  // Fixed-order reduction of the dsink partials: one warp per head.
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = (bid - p.q_blocks - p.kv_blocks) * 8 + warp;
+  if (h >= p.hq) return;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  int i = lane;
+  for (; i + 7 * 32 < p.nparts; i += 8 * 32) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) acc[u] += p.part[static_cast<size_t>(i + 32 * u) * p.hq + h];
+  }
+  for (; i < p.nparts; i += 32) acc[0] += p.part[static_cast<size_t>(i) * p.hq + h];
+  float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane == 0) p.dsink[h] = sum;
 }
 
 // Split tiles of a work list (each tile once, from its chunk 0).
@@ -864,9 +921,12 @@ int bwd_tc_main_slices(const Problem& pr) {
 int bwd_tc_main_launches(const Problem& pr) {
   if (pr.num_seqs == 0 || pr.total_tokens == 0 || pr.seqlen == 0) return 0;
   const std::vector<BwdItem> items = bwd_work_list(pr, bwd_qchunk(pr));
-  constexpr size_t kMaxTiles = sizeof(DkvConvK::tiles) / sizeof(DkvConvK::tiles[0]);
+  constexpr size_t kMaxTiles = sizeof(ConvK::tiles) / sizeof(ConvK::tiles[0]);
   const size_t n_split = split_tiles(items).size();
-  return static_cast<int>((items.size() + kMaxItems - 1) / kMaxItems + (n_split + kMaxTiles - 1) / kMaxTiles);
+  // Main kernel slices, then the conversion (its first launch also takes up
+  // to kMaxTiles split tiles; more tiles need more launches).
+  const size_t extra = n_split > kMaxTiles ? (n_split - 1) / kMaxTiles : 0;
+  return static_cast<int>((items.size() + kMaxItems - 1) / kMaxItems + 1 + extra);
 }
 
 namespace {
@@ -923,26 +983,37 @@ cudaError_t launch_bwd_tc_main(const Problem& pr, const BwdArgs& a, int* status,
     if (e != cudaSuccess) return e;
   }
   if ((e = prof_end(g_prof_bwd, stream)) != cudaSuccess) return e;
-  if (!tiles.empty()) {
-    thread_local DkvConvK c;
-    c.acc = a.dkv_acc;
-    c.dk = static_cast<__nv_bfloat16*>(a.dk);
-    c.dv = static_cast<__nv_bfloat16*>(a.dv);
-    c.cu = pr.cu;
-    c.seqlen = pr.seqlen;
-    c.hkv = pr.hkv;
-    c.scale = pr.scale;
-    constexpr int kMaxTiles = static_cast<int>(sizeof(c.tiles) / sizeof(c.tiles[0]));
-    for (size_t first = 0; first < tiles.size(); first += kMaxTiles) {
-      const int n = static_cast<int>(std::min<size_t>(kMaxTiles, tiles.size() - first));
-      std::copy(tiles.begin() + first, tiles.begin() + first + n, c.tiles);
-      c.n_tiles = n;
-      const long long groups = static_cast<long long>(n) * BN * pr.hkv * 2 * (D / 8);
-      const int blocks = static_cast<int>(std::min<long long>((groups + 255) / 256, 8LL * device_sms()));
-      dkv_convert_kernel<<<blocks, 256, 0, stream>>>(c);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
-  }
+  // Conversion pass: dQ, the split tiles' dK/dV, dsink.
+  thread_local ConvK c;
+  c.dq_acc = a.dq_accum;
+  c.dq = static_cast<__nv_bfloat16*>(a.dq);
+  c.n8 = static_cast<long long>(pr.total_tokens) * pr.hq * D / 8;
+  c.dkv_acc = a.dkv_acc;
+  c.dk = static_cast<__nv_bfloat16*>(a.dk);
+  c.dv = static_cast<__nv_bfloat16*>(a.dv);
+  c.cu = pr.cu;
+  c.seqlen = pr.seqlen;
+  c.hkv = pr.hkv;
+  c.part = a.dsink_part;
+  c.nparts = a.preprocess_blocks;
+  c.hq = pr.hq;
+  c.dsink = a.dsink;
+  c.scale = pr.scale;
+  constexpr int kMaxTiles = static_cast<int>(sizeof(c.tiles) / sizeof(c.tiles[0]));
+  size_t first = 0;
+  do {
+    const int n = static_cast<int>(std::min<size_t>(kMaxTiles, tiles.size() - first));
+    std::copy(tiles.begin() + first, tiles.begin() + first + n, c.tiles);
+    c.n_tiles = n;
+    const bool head = first == 0;  // the first launch also converts dQ and reduces dsink
+    c.q_blocks = head ? static_cast<int>(std::max<long long>(1, std::min<long long>((c.n8 + 255) / 256, 16LL * sms))) : 0;
+    const long long groups = static_cast<long long>(n) * BN * pr.hkv * 2 * (D / 8);
+    c.kv_blocks = static_cast<int>(std::min<long long>((groups + 255) / 256, 8LL * sms));
+    const int red_blocks = head ? (pr.hq + 7) / 8 : 0;
+    convert_kernel<<<c.q_blocks + c.kv_blocks + red_blocks, 256, 0, stream>>>(c);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    first += n;
+  } while (first < tiles.size());
   return cudaSuccess;
 }
 

@@ -148,6 +148,8 @@ inline cudaError_t prof_end(const ProfileEvents& e, cudaStream_t s) {
 cudaError_t launch_fwd_tc(const Problem& p, const FwdArgs& a, int* status, cudaStream_t s);
 // Kernel launches launch_fwd_tc / launch_bwd_tc_main make for a problem (host arithmetic).
 int fwd_tc_launches(const Problem& p);
+// Launches of launch_bwd_tc_main: the main kernel's work-list slices and the
+// conversion pass.
 int bwd_tc_main_launches(const Problem& p);
 int bwd_tc_main_slices(const Problem& p);  // launches of the main kernel itself (work-list slices)
 cudaError_t launch_bwd(const Problem& p, const BwdArgs& a, int* status, cudaStream_t s);

@@ -147,7 +147,7 @@ int32_t sinkattn_kernel_launches(const sinkattn_problem* prob, int32_t which) {
   sa::Problem p;
   if (normalise(prob, p) != SINKATTN_OK) return -1;
   if (which == 1) return sa::fwd_tc_launches(p);
-  if (which == 2) return (bwd_layout(p).pre_blocks > 0 ? 1 : 0) + sa::bwd_tc_main_launches(p) + 1;  // + dQ convert
+  if (which == 2) return (bwd_layout(p).pre_blocks > 0 ? 1 : 0) + sa::bwd_tc_main_launches(p);
   return -1;
 }
 

@@ -276,9 +276,10 @@ def test_grpo_workspace_layout(lib, total):
 
 
 @pytest.mark.parametrize("name,fwd,bwd", [
-    ("causal_gqa_b2_s8192", 1, 3),              # preprocess, main, dQ convert
-    ("causal_gqa_s4096", 1, 4),                 # + the dK/dV conversion of split key tiles
-    ("window128_prefix4_gqa_b2_s8192", 1, 4),   # the always-visible prefix tiles are split
+    # backward: preprocess, main, conversion (dQ, the split key tiles' dK/dV, dsink)
+    ("causal_gqa_b2_s8192", 1, 3),
+    ("causal_gqa_s4096", 1, 3),                 # key tiles split into chunks
+    ("window128_prefix4_gqa_b2_s8192", 1, 3),   # the always-visible prefix tiles are split
     ("window128_gqa_s4096", 1, 3),
     ("varlen8_causal", 1, 3),
 ])
