@@ -299,3 +299,19 @@ def test_kernel_launch_counts(lib, name, fwd, bwd):
     assert lib.sinkattn_kernel_launches(ctypes.byref(pr), 1) == fwd
     assert lib.sinkattn_kernel_launches(ctypes.byref(pr), 2) == bwd
     assert lib.sinkattn_kernel_launches(ctypes.byref(pr), 3) == -1
+
+
+@pytest.mark.parametrize("window,max_tokens", [(128, 1923), (-1, 1408)])
+def test_noalloc_limit_at_64_by_8_heads(lib, window, max_tokens):
+    """The no-allocation backward holds 32 MiB: 272 bytes per (token, query
+    head) for the dQ accumulator and bias rows, plus the dsink partials and,
+    for long causal tiles, the per-chunk dK/dV slots.  One sequence at 64/8
+    heads fits up to 1,923 tokens with a 128-token window and 1,408 fully
+    causal; one token more is rejected before anything is launched."""
+    def pr(S):
+        return problem(seqlen=S, total_tokens=S, num_heads_q=64, num_heads_kv=8, window=window)
+
+    limit = 32 << 20
+    assert lib.sinkattn_bwd_workspace_size(ctypes.byref(pr(max_tokens))) <= limit
+    assert lib.sinkattn_bwd_workspace_size(ctypes.byref(pr(max_tokens + 1))) > limit
+    assert lib.sinkattn_bwd_noalloc(ctypes.byref(pr(max_tokens + 1)), *([FAKE] * 11), None) == 4
