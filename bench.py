@@ -595,6 +595,114 @@ def measure_config(name, dev, flush, peaks, peak_src, target_s=0.3):
     return out
 
 
+def _time_graph(step, K, dev, flush, sample_ms=20):
+    """K CUDA-graph replays of ``step`` (L2 flushed before each, outside its
+    events), with the clocks sampled meanwhile."""
+    import torch
+
+    graph = capture_step(step)
+    for _ in range(3):
+        flush(1.0)
+        graph.replay()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index if dev.index is not None else 0, sample_ms)
+    clocks.start()
+    for i in range(K):
+        flush(float(i))
+        ev[i][0].record()
+        graph.replay()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    info = clocks.stop()
+    return [a.elapsed_time(b) for a, b in ev], info
+
+
+def measure_decode_config(name, dev, flush, peaks, peak_src, target_s=0.3):
+    """One decode workload at N = 1: graph replays of the one-kernel step for
+    about ``target_s`` seconds, GB/s of algorithmic bytes against HBM."""
+    import torch
+
+    import sink_aware_masked_gb300 as sa
+
+    wl, n = W.DECODE_WORKLOADS[name]
+    inp = W.make_decode_inputs(wl, n)
+    q, k, v, sink = (t.to(dev) for t in (inp.q_bf16, inp.k_bf16, inp.v_bf16, inp.sink))
+    if wl.uniform:
+        prob = dict(num_seqs=wl.num_seqs)
+    else:
+        cu = wl.cu_seqlens()
+        prob = dict(cu_seqlens=torch.tensor(cu, dtype=torch.int32, device=dev),
+                    cu_seqlens_host=[int(x) for x in cu], max_seqlen=wl.max_seqlen)
+    prob.update(window=wl.window, prefix=wl.prefix, causal=wl.causal, scale=wl.scale)
+    o = torch.empty_like(q)
+    lse = torch.empty((wl.num_heads_q, q.shape[0]), dtype=torch.float32, device=dev)
+    ws = torch.zeros(max(16, sa.decode_workspace_bytes(q, k, q_per_seq=n, **prob)), dtype=torch.uint8, device=dev)
+
+    def step():
+        sa.sinkattn_decode_fwd(q, k, v, sink, q_per_seq=n, o=o, lse=lse, workspace=ws, **prob)
+
+    for _ in range(3):
+        flush(1.0)
+        step()
+    torch.cuda.synchronize()
+    probe, _ = _time_graph(step, 5, dev, flush)
+    K = int(min(3000, max(20, math.ceil(target_s * 1e3 / (statistics.median(probe) + 0.1)))))
+    ms, clocks = _time_graph(step, K, dev, flush)
+    if sa.sinkattn_get_device_status() != 0:
+        raise RuntimeError("device status reported a timed-out wait")
+    nbytes = decode_bytes(wl, n)
+    gbs = nbytes * K / (sum(ms) / 1e3) / 1e9
+    out = {"gbs": gbs, "ms_per_step": sum(ms) / K, "steps": K, "dominant_kernel": "decode_split_kernel",
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "peak_source": f"{peak_src} HBM copy",
+                        "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": nbytes,
+                        "traffic": _committed_traffic(name, "decode_split")},
+           "gpu_launches": K * DECODE_LAUNCHES_PER_STEP, "clocks": clocks,
+           "timing": "CUDA-graph replay of the one-kernel step"}
+    del q, k, v, o, lse, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_grpo_config(name, dev, flush, peaks, peak_src, target_s=0.3):
+    """The GRPO loss workload at N = 1: graph replays of the one-kernel step."""
+    import torch
+
+    import sink_aware_masked_gb300 as sa
+
+    inp = W.make_grpo_inputs(W.GRPO_WORKLOADS[name])
+    wl = inp.wl
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    logp, old, lref, mask, rew, cu = (t(a) for a in (inp.logp, inp.logp_old, inp.logp_ref, inp.mask, inp.rewards,
+                                                      inp.cu_tokens))
+    cu_host = [int(x) for x in inp.cu_tokens]
+    dlogp = torch.empty_like(logp)
+    ws = torch.zeros(sa.grpo_workspace_bytes(cu, cu_host, group_size=wl.group_size), dtype=torch.uint8, device=dev)
+    kw = dict(group_size=wl.group_size, clip_eps=wl.clip_eps, adv_eps=wl.adv_eps, kl_beta=wl.kl_beta,
+              logp_ref=lref if wl.kl_beta else None, dlogp=dlogp, workspace=ws)
+
+    def step():
+        sa.grpo_loss(logp, old, mask, rew, cu, cu_host, **kw)
+
+    for _ in range(3):
+        flush(1.0)
+        step()
+    torch.cuda.synchronize()
+    probe, _ = _time_graph(step, 5, dev, flush)
+    K = int(min(3000, max(20, math.ceil(target_s * 1e3 / (statistics.median(probe) + 0.1)))))
+    ms, clocks = _time_graph(step, K, dev, flush)
+    if sa.sinkattn_get_device_status() != 0:
+        raise RuntimeError("device status reported a timed-out wait")
+    nbytes = grpo_bytes(inp)
+    gbs = nbytes * K / (sum(ms) / 1e3) / 1e9
+    return {"gbs": gbs, "ms_per_step": sum(ms) / K, "steps": K, "dominant_kernel": "grpo_kernel",
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "peak_source": f"{peak_src} HBM copy",
+                         "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": nbytes,
+                         "traffic": _committed_traffic(name, "grpo")},
+            "gpu_launches": K * GRPO_LAUNCHES_PER_STEP, "clocks": clocks,
+            "timing": "CUDA-graph replay of the one-kernel step"}
+
+
 def run_gpu(args, world, rank, local):
     import torch
 
@@ -710,6 +818,12 @@ def run_gpu(args, world, rank, local):
         # (not part of the line's value): causal and windowed, uniform and packed.
         line["configs"] = {name: measure_config(name, dev, flush, peaks, peak_src)
                            for name in EXTRA_CONFIGS if name != args.workload}
+        # The rollout-side decode forward and the GRPO loss of the same
+        # training loop, each one kernel, in GB/s of algorithmic bytes.
+        for name in sorted(W.DECODE_WORKLOADS):
+            line["configs"][name] = measure_decode_config(name, dev, flush, peaks, peak_src)
+        for name in sorted(W.GRPO_WORKLOADS):
+            line["configs"][name] = measure_grpo_config(name, dev, flush, peaks, peak_src)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl)
     if rank == 0:
