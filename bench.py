@@ -100,6 +100,13 @@ def decode_visible_keys(wl, n):
     return total
 
 
+def decode_kernel(wl, n):
+    """(short name, kernel function) of the decode launch: the warp-MMA kernel
+    for at most 16 rows per (sequence, kv head), the tcgen05 one above."""
+    rows = (wl.num_heads_q // wl.num_heads_kv) * n
+    return ("decode_split", "decode_split_kernel") if rows <= 16 else ("decode_tc", "decode_tc_kernel")
+
+
 def decode_bytes(wl, n):
     """Algorithmic HBM bytes of one decode step: visible K and V once per kv
     head, the query rows, O and lse."""
@@ -653,10 +660,11 @@ def measure_decode_config(name, dev, flush, peaks, peak_src, target_s=0.3):
         raise RuntimeError("device status reported a timed-out wait")
     nbytes = decode_bytes(wl, n)
     gbs = nbytes * K / (sum(ms) / 1e3) / 1e9
-    out = {"gbs": gbs, "ms_per_step": sum(ms) / K, "steps": K, "dominant_kernel": "decode_split_kernel",
+    short, kname = decode_kernel(wl, n)
+    out = {"gbs": gbs, "ms_per_step": sum(ms) / K, "steps": K, "dominant_kernel": kname,
            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "peak_source": f"{peak_src} HBM copy",
                         "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": nbytes,
-                        "traffic": _committed_traffic(name, "decode_split")},
+                        "traffic": _committed_traffic(name, short)},
            "gpu_launches": K * DECODE_LAUNCHES_PER_STEP, "clocks": clocks,
            "timing": "CUDA-graph replay of the one-kernel step"}
     del q, k, v, o, lse, ws
@@ -943,9 +951,11 @@ def run_gpu_decode(args, world, rank, local):
                    "decode_rows_per_s": world * wl.num_seqs * n * K / (tot / 1e3)},
         "pct_of_peak": 100.0 * value / world / peaks["hbm_gbs"],
         "breakdown_ms": {"split_kernel": avg_split, "rest": statistics.mean(step_ms) - avg_split},
-        "roofline": {"bound": "hbm", "kernel": "decode_split", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                     "peak_source": f"{peak_src} HBM copy", "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": _committed_traffic(args.workload, "decode_split"), "algorithmic_bytes": nbytes},
+        "roofline": {"bound": "hbm", "kernel": decode_kernel(wl, n)[0], "achieved": achieved,
+                     "peak": peaks["hbm_gbs"], "peak_source": f"{peak_src} HBM copy", "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": _committed_traffic(args.workload, decode_kernel(wl, n)[0]),
+                     "algorithmic_bytes": nbytes},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "the key/value cache is the decoder's resident state; the step's query rows cross PCIe"},
         "gpu_launches": K * DECODE_LAUNCHES_PER_STEP,

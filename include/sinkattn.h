@@ -234,7 +234,8 @@ sinkattn_status sinkattn_get_device_status(void* stream);
 
 /* Measurement hook.  kind 1 selects the forward attention kernel, kind 2
  * the backward main kernel, kind 3 the key-chunk kernel of the decode
- * forward.  With non-NULL `start` and `stop` (cudaEvent_t handles passed as
+ * forward (the warp-MMA kernel for at most 16 rows per (sequence, kv head),
+ * the tensor-core kernel above).  With non-NULL `start` and `stop` (cudaEvent_t handles passed as
  * void*), every later sinkattn_fwd / sinkattn_bwd / sinkattn_decode_fwd call
  * records `start` on its stream immediately before that kernel's launch and
  * `stop` immediately after it, so the caller can time the kernel alone with

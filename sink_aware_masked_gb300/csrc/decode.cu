@@ -11,29 +11,19 @@
 // Few query rows meet a long key history, so the work is a stream over K and
 // V bounded by HBM bandwidth (the 8 query heads of a GQA group share every
 // key: about 8 FLOP per byte at n = 1).  The key range of each (sequence, kv
-// head) is split into chunks of whole 128-key tiles (split-KV); one CTA per
-// (chunk, kv head) streams its tiles by TMA through a 2-stage mbarrier ring
-// (three such CTAs resident per SM)
-// and computes, for the group x n query rows, a partial online softmax
-// (running max m in log2 units, row sum l, unnormalised O) with warp-level
-// bf16 MMAs.  The last CTA of a (sequence, kv head) to finish (a counter in
-// the workspace, incremented after the partial is written and fenced) merges
-// the partials of each row,
-//     m = max m_i,  l = sum 2^{m_i - m} l_i,  O = sum 2^{m_i - m} O_i / l,
-// and only then applies the sink: lse = ln2 (m + log2 l), alpha =
-// sigmoid(lse - s_h), O <- alpha O (summary page, sink scaling of the output
-// by sigma(l - s_h)); it then clears the counter for the next call.  The
-// chunks of a sequence hold equal numbers of tiles (within one).
+// head) is split into chunks of whole 128-key tiles (split-KV), one CTA per
+// (chunk, kv head); the partials are merged by the last CTA of each
+// (sequence, kv head) with the sink applied once (decode_common.cuh).
 //
-// Rows r of one (sequence, kv head): r = i * group + j is query position
-// L - n + i of query head g * group + j.  Warps split the rows into groups of
-// at most two 16-row blocks and the keys of each tile among the rest; the
-// warps that share rows are merged inside the CTA before the partial is
-// written.  Every mbarrier wait is bounded.
-#include "common.cuh"
-#include "internal.h"
-#include "tc.cuh"
-#include "tmap.h"
+// This file holds the plan, the launcher and the kernel for a single 16-row
+// block (R = group x n <= 16, e.g. one new row per sequence with GQA 8): the
+// CTA streams its tiles by TMA through a 2-stage mbarrier ring (three such
+// CTAs resident per SM) and computes a partial online softmax (running max m
+// in log2 units, row sum l, unnormalised O) with warp-level bf16 MMAs, the
+// four warps splitting the keys of each tile and merging in shared memory
+// before the partial is written.  Wider row blocks run on the tensor-core
+// kernel of decode_tc.cu.  Every mbarrier wait is bounded.
+#include "decode_common.cuh"
 
 #include <algorithm>
 #include <vector>
@@ -42,58 +32,11 @@ namespace sa {
 namespace {
 
 using namespace tc;
+using namespace dec;
 
-constexpr int D = kHeadDim;
-constexpr int BN = 128;           // keys per tile
 constexpr int NS = 2;             // K/V stages (three CTAs per SM fit: 65 KB of shared memory each)
 constexpr int NTHR = 128;
-constexpr int TILE = BN * D * 2;  // 16 KB
 constexpr int SMEM_DYN = NS * 2 * TILE + 1024;
-
-// The work list's capacity is a template parameter: a short list keeps the
-// kernel parameter block small (a 16 KB block costs ~1.3 us more per launch
-// than a small one, a few per cent of a short decode step).
-constexpr int kDecodeSmallItems = 256;
-
-template <int CAP>
-struct DecK {
-  CUtensorMap tm_k, tm_v;
-  const __nv_bfloat16* q;  // [B * n, Hq, 64]
-  const float* sink;
-  __nv_bfloat16* o;        // [B * n, Hq, 64]
-  float* lse;              // [Hq, B * n]
-  int* counters;           // [B * Hkv] chunks finished; zero between calls
-  float* ws_acc;           // [items * Hkv, R, 64] unnormalised O of each partial
-  float2* ws_ml;           // [items * Hkv, Rml]: (m in log2 units of the scaled score, l)
-  const int32_t* cu;       // key/value offsets or nullptr (uniform length kv_len)
-  int* status;
-  int kv_len;
-  int n, hq, hkv, group, R;
-  int Rml;                 // R rounded up to even: (max, sum) blocks are whole 16-byte units
-  MaskParams mask;
-  float scale_log2;
-  int num_seqs;
-  int tiles_per_split;  // chunks of a sequence: ceil(tiles / tiles_per_split), equal shares
-  int n_items;
-  uint32_t items[CAP];  // sequence | (chunk << 16), chunks of a sequence consecutive
-};
-static_assert(sizeof(DecK<kDecodeMaxItems>) < 32000, "kernel parameter block too large");
-
-// Key tiles that the query rows [L - n, L - 1] see: the prefix tiles below the
-// window, then the window/causal band (same arithmetic as the full forward).
-struct KeyTiles {
-  int lo_t, n_pre, n_tiles;
-  SA_DEV int k0(int j) const { return (j < n_pre ? j : lo_t + (j - n_pre)) * BN; }
-};
-
-SA_DEV KeyTiles key_tiles(int L, int n, const MaskParams& m) {
-  const KeyRange kr = key_range(L - n, L - 1, L, m);
-  KeyTiles t;
-  t.lo_t = kr.lo / BN;
-  t.n_pre = min((kr.pre_end + BN - 1) / BN, t.lo_t);
-  t.n_tiles = t.n_pre + (kr.hi / BN - t.lo_t + 1);
-  return t;
-}
 
 SA_DEV float quad_max(float x) {
   x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
@@ -104,7 +47,8 @@ SA_DEV float quad_sum(float x) {
   return x + __shfl_xor_sync(0xffffffffu, x, 2);
 }
 
-// MB: 16-row blocks covering the R rows (1, 2, 4 or 8).
+// MB: 16-row blocks covering the R rows (launched with MB = 1; the body
+// also supports 2, 4 and 8).
 template <int MB, int CAP>
 __global__ void __launch_bounds__(NTHR, 3) decode_split_kernel(const __grid_constant__ DecK<CAP> p) {
   constexpr int MBW = MB < 2 ? MB : 2;  // row blocks per warp
@@ -121,13 +65,11 @@ __global__ void __launch_bounds__(NTHR, 3) decode_split_kernel(const __grid_cons
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wr = warp / WK, wk = warp % WK;
   const int item_idx = blockIdx.x, g = blockIdx.y;
-  const uint32_t item = p.items[item_idx];
-  const int b = static_cast<int>(item & 0xFFFFu), split = static_cast<int>(item >> 16);
-  const SeqSpan sp = seq_span(p.cu, p.kv_len, b);
-  const int L = sp.len, n = p.n;
-  const KeyTiles kt = key_tiles(L, n, p.mask);
-  const int nsplit = (kt.n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
-  const int j0 = split * kt.n_tiles / nsplit, j1 = (split + 1) * kt.n_tiles / nsplit;
+  const Chunk ch = chunk_of(p, item_idx);
+  const SeqSpan sp = ch.sp;
+  const int b = ch.b, L = sp.len, n = p.n;
+  const KeyTiles kt = ch.kt;
+  const int j0 = ch.j0, j1 = ch.j1;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
@@ -355,93 +297,14 @@ __global__ void __launch_bounds__(NTHR, 3) decode_split_kernel(const __grid_cons
       M = fmaxf(M, red_m[wr2 * WK + w][rl]);
       l += red_l[wr2 * WK + w][rl];
     }
-    p.ws_ml[part * p.Rml + r] = make_float2(M, l);
+    p.ws_ml[part * p.R + r] = make_float4(M, l, l, 0.f);
   }
 
-  // The last chunk of this (sequence, kv head) to finish merges all of them.
+  // The last chunk of this (sequence, kv head) to finish merges all of them
+  // (the stage buffers are idle now).
   __shared__ int is_last;
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) is_last = atomicAdd(p.counters + b * p.hkv + g, 1) == nsplit - 1;
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  // Partials of chunk c: O at ws_acc + (part0 + c Hkv) R 64, (max, sum) at
-  // ws_ml + (part0 + c Hkv) Rml.  They are staged in batches through the
-  // (now idle) stage buffers by bulk copies, then merged from shared memory
-  // with an online rescale per (row, dim pair) unit.
-  const size_t part0 = static_cast<size_t>(item_idx - split) * p.hkv + g;
-  const uint32_t blk_acc = static_cast<uint32_t>(p.R) * D * 4, blk_ml = static_cast<uint32_t>(p.Rml) * 8;
-  const int per_batch = max(1, (NS * 2 * TILE) / static_cast<int>(blk_acc + blk_ml));
-  constexpr int UP = MB * 4;  // units per thread: (MB * 16 rows) x 32 dim pairs / 128 threads
-  float2 acc[UP];
-  float Mu[UP], lu[UP];
-#pragma unroll
-  for (int k = 0; k < UP; ++k) {
-    acc[k] = make_float2(0.f, 0.f);
-    Mu[k] = -INFINITY;
-    lu[k] = 0.f;
-  }
-  const float* stg_acc = reinterpret_cast<const float*>(smem);
-  const float2* ml_s = reinterpret_cast<const float2*>(smem + per_batch * blk_acc);
-  if (tid == 0) fence_proxy_async_global();  // the partials were written through the generic proxy
-  for (int c0 = 0, batch = 0; c0 < nsplit; c0 += per_batch, ++batch) {
-    const int cnt = min(per_batch, nsplit - c0);
-    const uint32_t bar = smem_u32(&merge_bar);
-    if (tid == 0) {
-      mbar_expect_tx(bar, cnt * (blk_acc + blk_ml));
-      for (int c = 0; c < cnt; ++c) {
-        const size_t pc = part0 + static_cast<size_t>(c0 + c) * p.hkv;
-        bulk_load(sb + c * blk_acc, p.ws_acc + pc * p.R * D, blk_acc, bar);
-        bulk_load(sb + per_batch * blk_acc + c * blk_ml, p.ws_ml + pc * p.Rml, blk_ml, bar);
-      }
-    }
-    const bool ok = mbar_wait(bar, batch & 1, ab);
-    if (__syncthreads_or(!ok)) {
-      if (tid == 0) {  // let the copies still in flight land before the CTA leaves
-        const long long t0 = clock64();
-        while (!mbar_try_wait(bar, batch & 1) && clock64() - t0 < kTimeoutCycles) {
-        }
-      }
-      return;
-    }
-#pragma unroll
-    for (int k = 0; k < UP; ++k) {
-      const int u = tid + NTHR * k, r = u >> 5, d2 = u & 31;
-      if (r >= p.R) continue;
-      for (int c = 0; c < cnt; ++c) {
-        const float2 mv = ml_s[c * p.Rml + r];
-        if (mv.x == -INFINITY) continue;
-        if (mv.x > Mu[k]) {
-          const float sc = (Mu[k] == -INFINITY) ? 0.f : ex2(Mu[k] - mv.x);
-          acc[k].x *= sc;
-          acc[k].y *= sc;
-          lu[k] *= sc;
-          Mu[k] = mv.x;
-        }
-        const float w = ex2(mv.x - Mu[k]);
-        const float2 a = reinterpret_cast<const float2*>(stg_acc + (static_cast<size_t>(c) * p.R + r) * D)[d2];
-        acc[k].x += w * a.x;
-        acc[k].y += w * a.y;
-        lu[k] += w * mv.y;
-      }
-    }
-    __syncthreads();  // the next batch overwrites the staging buffers
-  }
-#pragma unroll
-  for (int k = 0; k < UP; ++k) {
-    const int u = tid + NTHR * k, r = u >> 5, d2 = u & 31;
-    if (r >= p.R) continue;
-    const float l = lu[k], M = Mu[k];
-    const int i = r / p.group, h = g * p.group + (r - i * p.group), bn = b * n + i;
-    const float lse = (l > 0.f) ? (M + __log2f(l)) * kLn2 : -INFINITY;
-    const float alpha = 1.f / (1.f + ex2((__ldg(p.sink + h) - lse) * kLog2e));
-    const float fac = (l > 0.f) ? alpha / l : 0.f;
-    reinterpret_cast<uint32_t*>(p.o + (static_cast<size_t>(bn) * p.hq + h) * D)[d2] =
-        pack_bf16(acc[k].x * fac, acc[k].y * fac);
-    if (d2 == 0) p.lse[static_cast<size_t>(h) * p.num_seqs * n + bn] = lse;
-  }
-  if (tid == 0) p.counters[b * p.hkv + g] = 0;  // every chunk of this call has counted
+  if (!count_partial(p, ch, g, &is_last)) return;
+  merge_partials<MB * 4, NTHR>(p, ch, g, item_idx, smem, NS * 2 * TILE, smem_u32(&merge_bar), ab);
 }
 
 }  // namespace
@@ -473,14 +336,39 @@ DecodePlan decode_plan(const Problem& p, int n) {
   // wider row blocks (8 x 32768 x 4 rows) win at 2.  At least two tiles per
   // chunk, and no more items than the parameter block holds.
   const int rows = (p.hq / std::max(p.hkv, 1)) * n;
-  const int factor = (rows <= 16 && total >= 1024) ? 4 : 2;
-  const long long want = std::max<long long>(1, static_cast<long long>(factor) * std::max(sms, 1) / std::max(p.hkv, 1));
-  int tps = static_cast<int>(std::max<long long>(2, (total + want - 1) / want));
-  for (;;) {
+  auto items_at = [&](int t) {
     long long items = 0;
-    for (int b = 0; b < p.num_seqs; ++b) items += (tiles[b] + tps - 1) / tps;
-    if (items <= kDecodeMaxItems) break;
-    tps *= 2;
+    for (int b = 0; b < p.num_seqs; ++b) items += (tiles[b] + t - 1) / t;
+    return items;
+  };
+  int tps;
+  if (rows <= 16) {
+    const int factor = total >= 1024 ? 4 : 2;
+    const long long want =
+        std::max<long long>(1, static_cast<long long>(factor) * std::max(sms, 1) / std::max(p.hkv, 1));
+    tps = static_cast<int>(std::max<long long>(2, (total + want - 1) / want));
+    while (items_at(tps) > kDecodeMaxItems) tps *= 2;
+  } else {
+    // Tensor-core kernel (two CTAs per SM up to 64 rows, one above): each CTA
+    // is a latency-bound stream, so the grid must fit in one wave of
+    // resident CTAs (a second wave of a few CTAs doubles the step).  The
+    // smallest chunk length whose item count fits: items_at() does not grow
+    // with the length, so a binary search finds it.
+    const int per_sm = rows <= 64 ? 2 : 1;
+    const long long fit = std::max<long long>(
+        std::max<long long>(1, static_cast<long long>(per_sm) * std::max(sms, 1) / std::max(p.hkv, 1)), p.num_seqs);
+    const long long target = std::min<long long>(fit, kDecodeMaxItems);
+    int max_tiles = 2;
+    for (int b = 0; b < p.num_seqs; ++b) max_tiles = std::max(max_tiles, tiles[b]);
+    int lo = static_cast<int>(std::max<long long>(2, (total + target - 1) / target)), hi = std::max(lo, max_tiles);
+    while (lo < hi) {
+      const int mid = lo + (hi - lo) / 2;
+      if (items_at(mid) <= target)
+        hi = mid;
+      else
+        lo = mid + 1;
+    }
+    tps = lo;
   }
   pl.tiles_per_split = tps;
   pl.items.clear();
@@ -490,7 +378,7 @@ DecodePlan decode_plan(const Problem& p, int n) {
   }
   const int R = (p.hq / p.hkv) * n;
   pl.acc_bytes = pl.items.size() * p.hkv * static_cast<size_t>(R) * D * 4;
-  pl.ml_bytes = pl.items.size() * p.hkv * static_cast<size_t>((R + 1) & ~1) * 8;
+  pl.ml_bytes = pl.items.size() * p.hkv * static_cast<size_t>(R) * 16;
   pl.counter_bytes = static_cast<size_t>(p.num_seqs) * p.hkv * 4;
   return pl;
 }
@@ -501,51 +389,20 @@ template <int CAP>
 cudaError_t launch_decode_cap(const Problem& pr, int n, const DecodeArgs& a, const DecodePlan& pl, int* status,
                               cudaStream_t stream) {
   thread_local DecK<CAP> k;
-  if (!make_rows_map(&k.tm_k, a.k, pr.total_tokens, pr.hkv, BN) ||
-      !make_rows_map(&k.tm_v, a.v, pr.total_tokens, pr.hkv, BN))
-    return cudaErrorInvalidValue;
-  const int group = pr.hq / pr.hkv, R = group * n;
-  k.q = static_cast<const __nv_bfloat16*>(a.q);
-  k.sink = a.sink;
-  k.o = static_cast<__nv_bfloat16*>(a.o);
-  k.lse = a.lse;
-  k.counters = a.counters;
-  k.num_seqs = pr.num_seqs;
-  k.ws_acc = a.ws_acc;
-  k.ws_ml = reinterpret_cast<float2*>(a.ws_ml);
-  k.cu = pr.cu;
-  k.status = status;
-  k.kv_len = pr.seqlen;
-  k.n = n;
-  k.hq = pr.hq;
-  k.hkv = pr.hkv;
-  k.group = group;
-  k.R = R;
-  k.Rml = (R + 1) & ~1;
-  k.mask = MaskParams{pr.window, pr.prefix, pr.causal};
-  k.scale_log2 = pr.scale * kLog2e;
-  k.tiles_per_split = pl.tiles_per_split;
-  k.n_items = static_cast<int>(pl.items.size());
-  std::copy(pl.items.begin(), pl.items.end(), k.items);
-  const int mb = R <= 16 ? 1 : R <= 32 ? 2 : R <= 64 ? 4 : 8;
+  if (!fill_params(k, pr, n, a, pl, status)) return cudaErrorInvalidValue;
   const dim3 grid(k.n_items, pr.hkv);
   cudaError_t e = prof_begin(g_prof_dec, stream);
   if (e != cudaSuccess) return e;
-  switch (mb) {
-#define SA_DECODE_CASE(MBV)                                                                                    \
-  case MBV:                                                                                                    \
-    if ((e = cudaFuncSetAttribute(decode_split_kernel<MBV, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                  SMEM_DYN)) != cudaSuccess)                                                   \
-      return e;                                                                                                \
-    decode_split_kernel<MBV, CAP><<<grid, NTHR, SMEM_DYN, stream>>>(k);                                        \
-    break;
-    SA_DECODE_CASE(1)
-    SA_DECODE_CASE(2)
-    SA_DECODE_CASE(4)
-    SA_DECODE_CASE(8)
-#undef SA_DECODE_CASE
+  if (k.R <= 16) {
+    if ((e = cudaFuncSetAttribute(decode_split_kernel<1, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  SMEM_DYN)) != cudaSuccess)
+      return e;
+    decode_split_kernel<1, CAP><<<grid, NTHR, SMEM_DYN, stream>>>(k);
+    e = cudaGetLastError();
+  } else {
+    e = launch_decode_tc(k, grid, stream);
   }
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (e != cudaSuccess) return e;
   return prof_end(g_prof_dec, stream);
 }
 
@@ -555,8 +412,8 @@ cudaError_t launch_decode(const Problem& pr, int n, const DecodeArgs& a, const D
                           cudaStream_t stream) {
   if (pr.num_seqs == 0) return cudaSuccess;
   if (pl.items.size() > static_cast<size_t>(kDecodeMaxItems)) return cudaErrorInvalidValue;
-  return pl.items.size() <= static_cast<size_t>(kDecodeSmallItems)
-             ? launch_decode_cap<kDecodeSmallItems>(pr, n, a, pl, status, stream)
+  return pl.items.size() <= static_cast<size_t>(kSmallItems)
+             ? launch_decode_cap<kSmallItems>(pr, n, a, pl, status, stream)
              : launch_decode_cap<kDecodeMaxItems>(pr, n, a, pl, status, stream);
 }
 

@@ -99,7 +99,7 @@ struct DecodeArgs {
   void* o;        // [B * n, Hq, 64]
   float* lse;     // [Hq, B * n]
   float* ws_acc;   // partial unnormalised outputs
-  void* ws_ml;     // partial (max, sum) pairs
+  void* ws_ml;     // per partial and row: (max, sum for O, sum for lse, 0) as float4
   int* counters;   // chunks finished per (sequence, kv head); zero between calls
 };
 

@@ -167,6 +167,17 @@ SA_DEV bool named_sync_and(int id, int n, bool v) {
   return r != 0;
 }
 
+// Named barrier over `n` threads that returns whether `v` holds for any of them.
+SA_DEV bool named_sync_or(int id, int n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, %2, %3, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
 // Named barrier over `n` threads (id 1..15; id 0 is __syncthreads).
 SA_DEV void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory"); }
 

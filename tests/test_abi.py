@@ -229,12 +229,22 @@ def _decode_plan_items(lens, hq, hkv, n, window=-1, prefix=0, sms=152):
         tiles.append(n_pre + (hi // 128 - lo_t + 1))
     total = sum(tiles)
     rows = (hq // hkv) * n
-    factor = 4 if rows <= 16 and total >= 1024 else 2
-    want = max(1, factor * sms // hkv)
-    tps = max(2, -(-total // want))
-    while sum(-(-t // tps) for t in tiles) > 4096:
-        tps *= 2
-    return sum(-(-t // tps) for t in tiles)
+    items_at = lambda t: sum(-(-x // t) for x in tiles)  # noqa: E731
+    if rows <= 16:
+        factor = 4 if total >= 1024 else 2
+        want = max(1, factor * sms // hkv)
+        tps = max(2, -(-total // want))
+        while items_at(tps) > 4096:
+            tps *= 2
+        return items_at(tps)
+    # Tensor-core kernel: the smallest chunk length whose grid fits one wave
+    # of resident CTAs (two per SM up to 64 rows, one above).
+    per_sm = 2 if rows <= 64 else 1
+    target = min(max(max(1, per_sm * sms // hkv), len(tiles)), 4096)
+    tps = max(2, -(-total // target))
+    while items_at(tps) > target:
+        tps += 1
+    return items_at(tps)
 
 
 @pytest.mark.parametrize("lens,n,window,prefix", [
@@ -242,10 +252,13 @@ def _decode_plan_items(lens, hq, hkv, n, window=-1, prefix=0, sms=152):
     ([32768] * 8, 4, -1, 0),                                       # 32 rows per kv head: factor 2
     ([6111, 5036, 1589, 6459, 1056, 6459, 3018, 2085], 1, -1, 0),  # packed: < 1024 tiles per kv head
     ([8192] * 32, 1, 128, 4),                                      # window and prefix
+    ([8192] * 32, 8, -1, 0),                                       # 64 rows: tensor-core kernel, 2 CTAs per SM
+    ([5000, 300, 9000], 16, 200, 3),                               # 128 rows: one CTA per SM
 ])
 def test_decode_plan_chunk_count(lib, lens, n, window, prefix):
     """The workspace size encodes the plan: counters, one partial (O and
-    (max, sum)) per chunk, kv head and row, each region 256-byte aligned."""
+    (max, sum for O, sum for lse, 0)) per chunk, kv head and row, each region
+    256-byte aligned."""
     from sink_aware_masked_gb300 import _lib
 
     hq, hkv = 64, 8
@@ -260,7 +273,7 @@ def test_decode_plan_chunk_count(lib, lens, n, window, prefix):
     items = _decode_plan_items(lens, hq, hkv, n, window, prefix)
     R = (hq // hkv) * n
     r256 = lambda x: -(-x // 256) * 256  # noqa: E731
-    want = r256(len(lens) * hkv * 4) + r256(items * hkv * R * 64 * 4) + r256(items * hkv * ((R + 1) & ~1) * 8) + 256
+    want = r256(len(lens) * hkv * 4) + r256(items * hkv * R * 64 * 4) + r256(items * hkv * R * 16) + 256
     assert lib.sinkattn_decode_workspace_size(ctypes.byref(pr), n) == want
 
 

@@ -19,10 +19,12 @@ def built():
     build.build()
 
 
-def run_decode(wl, n, sink=None):
+def run_decode(wl, n, sink=None, key_gain=None):
     import sink_aware_masked_gb300 as sa
 
     inp = W.make_decode_inputs(wl, n)
+    if key_gain is not None:  # per-token factor on the keys (bf16-exact powers of two)
+        inp.k_bf16 = (inp.k_bf16.float() * key_gain[:, None, None]).to(torch.bfloat16)
     q = inp.q_bf16
     s = inp.sink if sink is None else sink
     kw = dict(window=wl.window, prefix=wl.prefix, causal=wl.causal, scale=wl.scale)
@@ -50,6 +52,9 @@ CASES = [
     ((4096, 4096, 4096), 64, 8, 2, -1, 0, 97),      # 64/8 heads
     ((32768,), 64, 8, 1, -1, 0, 96),                # long history split over many chunks
     ((3000,), 12, 4, 3, 10, 2000, 98),              # group of 3, prefix wider than the window
+    ((1500, 700), 17, 1, 1, -1, 0, 86),             # 17 rows: tensor-core kernel, 15 padding columns
+    ((2100, 333), 12, 1, 4, 200, 3, 87),            # 48 rows padded to 64, window and prefix
+    ((1800, 97), 24, 1, 4, -1, 0, 88),              # 96 rows padded to 128, a sequence shorter than a tile
 ]
 
 
@@ -69,6 +74,19 @@ def test_decode_sink_limits():
     assert np.all(o == 0.0) and pu.max_abs(lse, ref_lse) <= pu.TOL["lse"]
     o, lse, ref_o, ref_lse = run_decode(wl, 2, sink=torch.full((hq,), float("-inf")))
     assert pu.max_abs(o, ref_o) <= pu.TOL["o"] and pu.max_abs(lse, ref_lse) <= pu.TOL["lse"]
+
+
+@pytest.mark.parametrize("n,hq", [(4, 16), (8, 16), (16, 16), (2, 64)])
+def test_decode_growing_scores(n, hq):
+    """Keys whose scale doubles every 300 tokens: late tiles score far above
+    the early ones, so the running references move in the middle of a chunk
+    (the rescale of the accumulated output and row sums), not just on the
+    first tile."""
+    wl = W.custom((2000, 3100), hq, 8 if hq == 64 else 2, seed=90 + n, sink_dist="uniform2")
+    gain = torch.tensor([2.0 ** min((t - 2000 if t >= 2000 else t) // 300, 5) for t in range(5100)])
+    o, lse, ref_o, ref_lse = run_decode(wl, n, key_gain=gain)
+    assert pu.max_abs(o, ref_o) <= pu.TOL["o"], pu.max_abs(o, ref_o)
+    assert pu.max_abs(lse, ref_lse) <= pu.TOL["lse"], pu.max_abs(lse, ref_lse)
 
 
 @pytest.mark.parametrize("name", sorted(W.DECODE_WORKLOADS))

@@ -125,7 +125,8 @@ def test_attention_writes_stay_inside_outputs(wl):
 
 @pytest.mark.parametrize("lens,hq,hkv,n,w,p", [((300, 1, 129, 2000), 16, 2, 1, -1, 0),
                                                ((700, 2048), 16, 2, 4, 128, 4),
-                                               ((3000,), 12, 4, 3, 10, 2000)])
+                                               ((3000,), 12, 4, 3, 10, 2000),
+                                               ((900, 129), 24, 1, 4, -1, 0)])
 def test_decode_writes_stay_inside_outputs(lens, hq, hkv, n, w, p):
     import sink_aware_masked_gb300 as sa
 
