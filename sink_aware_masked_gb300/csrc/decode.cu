@@ -282,6 +282,36 @@ __global__ void __launch_bounds__(NTHR, 3) decode_split_kernel(const __grid_cons
       if ((lane & 3) == 0) red_l[warp][rl] = l_run[mb][hr] * sc;
     }
   __syncthreads();
+  auto row_ml = [&](int r, float& M, float& l) {
+    const int wr2 = r / (MBW * 16), rl = r - wr2 * MBW * 16;
+    M = -INFINITY;
+    l = 0.f;
+#pragma unroll
+    for (int w = 0; w < WK; ++w) {
+      M = fmaxf(M, red_m[wr2 * WK + w][rl]);
+      l += red_l[wr2 * WK + w][rl];
+    }
+  };
+  if (ch.nsplit == 1) {
+    // The only chunk of this (sequence, kv head): finish the rows here,
+    // without the round trip through the workspace and the counter.
+    for (int u = tid; u < p.R * 32; u += NTHR) {
+      const int r = u >> 5, d2 = u & 31;
+      float M, l, lse;
+      row_ml(r, M, l);
+      const float fac = row_scale(p, ch, g, r, M, l, l, lse);
+      float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < WK; ++w) {
+        const float2 v = reinterpret_cast<const float2*>(acc_s + (static_cast<size_t>(w) * RP + r) * D)[d2];
+        a.x += v.x;
+        a.y += v.y;
+      }
+      store_pair(p, ch, g, r, d2, a.x * fac, a.y * fac);
+      if (d2 == 0) store_lse(p, ch, g, r, lse);
+    }
+    return;
+  }
   const size_t part = static_cast<size_t>(item_idx) * p.hkv + g;
   for (int idx = tid; idx < p.R * D; idx += NTHR) {
     float a = 0.f;
@@ -290,13 +320,8 @@ __global__ void __launch_bounds__(NTHR, 3) decode_split_kernel(const __grid_cons
     p.ws_acc[part * p.R * D + idx] = a;
   }
   for (int r = tid; r < p.R; r += NTHR) {
-    const int wr2 = r / (MBW * 16), rl = r - wr2 * MBW * 16;
-    float M = -INFINITY, l = 0.f;
-#pragma unroll
-    for (int w = 0; w < WK; ++w) {
-      M = fmaxf(M, red_m[wr2 * WK + w][rl]);
-      l += red_l[wr2 * WK + w][rl];
-    }
+    float M, l;
+    row_ml(r, M, l);
     p.ws_ml[part * p.R + r] = make_float4(M, l, l, 0.f);
   }
 

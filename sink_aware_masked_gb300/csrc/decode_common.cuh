@@ -114,6 +114,29 @@ SA_DEV bool count_partial(const DecK<CAP>& p, const Chunk& c, int g, int* is_las
   return last;
 }
 
+// The sink, applied once to a finished row r of (sequence c.b, kv head g):
+// returns the factor O is multiplied by (alpha / l_o) and sets lse from the
+// reference M (log2 units) and the fp32 sum l.
+template <int CAP>
+SA_DEV float row_scale(const DecK<CAP>& p, const Chunk& c, int g, int r, float M, float l_o, float l, float& lse) {
+  const int i = r / p.group, h = g * p.group + (r - i * p.group);
+  lse = (l > 0.f) ? (M + __log2f(l)) * kLn2 : -INFINITY;
+  const float alpha = 1.f / (1.f + ex2((__ldg(p.sink + h) - lse) * kLog2e));
+  return (l_o > 0.f) ? alpha / l_o : 0.f;
+}
+
+// Output element pair (2 d2, 2 d2 + 1) and lse of row r.
+template <int CAP>
+SA_DEV void store_pair(const DecK<CAP>& p, const Chunk& c, int g, int r, int d2, float x, float y) {
+  const int i = r / p.group, h = g * p.group + (r - i * p.group), bn = c.b * p.n + i;
+  reinterpret_cast<uint32_t*>(p.o + (static_cast<size_t>(bn) * p.hq + h) * D)[d2] = pack_bf16(x, y);
+}
+template <int CAP>
+SA_DEV void store_lse(const DecK<CAP>& p, const Chunk& c, int g, int r, float lse) {
+  const int i = r / p.group, h = g * p.group + (r - i * p.group), bn = c.b * p.n + i;
+  p.lse[static_cast<size_t>(h) * p.num_seqs * p.n + bn] = lse;
+}
+
 // Merge of the partials of (sequence c.b, kv head g) by the CTA's NT threads
 // (all of them call it).  The partials of chunk s are O at ws_acc +
 // (part0 + s Hkv) R 64 and (m, l_o, l) at ws_ml + (part0 + s Hkv) R; they
@@ -186,19 +209,14 @@ SA_DEV void merge_partials(const DecK<CAP>& p, const Chunk& c, int g, int item_i
     }
     __syncthreads();  // the next batch overwrites the staging buffers
   }
-  const int n = p.n;
 #pragma unroll
   for (int k = 0; k < UP; ++k) {
     const int u = tid + NT * k, r = u >> 5, d2 = u & 31;
     if (r >= p.R) continue;
-    const float l = lu[k], M = Mu[k];
-    const int i = r / p.group, h = g * p.group + (r - i * p.group), bn = c.b * n + i;
-    const float lse = (l > 0.f) ? (M + __log2f(l)) * kLn2 : -INFINITY;
-    const float alpha = 1.f / (1.f + ex2((__ldg(p.sink + h) - lse) * kLog2e));
-    const float fac = (lo[k] > 0.f) ? alpha / lo[k] : 0.f;
-    reinterpret_cast<uint32_t*>(p.o + (static_cast<size_t>(bn) * p.hq + h) * D)[d2] =
-        pack_bf16(acc[k].x * fac, acc[k].y * fac);
-    if (d2 == 0) p.lse[static_cast<size_t>(h) * p.num_seqs * n + bn] = lse;
+    float lse;
+    const float fac = row_scale(p, c, g, r, Mu[k], lo[k], lu[k], lse);
+    store_pair(p, c, g, r, d2, acc[k].x * fac, acc[k].y * fac);
+    if (d2 == 0) store_lse(p, c, g, r, lse);
   }
   if (tid == 0) p.counters[c.b * p.hkv + g] = 0;  // every chunk of this call has counted
 }

@@ -463,6 +463,7 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
       fence_after_sync();
     }
     const size_t part = static_cast<size_t>(item_idx) * p.hkv + g;
+    const bool single = ch.nsplit == 1;  // the only chunk: finish the rows here, no workspace round trip
     if (ok && warp < 3) {
 #pragma unroll
       for (int c = 0; c < N / 32; ++c) {
@@ -471,6 +472,7 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
         tmem_ld_wait();
         reg_fence32(o);
         if (warp < 2) {
+          if (single) continue;
           float* dst = p.ws_acc + part * p.R * D + tid;  // dimension tid of each row
 #pragma unroll
           for (int e = 0; e < 32; ++e)
@@ -503,7 +505,35 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
     ok = named_sync_and(1, NSOFT, ok);
     if (ok && tid < p.R) {
       const float l = red_s[0][tid] + red_s[1][tid] + red_s[2][tid] + red_s[3][tid];
-      p.ws_ml[part * p.R + tid] = make_float4(m_s[tid], l_s[tid], l, 0.f);
+      if (single) {
+        float lse;
+        fac_s[tid] = row_scale(p, ch, g, tid, m_s[tid], l_s[tid], l, lse);
+        store_lse(p, ch, g, tid, lse);
+      } else {
+        p.ws_ml[part * p.R + tid] = make_float4(m_s[tid], l_s[tid], l, 0.f);
+      }
+    }
+    if (single) {
+      ok = named_sync_and(1, NSOFT, ok);  // fac_s of every row
+      if (ok && warp < 2) {
+        // Thread tid holds dimension tid of every row: one bf16 per row,
+        // 64 contiguous bytes per warp and row.
+#pragma unroll
+        for (int c = 0; c < N / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lb + C::TM_O + 32 * c, o);
+          tmem_ld_wait();
+          reg_fence32(o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int r = 32 * c + e;
+            if (r >= p.R) continue;
+            const int i = r / p.group, h = g * p.group + (r - i * p.group);
+            p.o[(static_cast<size_t>(ch.b * p.n + i) * p.hq + h) * D + tid] =
+                __float2bfloat16_rn(__uint_as_float(o[e]) * fac_s[r]);
+          }
+        }
+      }
     }
     if constexpr (C::SPLIT) regs_dec<REGS_LAUNCH>();
   }
@@ -518,8 +548,9 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
     tmem_dealloc(tmem, C::TM_COLS);
   }
   if (abort_flag) return;  // written only before the barrier above: every thread reads the same value
-  // Recomputed rather than kept live through the role warps' 64 registers.
+  // Recomputed rather than kept live through the role warps' registers.
   const Chunk ch2 = chunk_of(p, blockIdx.x);
+  if (ch2.nsplit == 1) return;  // finished by the softmax warps above
   if (!count_partial(p, ch2, blockIdx.y, &is_last)) return;
   merge_partials<C::UP, NTHR>(p, ch2, blockIdx.y, blockIdx.x, smem, (NK + NV) * TILE, smem_u32(&bars.merge), ab);
 }
