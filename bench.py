@@ -100,11 +100,26 @@ def decode_visible_keys(wl, n):
     return total
 
 
+def decode_plan_tiles(wl, n):
+    """Key tiles per kv head of a decode step (the planner's count: the prefix
+    tiles below the window, then the window/causal band of the last n rows)."""
+    total = 0
+    for L in wl.seqlens:
+        q0, hi = L - n, L - 1
+        lo = 0 if wl.window < 0 else max(0, q0 - wl.window)
+        pre_end = max(0, min(min(wl.prefix, lo), hi + 1))
+        lo_t = lo // 128
+        total += min((pre_end + 127) // 128, lo_t) + (hi // 128 - lo_t + 1)
+    return total
+
+
 def decode_kernel(wl, n):
-    """(short name, kernel function) of the decode launch: the warp-MMA kernel
-    for at most 16 rows per (sequence, kv head), the tcgen05 one above."""
+    """(short name, kernel function) of the decode launch: the tcgen05 kernel
+    above 16 rows per (sequence, kv head) and for 16 or fewer from 1024 key
+    tiles per kv head, the warp-MMA kernel for the small steps."""
     rows = (wl.num_heads_q // wl.num_heads_kv) * n
-    return ("decode_split", "decode_split_kernel") if rows <= 16 else ("decode_tc", "decode_tc_kernel")
+    tc = rows > 16 or decode_plan_tiles(wl, n) >= 1024
+    return ("decode_tc", "decode_tc_kernel") if tc else ("decode_split", "decode_split_kernel")
 
 
 def decode_bytes(wl, n):

@@ -16,13 +16,15 @@
 // (sequence, kv head) with the sink applied once (decode_common.cuh).
 //
 // This file holds the plan, the launcher and the kernel for a single 16-row
-// block (R = group x n <= 16, e.g. one new row per sequence with GQA 8): the
+// block (R = group x n <= 16, e.g. one new row per sequence with GQA 8) on
+// steps too small for the tensor-core kernel of decode_tc.cu: the
 // CTA streams its tiles by TMA through a 2-stage mbarrier ring (three such
 // CTAs resident per SM) and computes a partial online softmax (running max m
 // in log2 units, row sum l, unnormalised O) with warp-level bf16 MMAs, the
 // four warps splitting the keys of each tile and merging in shared memory
-// before the partial is written.  Wider row blocks run on the tensor-core
-// kernel of decode_tc.cu.  Every mbarrier wait is bounded.
+// before the partial is written.  Wider row blocks, and 16-row blocks of
+// large steps, run on the tensor-core kernel.  Every mbarrier wait is
+// bounded.
 #include "decode_common.cuh"
 
 #include <algorithm>
@@ -35,6 +37,7 @@ using namespace tc;
 using namespace dec;
 
 constexpr int NS = 2;             // K/V stages (three CTAs per SM fit: 65 KB of shared memory each)
+constexpr long long kTcMinTiles = 1024;  // key tiles per kv head from which 16 rows go to the tensor cores
 constexpr int NTHR = 128;
 constexpr int SMEM_DYN = NS * 2 * TILE + 1024;
 
@@ -366,8 +369,13 @@ DecodePlan decode_plan(const Problem& p, int n) {
     for (int b = 0; b < p.num_seqs; ++b) items += (tiles[b] + t - 1) / t;
     return items;
   };
+  // Kernel: the tensor-core one above 16 rows, and for 16 or fewer once the
+  // step streams at least 1024 key tiles per kv head (32 x 8192 keys: 0.84
+  // of the copy bandwidth against 0.82); small steps (packed or windowed,
+  // a few hundred tiles) keep the warp-MMA kernel and its three CTAs per SM.
+  pl.tensor_core = rows > 16 || total >= kTcMinTiles;
   int tps;
-  if (rows <= 16) {
+  if (!pl.tensor_core) {
     const int factor = total >= 1024 ? 4 : 2;
     const long long want =
         std::max<long long>(1, static_cast<long long>(factor) * std::max(sms, 1) / std::max(p.hkv, 1));
@@ -418,7 +426,7 @@ cudaError_t launch_decode_cap(const Problem& pr, int n, const DecodeArgs& a, con
   const dim3 grid(k.n_items, pr.hkv);
   cudaError_t e = prof_begin(g_prof_dec, stream);
   if (e != cudaSuccess) return e;
-  if (k.R <= 16) {
+  if (!pl.tensor_core) {
     if ((e = cudaFuncSetAttribute(decode_split_kernel<1, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   SMEM_DYN)) != cudaSuccess)
       return e;

@@ -1,11 +1,13 @@
-// Decode forward on the 5th-generation tensor cores for row blocks wider than
+// Decode forward on the 5th-generation tensor cores: row blocks wider than
 // 16 (R = group x n in (16, 128]: several new rows per sequence, or large GQA
-// groups).  Same split-KV plan, partial format and merge as the warp-MMA
-// kernel (decode_common.cuh); only the per-chunk partial is computed here.
+// groups), and blocks of up to 16 rows on steps long enough to stream at
+// least 1024 key tiles per kv head.  Same split-KV plan, partial format and
+// merge as the warp-MMA kernel (decode_common.cuh); only the per-chunk
+// partial is computed here.
 //
 // Few query rows meet 128 keys per tile, so the tile is computed transposed,
-// keys on the 128 TMEM lanes and the R query rows (padded to N = 32, 64 or
-// 128 columns) along the columns:
+// keys on the 128 TMEM lanes and the R query rows (padded to N = 16, 32, 64
+// or 128 columns) along the columns:
 //   S^T = K Q^T                 M = 128 keys, N, K = 64 dims: A = the K tile
 //                               as TMA lands it (K-major), B = Q [N, 64]
 //                               (K-major, staged once per CTA)
@@ -123,15 +125,23 @@ SA_DEV void rows_seeing(int key, int L, int n, int group, const MaskParams& m, i
 }
 
 // In-place halving butterfly over the warp: x holds N values per lane; after
-// five exchange steps lane l holds in x[0 .. N/32) the maxima (SUM: sums)
-// over the 32 lanes of entries l N/32 + [0, N/32).  At each step the lanes
-// whose bit is set keep the upper half and send the lower one.
+// five exchange steps lane l holds the maxima (SUM: sums) over the 32 lanes
+// of entries l N/32 + [0, N/32) in x[0 .. N/32) when N >= 32, and of entry
+// l / 2 in x[0] when N = 16 (the last step exchanges the single value whole).
+// At each halving step the lanes whose bit is set keep the upper half and
+// send the lower one.
 template <int N, bool SUM = false>
 SA_DEV void lane_butterfly(uint32_t (&x)[N], int lane) {
 #pragma unroll
   for (int step = 0; step < 5; ++step) {
     const int half = N >> (step + 1);
     const bool up = (lane >> (4 - step)) & 1;
+    if (half == 0) {
+      const float v = __uint_as_float(x[0]);
+      const float got = __shfl_xor_sync(0xffffffffu, v, 16 >> step);
+      x[0] = __float_as_uint(SUM ? v + got : fmaxf(v, got));
+      continue;
+    }
 #pragma unroll
     for (int i = 0; i < N / 2; ++i) {
       if (i < half) {
@@ -144,10 +154,47 @@ SA_DEV void lane_butterfly(uint32_t (&x)[N], int lane) {
   }
 }
 
+// Stores the butterfly's results of one warp: dst[e] for the N entries.
+template <int N>
+SA_DEV void butterfly_store(float* dst, const uint32_t (&x)[N], int lane) {
+  if constexpr (N >= 32) {
+#pragma unroll
+    for (int i = 0; i < N / 32; ++i) dst[lane * (N / 32) + i] = __uint_as_float(x[i]);
+  } else {
+    if ((lane & 1) == 0) dst[lane >> 1] = __uint_as_float(x[0]);
+  }
+}
+
+// W (16 or 32) consecutive 32-bit TMEM columns of this thread's lane.
+template <int W>
+SA_DEV void tmem_ldw(uint32_t taddr, uint32_t* r) {
+  if constexpr (W == 32) {
+    tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(r));
+  } else {
+    static_assert(W == 16, "chunk width");
+    tmem_ld16(taddr, *reinterpret_cast<uint32_t(*)[16]>(r));
+  }
+}
+template <int W>
+SA_DEV void tmem_stw(uint32_t taddr, uint32_t* r) {
+  if constexpr (W == 32)
+    tmem_st32(taddr, *reinterpret_cast<const uint32_t(*)[32]>(r));
+  else
+    tmem_st16(taddr, *reinterpret_cast<const uint32_t(*)[16]>(r));
+}
+template <int W>
+SA_DEV void reg_fencew(uint32_t* r) {
+  if constexpr (W == 32)
+    reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(r));
+  else
+    reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(r));
+}
+
 template <int N, int CAP>
 __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __grid_constant__ DecK<CAP> p) {
   using C = Cfg<N>;
   constexpr int NK = C::NK, NV = C::NV;
+  constexpr int CW = N < 32 ? N : 32;  // TMEM columns per load or store
   extern __shared__ uint8_t smem_raw[];
   __shared__ Bars bars;
   __shared__ uint32_t tmem_base_sh;
@@ -327,7 +374,7 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
 #pragma unroll
       for (int e = 0; e < 32; ++e) z[e] = 0u;
 #pragma unroll
-      for (int c = 0; c < N / 32; ++c) tmem_st32(tmem + lb + C::TM_L + 32 * c, z);
+      for (int c = 0; c < N / 32; ++c) tmem_st32(tmem + lb + C::TM_L + 32 * c, z);  // N >= 128 here
       tmem_st_wait();
     }
     const float sl2 = p.scale_log2;
@@ -346,11 +393,10 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
       // S^T stays in TMEM until P(t) is handed over, so the slow path may read it twice.
       auto load_scores = [&]() {
 #pragma unroll
-        for (int c = 0; c < N / 32; ++c)
-          tmem_ld32(tmem + lb + C::TM_S + buf * N + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(x + 32 * c));
+        for (int c = 0; c < N / CW; ++c) tmem_ldw<CW>(tmem + lb + C::TM_S + buf * N + CW * c, x + CW * c);
         tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < N / 32; ++c) reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(x + 32 * c));
+        for (int c = 0; c < N / CW; ++c) reg_fencew<CW>(x + CW * c);
         if (partial) {
           int rlo, rhi;
           rows_seeing(k0 + tid, L, p.n, p.group, p.mask, rlo, rhi);
@@ -373,8 +419,7 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
         // Row maxima of this tile: a halving butterfly over the lanes (in
         // place), after which lane l holds rows l N/32 + [0, N/32).
         lane_butterfly<N>(x, lane);
-#pragma unroll
-        for (int i = 0; i < N / 32; ++i) red_s[warp][lane * (N / 32) + i] = __uint_as_float(x[i]);
+        butterfly_store<N>(red_s[warp], x, lane);
         named_sync(1, NSOFT);
         bool moved = false;
         if (tid < N) {
@@ -394,14 +439,14 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
         if (named_sync_or(1, NSOFT, moved) && t > 0) {
           auto rescale = [&](uint32_t col) {
 #pragma unroll
-            for (int c = 0; c < N / 32; ++c) {
-              uint32_t o[32];
-              tmem_ld32(tmem + lb + col + 32 * c, o);
+            for (int c = 0; c < N / CW; ++c) {
+              uint32_t o[CW];
+              tmem_ldw<CW>(tmem + lb + col + CW * c, o);
               tmem_ld_wait();
-              reg_fence32(o);
+              reg_fencew<CW>(o);
 #pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * fac_s[32 * c + e]);
-              tmem_st32(tmem + lb + col + 32 * c, o);
+              for (int e = 0; e < CW; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * fac_s[CW * c + e]);
+              tmem_stw<CW>(tmem + lb + col + CW * c, o);
             }
           };
           if constexpr (C::L_REGS) {
@@ -424,20 +469,20 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
       if (ok) {
         const uint32_t pb = sb + C::OFF_P + buf * C::PBUF + p_col;
 #pragma unroll
-        for (int c = 0; c < N / 32; ++c) {
-          uint32_t lt[32];
+        for (int c = 0; c < N / CW; ++c) {
+          uint32_t lt[CW];
           if constexpr (!C::L_REGS) {
-            tmem_ld32(tmem + lb + C::TM_L + 32 * c, lt);
+            tmem_ldw<CW>(tmem + lb + C::TM_L + CW * c, lt);
             tmem_ld_wait();
-            reg_fence32(lt);
+            reg_fencew<CW>(lt);
           }
 #pragma unroll
-          for (int r4 = 0; r4 < 32; r4 += 4) {
-            const float4 ng = *reinterpret_cast<const float4*>(neg_s + 32 * c + r4);
+          for (int r4 = 0; r4 < CW; r4 += 4) {
+            const float4 ng = *reinterpret_cast<const float4*>(neg_s + CW * c + r4);
             const float ngv[4] = {ng.x, ng.y, ng.z, ng.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int rr = 32 * c + r4 + e;
+              const int rr = CW * c + r4 + e;
               const float pv = ex2(fmaf(__uint_as_float(x[rr]), sl2, ngv[e]));
               if constexpr (C::L_REGS)
                 lreg[rr] += pv;
@@ -447,7 +492,7 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
                             bf16_bits(pv));
             }
           }
-          if constexpr (!C::L_REGS) tmem_st32(tmem + lb + C::TM_L + 32 * c, lt);
+          if constexpr (!C::L_REGS) tmem_stw<CW>(tmem + lb + C::TM_L + CW * c, lt);
         }
         if constexpr (!C::L_REGS) tmem_st_wait();
         fence_async_smem();
@@ -466,20 +511,20 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
     const bool single = ch.nsplit == 1;  // the only chunk: finish the rows here, no workspace round trip
     if (ok && warp < 3) {
 #pragma unroll
-      for (int c = 0; c < N / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tmem + lb + C::TM_O + 32 * c, o);
+      for (int c = 0; c < N / CW; ++c) {
+        uint32_t o[CW];
+        tmem_ldw<CW>(tmem + lb + C::TM_O + CW * c, o);
         tmem_ld_wait();
-        reg_fence32(o);
+        reg_fencew<CW>(o);
         if (warp < 2) {
           if (single) continue;
           float* dst = p.ws_acc + part * p.R * D + tid;  // dimension tid of each row
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (32 * c + e < p.R) dst[static_cast<size_t>(32 * c + e) * D] = __uint_as_float(o[e]);
+          for (int e = 0; e < CW; ++e)
+            if (CW * c + e < p.R) dst[static_cast<size_t>(CW * c + e) * D] = __uint_as_float(o[e]);
         } else if (lane == 0) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) l_s[32 * c + e] = __uint_as_float(o[e]);
+          for (int e = 0; e < CW; ++e) l_s[CW * c + e] = __uint_as_float(o[e]);
         }
       }
     }
@@ -488,18 +533,18 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
       // Row sums of the unrounded exponentials: this lane's partials, summed
       // over the warp (lane l ends with row 32 c + l), then over the warps.
 #pragma unroll
-      for (int c = 0; c < N / 32; ++c) {
-        uint32_t lt[32];
+      for (int c = 0; c < N / CW; ++c) {
+        uint32_t lt[CW];
         if constexpr (C::L_REGS) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) lt[e] = __float_as_uint(lreg[32 * c + e]);
+          for (int e = 0; e < CW; ++e) lt[e] = __float_as_uint(lreg[CW * c + e]);
         } else {
-          tmem_ld32(tmem + lb + C::TM_L + 32 * c, lt);
+          tmem_ldw<CW>(tmem + lb + C::TM_L + CW * c, lt);
           tmem_ld_wait();
-          reg_fence32(lt);
+          reg_fencew<CW>(lt);
         }
-        lane_butterfly<32, true>(lt, lane);
-        red_s[warp][32 * c + lane] = __uint_as_float(lt[0]);
+        lane_butterfly<CW, true>(lt, lane);
+        butterfly_store<CW>(red_s[warp] + CW * c, lt, lane);
       }
     }
     ok = named_sync_and(1, NSOFT, ok);
@@ -519,14 +564,14 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
         // Thread tid holds dimension tid of every row: one bf16 per row,
         // 64 contiguous bytes per warp and row.
 #pragma unroll
-        for (int c = 0; c < N / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tmem + lb + C::TM_O + 32 * c, o);
+        for (int c = 0; c < N / CW; ++c) {
+          uint32_t o[CW];
+          tmem_ldw<CW>(tmem + lb + C::TM_O + CW * c, o);
           tmem_ld_wait();
-          reg_fence32(o);
+          reg_fencew<CW>(o);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int r = 32 * c + e;
+          for (int e = 0; e < CW; ++e) {
+            const int r = CW * c + e;
             if (r >= p.R) continue;
             const int i = r / p.group, h = g * p.group + (r - i * p.group);
             p.o[(static_cast<size_t>(ch.b * p.n + i) * p.hq + h) * D + tid] =
@@ -568,6 +613,7 @@ cudaError_t launch_n(const DecK<CAP>& k, dim3 grid, cudaStream_t stream) {
 
 template <int CAP>
 cudaError_t launch_decode_tc(const DecK<CAP>& k, dim3 grid, cudaStream_t stream) {
+  if (k.R <= 16) return launch_n<16>(k, grid, stream);
   if (k.R <= 32) return launch_n<32>(k, grid, stream);
   if (k.R <= 64) return launch_n<64>(k, grid, stream);
   return launch_n<128>(k, grid, stream);

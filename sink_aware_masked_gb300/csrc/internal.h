@@ -104,6 +104,7 @@ struct DecodeArgs {
 };
 
 struct DecodePlan {
+  bool tensor_core = false;      // the tcgen05 kernel (else the warp-MMA one)
   int tiles_per_split = 0;
   std::vector<uint32_t> items;   // sequence | (chunk << 16), sequence-major
   size_t acc_bytes = 0, ml_bytes = 0, counter_bytes = 0;

@@ -89,6 +89,18 @@ def test_decode_growing_scores(n, hq):
     assert pu.max_abs(lse, ref_lse) <= pu.TOL["lse"], pu.max_abs(lse, ref_lse)
 
 
+def test_decode_growing_scores_16_rows_tensor_core():
+    """8 rows per kv head on a step long enough (1032 key tiles per kv head)
+    for the tensor-core kernel's 16-column form; the key scale grows 2x every
+    300 tokens and restarts every 1800, so references move inside chunks."""
+    wl = W.custom((70000, 62000), 16, 2, seed=85, sink_dist="uniform2")
+    starts = [0, 70000]
+    gain = torch.tensor([2.0 ** (((t - (starts[1] if t >= starts[1] else 0)) // 300) % 6) for t in range(132000)])
+    o, lse, ref_o, ref_lse = run_decode(wl, 1, key_gain=gain)
+    assert pu.max_abs(o, ref_o) <= pu.TOL["o"], pu.max_abs(o, ref_o)
+    assert pu.max_abs(lse, ref_lse) <= pu.TOL["lse"], pu.max_abs(lse, ref_lse)
+
+
 @pytest.mark.parametrize("name", sorted(W.DECODE_WORKLOADS))
 def test_decode_workloads_sampled(name):
     """Full-size decode workloads, checked on every row of every head."""
