@@ -14,8 +14,9 @@
 //   [O^T; l] = [V^T; 1] P^T     M = 128, N, K = 128 keys: A = the V tile read
 //                               MN-major (dims 0-63) stacked on a constant
 //                               block whose first row is all ones (rows
-//                               64-127), B = P [N, 128 keys] (K-major, written
-//                               by the softmax threads)
+//                               64-127), B = P stored keys x rows
+//                               (MN-major, written by the softmax threads,
+//                               eight rows per 16-byte store)
 // so TMEM lanes 0-63 accumulate O^T and lane 64 the row sums l_o of exactly
 // the bf16 weights the numerator used: the sums over the keys, which lie
 // across threads here, come out of the tensor core.  The log-sum-exp takes
@@ -67,7 +68,14 @@ struct Cfg {
   static constexpr int OFF_K = 0;                  // K stage s at s TILE
   static constexpr int OFF_V = NK * TILE;          // V stage s at OFF_V + s TILE
   static constexpr int OFF_Q = (NK + NV) * TILE;   // [N rows][64] K-major, 8-row groups of 1 KB
-  static constexpr int PBUF = 2 * N * 128;         // one P buffer: two 64-key atoms of [N rows][64 keys]
+  // P buffer, MN-major (keys along the contraction, rows contiguous): key
+  // k's row of min(N, 64) bf16 (PRB bytes) in swizzle atoms of 8 keys, N =
+  // 128 as two such 64-row columns PATOM apart.
+  static constexpr int PRB = (N >= 64 ? 64 : N) * 2;                 // 32, 64 or 128 bytes
+  static constexpr int PATOM = BN * PRB;
+  static constexpr int PSHIFT = PRB == 128 ? 0 : (PRB == 64 ? 1 : 2);  // 16-byte chunk ^= (key % 8) >> PSHIFT
+  static constexpr uint32_t PLAYOUT = PRB == 128 ? 2 : (PRB == 64 ? 4 : 6);  // 128-, 64-, 32-byte swizzle
+  static constexpr int PBUF = N * 256;             // one P buffer: 128 keys x N rows of bf16
   static constexpr int OFF_P = OFF_Q + N * 128;    // buffer b at + b PBUF
   static constexpr int OFF_ONES = OFF_P + 2 * PBUF;  // 16 key rows x 128 B, element 0 of each row = 1
   static constexpr int SMEM_DYN = OFF_ONES + 2048 + 1024;  // + alignment slack
@@ -99,13 +107,8 @@ SA_DEV void wait_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
-SA_DEV void st_shared_u16(uint32_t addr, uint16_t v) {
-  asm volatile("st.shared.u16 [%0], %1;\n" ::"r"(addr), "h"(v) : "memory");
-}
-
-SA_DEV uint16_t bf16_bits(float x) {
-  const __nv_bfloat16 h = __float2bfloat16_rn(x);
-  return *reinterpret_cast<const uint16_t*>(&h);
+SA_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 // Rows [rlo, rhi) of the block that see `key`: query position L - n + i sees
@@ -318,7 +321,7 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
       // ---------------------------------------------------------- P.V issuer
       // [O^T; l_o] += [V^T; 1] P(t)^T once P(t) is written and V(t) landed.
       const bool leader = elect_one();
-      const uint32_t id_o = idesc_bf16(128, N, true, false);
+      const uint32_t id_o = idesc_bf16(128, N, true, true);
       bool ok = true;
       for (int t = 0; ok && t < nt; ++t) {
         const int s = t % NV;
@@ -330,7 +333,7 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
         for (int kk = 0; kk < BN / 16; ++kk) {
           const uint32_t a_off = v_off + kk * 2048;  // 16 keys of 128 B rows
           const uint64_t da = sdesc_sw128(sb + a_off, C::OFF_ONES - a_off, 1024);
-          const uint64_t db = sdesc_sw128(sb + p_off + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024);
+          const uint64_t db = sdesc_swz(sb + p_off + kk * 16 * C::PRB, C::PATOM, 8 * C::PRB, C::PLAYOUT);
           if (leader) mma_ss(tmem + C::TM_O, da, db, id_o, (t > 0 || kk > 0) ? 1u : 0u);
         }
         if (leader) {
@@ -379,9 +382,9 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
     }
     const float sl2 = p.scale_log2;
     const int L = ch.sp.len;
-    // This thread's key column in a P buffer: atom tid / 64, chunk, element.
-    const uint32_t p_col = (tid >> 6) * (N * 128);
-    const int kin = tid & 63, kcl = kin >> 3, ke = kin & 7;
+    // This thread's key row in a P buffer, and its swizzle.
+    const uint32_t p_row = (tid >> 3) * (8 * C::PRB) + (tid & 7) * C::PRB;
+    const int p_swz = (tid & 7) >> C::PSHIFT;
     bool ok = true;
     for (int t = 0; t < nt; ++t) {
       const int buf = t & 1;
@@ -464,10 +467,11 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
         }
         load_scores();
       }
-      // P = 2^{x sl2 - m}, stored as bf16 into P buffer buf (K-major, keys contiguous).
+      // P = 2^{x sl2 - m}, stored as bf16 into P buffer buf: this key's row,
+      // eight rows per 16-byte chunk.
       if (t >= 2) ok = mbar_wait_warp(b_pe(buf), ((t - 2) >> 1) & 1, ab) && ok;
       if (ok) {
-        const uint32_t pb = sb + C::OFF_P + buf * C::PBUF + p_col;
+        const uint32_t pb = sb + C::OFF_P + buf * C::PBUF + p_row;
 #pragma unroll
         for (int c = 0; c < N / CW; ++c) {
           uint32_t lt[CW];
@@ -477,20 +481,22 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
             reg_fencew<CW>(lt);
           }
 #pragma unroll
-          for (int r4 = 0; r4 < CW; r4 += 4) {
-            const float4 ng = *reinterpret_cast<const float4*>(neg_s + CW * c + r4);
-            const float ngv[4] = {ng.x, ng.y, ng.z, ng.w};
+          for (int g8 = 0; g8 < CW / 8; ++g8) {
+            const int r0 = CW * c + 8 * g8;
+            const float4 n0 = *reinterpret_cast<const float4*>(neg_s + r0);
+            const float4 n1 = *reinterpret_cast<const float4*>(neg_s + r0 + 4);
+            const float ngv[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+            float pv[8];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int rr = CW * c + r4 + e;
-              const float pv = ex2(fmaf(__uint_as_float(x[rr]), sl2, ngv[e]));
+            for (int e = 0; e < 8; ++e) {
+              pv[e] = ex2(fmaf(__uint_as_float(x[r0 + e]), sl2, ngv[e]));
               if constexpr (C::L_REGS)
-                lreg[rr] += pv;
+                lreg[r0 + e] += pv[e];
               else
-                lt[r4 + e] = __float_as_uint(__uint_as_float(lt[r4 + e]) + pv);
-              st_shared_u16(pb + (rr >> 3) * 1024 + (rr & 7) * 128 + (((kcl ^ (rr & 7)) << 4) | (ke << 1)),
-                            bf16_bits(pv));
+                lt[8 * g8 + e] = __float_as_uint(__uint_as_float(lt[8 * g8 + e]) + pv[e]);
             }
+            st_shared_v4(pb + (r0 >> 6) * C::PATOM + ((((r0 & 63) >> 3) ^ p_swz) << 4), pack_bf16(pv[0], pv[1]),
+                         pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]), pack_bf16(pv[6], pv[7]));
           }
           if constexpr (!C::L_REGS) tmem_stw<CW>(tmem + lb + C::TM_L + CW * c, lt);
         }

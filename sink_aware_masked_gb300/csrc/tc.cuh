@@ -207,6 +207,20 @@ SA_DEV uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
   return d;
 }
 
+// The same with the swizzle given as the descriptor's layout type (bits
+// 61-63): 2 = 128-byte, 4 = 64-byte, 6 = 32-byte swizzle.  For an MN-major
+// operand whose swizzle atom spans fewer than 64 bf16 along M or N, the atom
+// is 8 rows along K of 64 or 32 bytes (lbo: byte offset between atoms along
+// M/N, sbo: between 8-row groups along K).
+SA_DEV uint64_t sdesc_swz(uint32_t smem_addr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
+  uint64_t d = static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  d |= static_cast<uint64_t>(layout & 7u) << 61;
+  return d;
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A
 // and B (bits 7-9 = 1, 10-12 = 1), operand majorness (bit 15 A, bit 16 B;
 // 0 = K-major, 1 = MN-major), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
