@@ -115,10 +115,10 @@ def decode_plan_tiles(wl, n):
 
 def decode_kernel(wl, n):
     """(short name, kernel function) of the decode launch: the tcgen05 kernel
-    above 16 rows per (sequence, kv head) and for 16 or fewer from 1024 key
-    tiles per kv head, the warp-MMA kernel for the small steps."""
+    above 16 rows per (sequence, kv head) and for 16 or fewer from 128 key
+    tiles per kv head, the warp-MMA kernel for the smallest steps."""
     rows = (wl.num_heads_q // wl.num_heads_kv) * n
-    tc = rows > 16 or decode_plan_tiles(wl, n) >= 1024
+    tc = rows > 16 or decode_plan_tiles(wl, n) >= 128
     return ("decode_tc", "decode_tc_kernel") if tc else ("decode_split", "decode_split_kernel")
 
 

@@ -37,7 +37,7 @@ using namespace tc;
 using namespace dec;
 
 constexpr int NS = 2;             // K/V stages (three CTAs per SM fit: 65 KB of shared memory each)
-constexpr long long kTcMinTiles = 1024;  // key tiles per kv head from which 16 rows go to the tensor cores
+constexpr long long kTcMinTiles = 128;   // key tiles per kv head from which 16 rows go to the tensor cores
 constexpr int NTHR = 128;
 constexpr int SMEM_DYN = NS * 2 * TILE + 1024;
 
@@ -369,10 +369,11 @@ DecodePlan decode_plan(const Problem& p, int n) {
     for (int b = 0; b < p.num_seqs; ++b) items += (tiles[b] + t - 1) / t;
     return items;
   };
-  // Kernel: the tensor-core one above 16 rows, and for 16 or fewer once the
-  // step streams at least 1024 key tiles per kv head (32 x 8192 keys: 0.84
-  // of the copy bandwidth against 0.82); small steps (packed or windowed,
-  // a few hundred tiles) keep the warp-MMA kernel and its three CTAs per SM.
+  // Kernel: the tensor-core one above 16 rows, and for 16 or fewer from 128
+  // key tiles per kv head.  Measured, 16 rows: 2048 tiles (32 x 8192)
+  // 6033 against 5429 GB/s, 253 tiles (the packed step) 24.3 against
+  // 25.0 us; at 96 tiles (the windowed step, three per CTA) the warp-MMA
+  // kernel with its lighter CTAs wins, 14.3 against 16.4 us.
   pl.tensor_core = rows > 16 || total >= kTcMinTiles;
   int tps;
   if (!pl.tensor_core) {

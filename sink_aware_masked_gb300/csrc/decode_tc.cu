@@ -1,7 +1,7 @@
 // Decode forward on the 5th-generation tensor cores: row blocks wider than
 // 16 (R = group x n in (16, 128]: several new rows per sequence, or large GQA
-// groups), and blocks of up to 16 rows on steps long enough to stream at
-// least 1024 key tiles per kv head.  Same split-KV plan, partial format and
+// groups), and blocks of up to 16 rows on steps that stream at least 128
+// key tiles per kv head.  Same split-KV plan, partial format and
 // merge as the warp-MMA kernel (decode_common.cuh); only the per-chunk
 // partial is computed here.
 //

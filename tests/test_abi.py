@@ -230,7 +230,7 @@ def _decode_plan_items(lens, hq, hkv, n, window=-1, prefix=0, sms=152):
     total = sum(tiles)
     rows = (hq // hkv) * n
     items_at = lambda t: sum(-(-x // t) for x in tiles)  # noqa: E731
-    if rows <= 16 and total < 1024:
+    if rows <= 16 and total < 128:
         factor = 4 if total >= 1024 else 2
         want = max(1, factor * sms // hkv)
         tps = max(2, -(-total // want))
@@ -250,7 +250,7 @@ def _decode_plan_items(lens, hq, hkv, n, window=-1, prefix=0, sms=152):
 @pytest.mark.parametrize("lens,n,window,prefix", [
     ([8192] * 32, 1, -1, 0),                                       # 32 x 8192: tensor cores, one wave
     ([32768] * 8, 4, -1, 0),                                       # 32 rows per kv head: factor 2
-    ([6111, 5036, 1589, 6459, 1056, 6459, 3018, 2085], 1, -1, 0),  # packed: < 1024 tiles per kv head
+    ([6111, 5036, 1589, 6459, 1056, 6459, 3018, 2085], 1, -1, 0),  # packed: 253 tiles per kv head, tensor cores
     ([8192] * 32, 1, 128, 4),                                      # window and prefix
     ([8192] * 32, 8, -1, 0),                                       # 64 rows: tensor-core kernel, 2 CTAs per SM
     ([5000, 300, 9000], 16, 200, 3),                               # 128 rows: one CTA per SM
