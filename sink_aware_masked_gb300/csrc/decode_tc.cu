@@ -85,6 +85,8 @@ struct Cfg {
   static constexpr uint32_t TM_S = 0, TM_O = 2 * N, TM_L = 3 * N;  // S buffer b at + b N
   static constexpr uint32_t TM_COLS = ((L_REGS ? 3 : 4) * N <= 128) ? 128 : ((L_REGS ? 3 : 4) * N <= 256 ? 256 : 512);
   static constexpr int UP = (N * 32 + NTHR - 1) / NTHR;    // merge units per thread
+  static_assert(TM_O + N <= TM_COLS && (L_REGS || TM_L + N <= TM_COLS), "TMEM columns");
+  static_assert(CTAS * TM_COLS <= 512, "TMEM of the resident CTAs");
 };
 // Register split of the 64-row kernel, resident twice per SM: launched with
 // 128 a thread (65,536 / 512), the softmax warpgroup takes 176 and the role
