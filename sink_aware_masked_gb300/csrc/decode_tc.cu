@@ -28,23 +28,25 @@
 // Softmax without a per-tile row maximum: each row keeps a reference m (log2
 // units of the scaled score) and P = 2^{x - m}.  A tile is checked against
 // m + 16; only if some score exceeds it (always on the first visible tile of
-// a row, rarely afterwards) do the four softmax warps compute that tile's row
+// a row, rarely afterwards) do the softmax warps compute that tile's row
 // maxima (a halving butterfly, N shuffles per warp), move the references and
 // rescale the accumulated O^T and l_o columns and the fp32 partial sums.  P
 // stays below 2^16, far inside the range of bf16 and of the fp32 sums; the
 // result is the same online softmax with a different (exact) reference per
 // row, recorded with the partial.
 //
-// Warp roles (8 warps): 0-3 softmax, thread t of warp w owns key 32 w + t of
-// the tile (its TMEM lane); 4 and 6 TMA producers of the K and the V tiles,
-// each through its own ring (a K stage is free once S^T of its tile is
-// computed, a V stage once its P.V is, so the next K load starts a whole
-// softmax earlier than a shared stage would allow); 5 S^T issuer and TMEM
-// owner; 7 P.V issuer.  Each issuer blocks on its own barriers, so neither
-// polls nor waits behind the other's loads; S^T runs one tile ahead (two S
-// buffers, two P buffers).  Every wait is bounded; the softmax warps decide
-// together at their named barriers, and every role drains its copies and
-// MMAs before TMEM is freed.
+// Warp roles: one softmax warpgroup per NC rows (two at 32 columns, else
+// one), thread t of warp w owning key 32 (w % 4) + t of the tile (its TMEM
+// lane) for the warpgroup's rows; then four role warps: the TMA producers of
+// the K and the V tiles (first and third), each through its own ring (a K
+// stage is free once S^T of its tile is computed, a V stage once its P.V is,
+// so the next K load starts a whole softmax earlier than a shared stage
+// would allow), the S^T issuer and TMEM owner (second) and the P.V issuer
+// (fourth).  Each issuer blocks on its own barriers, so neither polls nor
+// waits behind the other's loads; S^T runs one tile ahead (two S buffers,
+// two P buffers).  Every wait is bounded; each softmax warpgroup decides
+// together at its named barrier, and every role drains its copies and MMAs
+// before TMEM is freed.
 #include "decode_common.cuh"
 
 namespace sa {
@@ -53,8 +55,6 @@ namespace {
 
 using namespace tc;
 
-constexpr int NTHR = 256;
-constexpr int NSOFT = 128;         // softmax threads (warps 0-3)
 constexpr float kRefSlack = 16.f;  // log2 units a score may exceed its row reference by
 
 template <int N>
@@ -64,6 +64,13 @@ struct Cfg {
   static constexpr int NK = (N == 128) ? 4 : 2;
   static constexpr int NV = (N == 128) ? 4 : 2;
   static constexpr int CTAS = (N == 128) ? 1 : 2;  // resident CTAs per SM
+  // Softmax warpgroups: at 32 columns two, each owning 16 rows (the softmax
+  // threads' per-tile work sets the pace; 16 columns a thread measured 0.91
+  // of the copy bandwidth against 0.86 for 32), else one owning all N.
+  static constexpr int NWG = (N == 32) ? 2 : 1;
+  static constexpr int NC = N / NWG;               // rows (TMEM columns) per softmax thread
+  static constexpr int NSOFT = 128 * NWG;          // softmax threads; the four role warps follow
+  static constexpr int NTHR = NSOFT + 128;
   static constexpr bool SPLIT = N == 64;           // registers moved to the softmax warpgroup
   static constexpr int OFF_K = 0;                  // K stage s at s TILE
   static constexpr int OFF_V = NK * TILE;          // V stage s at OFF_V + s TILE
@@ -85,14 +92,17 @@ struct Cfg {
   static constexpr uint32_t TM_S = 0, TM_O = 2 * N, TM_L = 3 * N;  // S buffer b at + b N
   static constexpr uint32_t TM_COLS = ((L_REGS ? 3 : 4) * N <= 128) ? 128 : ((L_REGS ? 3 : 4) * N <= 256 ? 256 : 512);
   static constexpr int UP = (N * 32 + NTHR - 1) / NTHR;    // merge units per thread
+  static_assert(!SPLIT || NWG == 1, "the register split assumes one softmax warpgroup");
   static_assert(TM_O + N <= TM_COLS && (L_REGS || TM_L + N <= TM_COLS), "TMEM columns");
   static_assert(CTAS * TM_COLS <= 512, "TMEM of the resident CTAs");
 };
-// Register split of the 64-row kernel, resident twice per SM: launched with
-// 128 a thread (65,536 / 512), the softmax warpgroup takes 176 and the role
-// warps keep 80: 128 x 176 + 128 x 80 = 32,768 = 256 x 128.
+// Register split of the 64-row kernel (256 threads), resident twice per SM:
+// launched with 128 a thread (65,536 / 512), the softmax warpgroup takes 176
+// and the role warps keep 80: 128 x 176 + 128 x 80 = 32,768 = 256 x 128.
 constexpr int REGS_LAUNCH = 128, REGS_SOFT = 176, REGS_ROLE = 80;
-static_assert(NSOFT * REGS_SOFT + (NTHR - NSOFT) * REGS_ROLE == NTHR * REGS_LAUNCH, "register split");
+static_assert(Cfg<64>::NSOFT * REGS_SOFT + (Cfg<64>::NTHR - Cfg<64>::NSOFT) * REGS_ROLE ==
+                  Cfg<64>::NTHR * REGS_LAUNCH,
+              "register split");
 
 struct Bars {
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
@@ -196,10 +206,10 @@ SA_DEV void reg_fencew(uint32_t* r) {
 }
 
 template <int N, int CAP>
-__global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __grid_constant__ DecK<CAP> p) {
+__global__ void __launch_bounds__(Cfg<N>::NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __grid_constant__ DecK<CAP> p) {
   using C = Cfg<N>;
-  constexpr int NK = C::NK, NV = C::NV;
-  constexpr int CW = N < 32 ? N : 32;  // TMEM columns per load or store
+  constexpr int NK = C::NK, NV = C::NV, NC = C::NC, NSOFT = C::NSOFT;
+  constexpr int CW = NC < 32 ? NC : 32;  // TMEM columns per load or store
   extern __shared__ uint8_t smem_raw[];
   __shared__ Bars bars;
   __shared__ uint32_t tmem_base_sh;
@@ -208,10 +218,11 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
   __shared__ __align__(16) float thr_s[N];  // (m + kRefSlack) / scale_log2: the bound on the raw score
   __shared__ __align__(16) float neg_s[N];  // -m, 0 while m = -inf
   __shared__ __align__(16) float fac_s[N];  // factor of the last reference move
-  __shared__ float red_s[4][N];             // per softmax warp: tile maximum (or sum) of each row
+  __shared__ float red_s[4][N];             // per lane quarter: tile maximum (or sum) of each row
   __shared__ float l_s[N];                  // l_o (TMEM lane 64)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int role = warp - NSOFT / 32;  // 0 K producer, 1 S^T issuer, 2 V producer, 3 P.V issuer; < 0 softmax
   const int item_idx = blockIdx.x, g = blockIdx.y;
   const Chunk ch = chunk_of(p, item_idx);
   const int nt = ch.j1 - ch.j0;  // >= 1: every chunk holds at least one tile
@@ -240,7 +251,7 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
     mbar_init(b_qf, NSOFT);
     for (int b = 0; b < 2; ++b) {
       mbar_init(b_sf(b), 1);
-      mbar_init(b_pf(b), 4);
+      mbar_init(b_pf(b), NSOFT / 32);  // one arrival per softmax warp
       mbar_init(b_pe(b), 1);
     }
     mbar_init(smem_u32(&bars.drain_s), 1);
@@ -253,7 +264,7 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
     thr_s[tid] = -INFINITY;
     neg_s[tid] = 0.f;
   }
-  if (warp == 5) {
+  if (role == 1) {
     tmem_alloc(smem_u32(&tmem_base_sh), C::TM_COLS);
     tmem_relinquish();
   }
@@ -263,16 +274,16 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
   const uint32_t tmem = tmem_base_sh;
   const Abort ab{&abort_flag, p.status};
 
-  if (warp >= 4) {
+  if (role >= 0) {
     if constexpr (C::SPLIT) regs_dec<REGS_ROLE>();
-    if (warp == 4 || warp == 6) {
+    if (role == 0 || role == 2) {
       // ---------------------------------------------------------- TMA producers
-      // Warp 4 streams the K tiles, warp 6 the V tiles, each through its own
-      // ring: a K stage is free again once S^T of its tile is computed, a V
+      // One warp streams the K tiles, another the V tiles, each through its
+      // own ring: a K stage is free once S^T of its tile is computed, a V
       // stage once its P.V is, so the next K load starts a whole softmax
       // earlier than a shared K/V stage would allow.
       if (lane == 0) {
-        const bool is_k = warp == 4;
+        const bool is_k = role == 0;
         const CUtensorMap* map = is_k ? &p.tm_k : &p.tm_v;
         const uint32_t base = sb + (is_k ? C::OFF_K : C::OFF_V);
         const int NS = is_k ? NK : NV;
@@ -290,7 +301,7 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
           for (int t = max(0, issued - NS); t < issued; ++t)
             wait_drain(is_k ? b_kf(t % NS) : b_vf(t % NS), (t / NS) & 1);
       }
-    } else if (warp == 5) {
+    } else if (role == 1) {
       // ---------------------------------------------------------- S^T issuer
       // S^T(t) = K(t) Q^T into S buffer t & 1, free again once the softmax
       // warps handed over P(t - 2).
@@ -351,6 +362,11 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
   } else {
     if constexpr (C::SPLIT) regs_inc<REGS_SOFT>();
     // ------------------------------------------------------------ softmax
+    // Warpgroup wg owns rows [c0, c0 + NC): their S^T columns, references,
+    // sums, P rows and output; thread (warp % 4, lane) owns key 32 (warp % 4)
+    // + lane of each tile (its TMEM lane).  Each warpgroup decides at its own
+    // named barrier.
+    const int wg = warp >> 2, q4 = warp & 3, key = tid & 127, c0 = wg * NC, bar = 1 + wg;
     // Q rows (zero rows up to N) and the constant ones block.
     for (int idx = tid; idx < N * 8; idx += NSOFT) {
       const int r = idx >> 3, c = idx & 7;
@@ -362,7 +378,7 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
       }
       *reinterpret_cast<uint4*>(smem + C::OFF_Q + (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4)) = v;
     }
-    {
+    if (tid < 128) {
       const int r = tid >> 3, c = tid & 7;  // 16 rows x 8 chunks; logical chunk 0 sits at chunk r % 8
       *reinterpret_cast<uint4*>(smem + C::OFF_ONES + tid * 16) = make_uint4(c == (r & 7) ? 0x3F80u : 0u, 0u, 0u, 0u);
     }
@@ -370,23 +386,23 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
     mbar_arrive(b_qf);
 
     const uint32_t lb = lane_base(warp);
-    // fp32 sums of this key's unrounded P for every row (registers or TMEM).
-    float lreg[C::L_REGS ? N : 1];
+    // fp32 sums of this key's unrounded P for every owned row (registers or TMEM).
+    float lreg[C::L_REGS ? NC : 1];
 #pragma unroll
-    for (int r = 0; r < (C::L_REGS ? N : 1); ++r) lreg[r] = 0.f;
+    for (int r = 0; r < (C::L_REGS ? NC : 1); ++r) lreg[r] = 0.f;
     if constexpr (!C::L_REGS) {
       uint32_t z[32];
 #pragma unroll
       for (int e = 0; e < 32; ++e) z[e] = 0u;
 #pragma unroll
-      for (int c = 0; c < N / 32; ++c) tmem_st32(tmem + lb + C::TM_L + 32 * c, z);  // N >= 128 here
+      for (int c = 0; c < NC / 32; ++c) tmem_st32(tmem + lb + C::TM_L + c0 + 32 * c, z);  // NC >= 128 here
       tmem_st_wait();
     }
     const float sl2 = p.scale_log2;
     const int L = ch.sp.len;
     // This thread's key row in a P buffer, and its swizzle.
-    const uint32_t p_row = (tid >> 3) * (8 * C::PRB) + (tid & 7) * C::PRB;
-    const int p_swz = (tid & 7) >> C::PSHIFT;
+    const uint32_t p_row = (key >> 3) * (8 * C::PRB) + (key & 7) * C::PRB;
+    const int p_swz = (key & 7) >> C::PSHIFT;
     bool ok = true;
     for (int t = 0; t < nt; ++t) {
       const int buf = t & 1;
@@ -394,41 +410,41 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
       fence_after_sync();
       const int k0 = ch.kt.k0(ch.j0 + t);
       const bool partial = !block_full(L - p.n, p.n, k0, BN, L, p.mask);
-      uint32_t x[N];  // this key's raw scores for every row (-inf where masked); then P
+      uint32_t x[NC];  // this key's raw scores for every owned row (-inf where masked); then P
       // S^T stays in TMEM until P(t) is handed over, so the slow path may read it twice.
       auto load_scores = [&]() {
 #pragma unroll
-        for (int c = 0; c < N / CW; ++c) tmem_ldw<CW>(tmem + lb + C::TM_S + buf * N + CW * c, x + CW * c);
+        for (int c = 0; c < NC / CW; ++c) tmem_ldw<CW>(tmem + lb + C::TM_S + buf * N + c0 + CW * c, x + CW * c);
         tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < N / CW; ++c) reg_fencew<CW>(x + CW * c);
+        for (int c = 0; c < NC / CW; ++c) reg_fencew<CW>(x + CW * c);
         if (partial) {
           int rlo, rhi;
-          rows_seeing(k0 + tid, L, p.n, p.group, p.mask, rlo, rhi);
+          rows_seeing(k0 + key, L, p.n, p.group, p.mask, rlo, rhi);
 #pragma unroll
-          for (int r = 0; r < N; ++r)
-            if (r < rlo || r >= rhi) x[r] = __float_as_uint(-INFINITY);
+          for (int r = 0; r < NC; ++r)
+            if (c0 + r < rlo || c0 + r >= rhi) x[r] = __float_as_uint(-INFINITY);
         }
       };
       load_scores();
       bool over = false;
 #pragma unroll
-      for (int r = 0; r < N; r += 4) {
-        const float4 th = *reinterpret_cast<const float4*>(thr_s + r);
+      for (int r = 0; r < NC; r += 4) {
+        const float4 th = *reinterpret_cast<const float4*>(thr_s + c0 + r);
         over |= (__uint_as_float(x[r]) > th.x) | (__uint_as_float(x[r + 1]) > th.y) |
                 (__uint_as_float(x[r + 2]) > th.z) | (__uint_as_float(x[r + 3]) > th.w);
       }
-      if (named_sync_or(1, NSOFT, over || !ok)) {
+      if (named_sync_or(bar, 128, over || !ok)) {
         // A failed wait anywhere in the group: leave together.
-        if (!named_sync_and(1, NSOFT, ok)) break;
+        if (!named_sync_and(bar, 128, ok)) break;
         // Row maxima of this tile: a halving butterfly over the lanes (in
-        // place), after which lane l holds rows l N/32 + [0, N/32).
-        lane_butterfly<N>(x, lane);
-        butterfly_store<N>(red_s[warp], x, lane);
-        named_sync(1, NSOFT);
+        // place), then the four lane quarters in shared memory.
+        lane_butterfly<NC>(x, lane);
+        butterfly_store<NC>(red_s[q4] + c0, x, lane);
+        named_sync(bar, 128);
         bool moved = false;
-        if (tid < N) {
-          const int r = tid;
+        if (key < NC) {
+          const int r = c0 + key;
           const float M = fmaxf(fmaxf(red_s[0][r], red_s[1][r]), fmaxf(red_s[2][r], red_s[3][r])) * sl2;
           const float m_old = m_s[r];
           float f = 1.f;
@@ -441,27 +457,27 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
           }
           fac_s[r] = f;
         }
-        if (named_sync_or(1, NSOFT, moved) && t > 0) {
+        if (named_sync_or(bar, 128, moved) && t > 0) {
           auto rescale = [&](uint32_t col) {
 #pragma unroll
-            for (int c = 0; c < N / CW; ++c) {
+            for (int c = 0; c < NC / CW; ++c) {
               uint32_t o[CW];
-              tmem_ldw<CW>(tmem + lb + col + CW * c, o);
+              tmem_ldw<CW>(tmem + lb + col + c0 + CW * c, o);
               tmem_ld_wait();
               reg_fencew<CW>(o);
 #pragma unroll
-              for (int e = 0; e < CW; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * fac_s[CW * c + e]);
-              tmem_stw<CW>(tmem + lb + col + CW * c, o);
+              for (int e = 0; e < CW; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * fac_s[c0 + CW * c + e]);
+              tmem_stw<CW>(tmem + lb + col + c0 + CW * c, o);
             }
           };
           if constexpr (C::L_REGS) {
 #pragma unroll
-            for (int r = 0; r < N; ++r) lreg[r] *= fac_s[r];
+            for (int r = 0; r < NC; ++r) lreg[r] *= fac_s[c0 + r];
           } else {
             rescale(C::TM_L);
           }
           // O^T (lanes 0-63) and l_o (lane 64) must hold every P.V so far.
-          if (warp < 3 && (ok = mbar_wait_warp(b_pe((t - 1) & 1), ((t - 1) >> 1) & 1, ab))) {
+          if (q4 < 3 && (ok = mbar_wait_warp(b_pe((t - 1) & 1), ((t - 1) >> 1) & 1, ab))) {
             fence_after_sync();
             rescale(C::TM_O);
           }
@@ -475,32 +491,32 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
       if (ok) {
         const uint32_t pb = sb + C::OFF_P + buf * C::PBUF + p_row;
 #pragma unroll
-        for (int c = 0; c < N / CW; ++c) {
+        for (int c = 0; c < NC / CW; ++c) {
           uint32_t lt[CW];
           if constexpr (!C::L_REGS) {
-            tmem_ldw<CW>(tmem + lb + C::TM_L + CW * c, lt);
+            tmem_ldw<CW>(tmem + lb + C::TM_L + c0 + CW * c, lt);
             tmem_ld_wait();
             reg_fencew<CW>(lt);
           }
 #pragma unroll
           for (int g8 = 0; g8 < CW / 8; ++g8) {
-            const int r0 = CW * c + 8 * g8;
+            const int rl = CW * c + 8 * g8, r0 = c0 + rl;  // first of eight rows: local, global
             const float4 n0 = *reinterpret_cast<const float4*>(neg_s + r0);
             const float4 n1 = *reinterpret_cast<const float4*>(neg_s + r0 + 4);
             const float ngv[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
             float pv[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              pv[e] = ex2(fmaf(__uint_as_float(x[r0 + e]), sl2, ngv[e]));
+              pv[e] = ex2(fmaf(__uint_as_float(x[rl + e]), sl2, ngv[e]));
               if constexpr (C::L_REGS)
-                lreg[r0 + e] += pv[e];
+                lreg[rl + e] += pv[e];
               else
                 lt[8 * g8 + e] = __float_as_uint(__uint_as_float(lt[8 * g8 + e]) + pv[e]);
             }
             st_shared_v4(pb + (r0 >> 6) * C::PATOM + ((((r0 & 63) >> 3) ^ p_swz) << 4), pack_bf16(pv[0], pv[1]),
                          pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]), pack_bf16(pv[6], pv[7]));
           }
-          if constexpr (!C::L_REGS) tmem_stw<CW>(tmem + lb + C::TM_L + CW * c, lt);
+          if constexpr (!C::L_REGS) tmem_stw<CW>(tmem + lb + C::TM_L + c0 + CW * c, lt);
         }
         if constexpr (!C::L_REGS) tmem_st_wait();
         fence_async_smem();
@@ -510,79 +526,82 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
       }
     }
     // ---------------------------------------------------------- partial out
-    ok = named_sync_and(1, NSOFT, ok);
+    ok = named_sync_and(bar, 128, ok);
     if (ok) {
       ok = mbar_wait_warp(b_pe((nt - 1) & 1), ((nt - 1) >> 1) & 1, ab);
       fence_after_sync();
     }
     const size_t part = static_cast<size_t>(item_idx) * p.hkv + g;
     const bool single = ch.nsplit == 1;  // the only chunk: finish the rows here, no workspace round trip
-    if (ok && warp < 3) {
+    if (ok && q4 < 3) {
 #pragma unroll
-      for (int c = 0; c < N / CW; ++c) {
+      for (int c = 0; c < NC / CW; ++c) {
         uint32_t o[CW];
-        tmem_ldw<CW>(tmem + lb + C::TM_O + CW * c, o);
+        tmem_ldw<CW>(tmem + lb + C::TM_O + c0 + CW * c, o);
         tmem_ld_wait();
         reg_fencew<CW>(o);
-        if (warp < 2) {
+        if (q4 < 2) {
           if (single) continue;
-          float* dst = p.ws_acc + part * p.R * D + tid;  // dimension tid of each row
+          float* dst = p.ws_acc + part * p.R * D + key;  // dimension `key` (TMEM lane) of each row
 #pragma unroll
-          for (int e = 0; e < CW; ++e)
-            if (CW * c + e < p.R) dst[static_cast<size_t>(CW * c + e) * D] = __uint_as_float(o[e]);
+          for (int e = 0; e < CW; ++e) {
+            const int r = c0 + CW * c + e;
+            if (r < p.R) dst[static_cast<size_t>(r) * D] = __uint_as_float(o[e]);
+          }
         } else if (lane == 0) {
 #pragma unroll
-          for (int e = 0; e < CW; ++e) l_s[CW * c + e] = __uint_as_float(o[e]);
+          for (int e = 0; e < CW; ++e) l_s[c0 + CW * c + e] = __uint_as_float(o[e]);
         }
       }
     }
-    ok = named_sync_and(1, NSOFT, ok);  // red_s is reused below
+    ok = named_sync_and(bar, 128, ok);  // red_s is reused below
     if (ok) {
       // Row sums of the unrounded exponentials: this lane's partials, summed
-      // over the warp (lane l ends with row 32 c + l), then over the warps.
+      // over the warp, then over the four lane quarters.
 #pragma unroll
-      for (int c = 0; c < N / CW; ++c) {
+      for (int c = 0; c < NC / CW; ++c) {
         uint32_t lt[CW];
         if constexpr (C::L_REGS) {
 #pragma unroll
           for (int e = 0; e < CW; ++e) lt[e] = __float_as_uint(lreg[CW * c + e]);
         } else {
-          tmem_ldw<CW>(tmem + lb + C::TM_L + CW * c, lt);
+          tmem_ldw<CW>(tmem + lb + C::TM_L + c0 + CW * c, lt);
           tmem_ld_wait();
           reg_fencew<CW>(lt);
         }
         lane_butterfly<CW, true>(lt, lane);
-        butterfly_store<CW>(red_s[warp] + CW * c, lt, lane);
+        butterfly_store<CW>(red_s[q4] + c0 + CW * c, lt, lane);
       }
     }
-    ok = named_sync_and(1, NSOFT, ok);
-    if (ok && tid < p.R) {
-      const float l = red_s[0][tid] + red_s[1][tid] + red_s[2][tid] + red_s[3][tid];
+    ok = named_sync_and(bar, 128, ok);
+    if (ok && key < NC && c0 + key < p.R) {
+      const int r = c0 + key;
+      const float l = red_s[0][r] + red_s[1][r] + red_s[2][r] + red_s[3][r];
       if (single) {
         float lse;
-        fac_s[tid] = row_scale(p, ch, g, tid, m_s[tid], l_s[tid], l, lse);
-        store_lse(p, ch, g, tid, lse);
+        fac_s[r] = row_scale(p, ch, g, r, m_s[r], l_s[r], l, lse);
+        store_lse(p, ch, g, r, lse);
       } else {
-        p.ws_ml[part * p.R + tid] = make_float4(m_s[tid], l_s[tid], l, 0.f);
+        p.ws_ml[part * p.R + r] = make_float4(m_s[r], l_s[r], l, 0.f);
       }
     }
     if (single) {
-      ok = named_sync_and(1, NSOFT, ok);  // fac_s of every row
-      if (ok && warp < 2) {
-        // Thread tid holds dimension tid of every row: one bf16 per row,
-        // 64 contiguous bytes per warp and row.
+      ok = named_sync_and(bar, 128, ok);  // fac_s of every owned row
+      if (ok && q4 < 2) {
+        // Thread `key` holds dimension `key` of every owned row: one bf16
+        // per row, 64 contiguous bytes per warp and row.
 #pragma unroll
-        for (int c = 0; c < N / CW; ++c) {
+        for (int c = 0; c < NC / CW; ++c) {
           uint32_t o[CW];
-          tmem_ldw<CW>(tmem + lb + C::TM_O + CW * c, o);
+          tmem_ldw<CW>(tmem + lb + C::TM_O + c0 + CW * c, o);
           tmem_ld_wait();
           reg_fencew<CW>(o);
 #pragma unroll
           for (int e = 0; e < CW; ++e) {
-            const int r = CW * c + e;
+            const int r = c0 + CW * c + e;
             if (r >= p.R) continue;
             const int i = r / p.group, h = g * p.group + (r - i * p.group);
-            p.o[(static_cast<size_t>(ch.b * p.n + i) * p.hq + h) * D + tid] =
+            p.o[(static_cast<size_t>(ch.b * p.n + i) * p.hq + h) * D + key] =
                 __float2bfloat16_rn(__uint_as_float(o[e]) * fac_s[r]);
           }
         }
@@ -594,9 +613,9 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
   fence_before_sync();
   __syncthreads();
   if constexpr (C::SPLIT) {
-    if (warp >= 4) regs_inc<REGS_LAUNCH>();  // the softmax warpgroup gave its share back before the barrier
+    if (role >= 0) regs_inc<REGS_LAUNCH>();  // the softmax warpgroup gave its share back before the barrier
   }
-  if (warp == 5) {
+  if (role == 1) {
     fence_after_sync();
     tmem_dealloc(tmem, C::TM_COLS);
   }
@@ -605,7 +624,7 @@ __global__ void __launch_bounds__(NTHR, Cfg<N>::CTAS) decode_tc_kernel(const __g
   const Chunk ch2 = chunk_of(p, blockIdx.x);
   if (ch2.nsplit == 1) return;  // finished by the softmax warps above
   if (!count_partial(p, ch2, blockIdx.y, &is_last)) return;
-  merge_partials<C::UP, NTHR>(p, ch2, blockIdx.y, blockIdx.x, smem, (NK + NV) * TILE, smem_u32(&bars.merge), ab);
+  merge_partials<C::UP, C::NTHR>(p, ch2, blockIdx.y, blockIdx.x, smem, (NK + NV) * TILE, smem_u32(&bars.merge), ab);
 }
 
 template <int N, int CAP>
@@ -613,7 +632,7 @@ cudaError_t launch_n(const DecK<CAP>& k, dim3 grid, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<N, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg<N>::SMEM_DYN);
   if (e != cudaSuccess) return e;
-  decode_tc_kernel<N, CAP><<<grid, NTHR, Cfg<N>::SMEM_DYN, stream>>>(k);
+  decode_tc_kernel<N, CAP><<<grid, Cfg<N>::NTHR, Cfg<N>::SMEM_DYN, stream>>>(k);
   return cudaGetLastError();
 }
 
