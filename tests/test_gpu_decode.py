@@ -101,6 +101,34 @@ def test_decode_growing_scores_16_rows_tensor_core():
     assert pu.max_abs(lse, ref_lse) <= pu.TOL["lse"], pu.max_abs(lse, ref_lse)
 
 
+# Row counts R = group x n across every kernel width (16, 32, 64, 128
+# columns, one or two softmax warpgroups) and both routings: few key tiles
+# per kv head (warp-MMA kernel for R <= 16) and >= 128 (tensor cores), with
+# padding rows, windows, prefixes and causal bounds inside the last tile.
+SWEEP = [
+    # seqlens, hq, hkv, rows per sequence, window, prefix, seed
+    ((5000, 4000, 3000, 4500), 8, 8, 1, -1, 0, 101),       # R = 1, 129 tiles per kv head: tensor cores, 16 columns
+    ((700, 300), 8, 8, 3, 40, 2, 102),                     # R = 3, warp-MMA kernel
+    ((6000, 5000, 5500), 18, 2, 1, 300, 5, 103),           # R = 9, tensor cores (windowed, but 3 long sequences)
+    ((9000, 8000), 12, 1, 2, -1, 0, 104),                  # R = 24: 32 columns, two softmax warpgroups
+    ((2500, 129, 1000), 31, 1, 1, 64, 7, 105),             # R = 31: one padding row
+    ((3000, 2000), 33, 1, 1, -1, 0, 106),                  # R = 33: 64 columns, 31 padding
+    ((1500, 400), 8, 1, 8, 100, 0, 107),                   # R = 64, window
+    ((2200, 640), 13, 1, 5, -1, 3, 108),                   # R = 65: 128 columns, group 13
+    ((1300, 900), 127, 1, 1, -1, 0, 109),                  # R = 127
+    ((777,), 16, 2, 16, 50, 20, 110),                      # R = 128, window and prefix, one sequence
+]
+
+
+@pytest.mark.parametrize("case", SWEEP, ids=lambda c: f"R{(c[1] // c[2]) * c[3]}_L{'-'.join(map(str, c[0]))}")
+def test_decode_row_sweep(case):
+    lens, hq, hkv, n, w, p, seed = case
+    wl = W.custom(lens, hq, hkv, window=w, prefix=p, seed=seed, sink_dist="uniform2")
+    o, lse, ref_o, ref_lse = run_decode(wl, n)
+    assert pu.max_abs(o, ref_o) <= pu.TOL["o"], pu.max_abs(o, ref_o)
+    assert pu.max_abs(lse, ref_lse) <= pu.TOL["lse"], pu.max_abs(lse, ref_lse)
+
+
 @pytest.mark.parametrize("name", sorted(W.DECODE_WORKLOADS))
 def test_decode_workloads_sampled(name):
     """Full-size decode workloads, checked on every row of every head."""
