@@ -59,8 +59,9 @@ constexpr float kRefSlack = 16.f;  // log2 units a score may exceed its row refe
 
 template <int N>
 struct Cfg {
-  // Ring stages.  Two CTAs per SM up to 64 rows; a third V stage (which
-  // still fits at 32 rows) measured slower on 8 x 32768 x 4 rows.
+  // Ring stages.  Two CTAs per SM up to 64 rows; deeper rings measured
+  // slower (a third V stage at 32 columns on 8 x 32768 x 4 rows, a third K
+  // and V stage at 16 columns on 32 x 8192).
   static constexpr int NK = (N == 128) ? 4 : 2;
   static constexpr int NV = (N == 128) ? 4 : 2;
   static constexpr int CTAS = (N == 128) ? 1 : 2;  // resident CTAs per SM
