@@ -117,6 +117,7 @@ SWEEP = [
     ((2200, 640), 13, 1, 5, -1, 3, 108),                   # R = 65: 128 columns, group 13
     ((1300, 900), 127, 1, 1, -1, 0, 109),                  # R = 127
     ((777,), 16, 2, 16, 50, 20, 110),                      # R = 128, window and prefix, one sequence
+    (tuple(W.random_lengths(300, 4, 900, 111)), 16, 2, 4, -1, 0, 112),  # 300 short sequences: > 256 work items
 ]
 
 
