@@ -49,6 +49,11 @@
 // Epilogue (SinkFlex-RL summary page: auxiliary log-sum-exp and the sink
 // scaling function; section 5: zero-value sink equivalence):
 //   l = ln2 * (m + log2 sum),  alpha = sigmoid(l - sink[h]),  O = alpha * acc / sum.
+// A tile that lies wholly inside its sequence is written through a staging
+// tile per head by one TMA tensor store (row-strided stores from every
+// thread took ~2.5 K cycles per unit); the last tile of a sequence, whose
+// rows past the end belong to the next packed sequence, is stored row by
+// row.
 //
 // Key tiles outside the mask are never loaded: the prefix tiles, then the
 // causal/window band; fully visible tiles skip the per-element predicate.
@@ -80,12 +85,14 @@ constexpr int TILE = BM * D * 2;  // 16 KB: 128 rows x 128 bytes
 constexpr int OFF_Q = 0;                      // buffer b, head i: + (2 b + i) * TILE
 constexpr int OFF_K = OFF_Q + NQB * 2 * TILE;
 constexpr int OFF_V = OFF_K + NS * TILE;
-constexpr int SMEM_DYN = OFF_V + NS * TILE + 1024;  // + alignment slack
+constexpr int OFF_OST = OFF_V + NS * TILE;   // head i: + i * TILE, the finished O tile the TMA store reads
+constexpr int SMEM_DYN = OFF_OST + 2 * TILE + 1024;  // + alignment slack
+static_assert(SMEM_DYN <= 227 * 1024 - 512, "shared memory");
 
 constexpr uint32_t TM_S = 0, TM_P = 256, TM_O = 384;  // + 128 i, + 64 i, + 64 i
 
 struct FwdTcK {
-  CUtensorMap tm_q, tm_k, tm_v;
+  CUtensorMap tm_q, tm_k, tm_v, tm_o;
   const float* sink;
   __nv_bfloat16* o;
   float* lse;
@@ -136,6 +143,10 @@ SA_DEV bool get_unit(const FwdTcK& p, int r, Unit& u) {
   u.n_pre = min((kr.pre_end + BN - 1) / BN, u.lo_t);
   u.n_tiles = u.n_pre + (kr.hi / BN - u.lo_t + 1);  // >= 1: the diagonal is always visible
   return true;
+}
+
+SA_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 // Waits without the abort short-cut: used on the exit path to let copies and
@@ -316,6 +327,7 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
       for (int r = 0; ok && get_unit(p, r, u); ++r) {
         const int h = u.h0 + i;
         const int q = u.q0 + row;
+        const float sink_h = __ldg(p.sink + h);  // loaded now, used by the epilogue
         float m_ref = -INFINITY, l = 0.f;
         for (int j = 0; j < u.n_tiles; ++j, ++nt) {
           if (!(ok = wait_all(b_s(i), nt & 1))) break;
@@ -427,24 +439,46 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
         reg_fence32(o[0]);
         reg_fence32(o[1]);
         const float lse = (l > 0.f) ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
-        const float alpha = 1.f / (1.f + ex2((__ldg(p.sink + h) - lse) * kLog2e));
+        const float alpha = 1.f / (1.f + ex2((sink_h - lse) * kLog2e));
         const float fac = (l > 0.f) ? alpha / l : 0.f;
-        if (q < u.sp.len) {
+#define O_(e) __uint_as_float(o[c >> 2][(c & 3) * 8 + (e)]) * fac
+        if (u.q0 + BM <= u.sp.len) {
+          // A whole tile of the sequence: the rows go to this head's staging
+          // tile (the 128-byte-swizzled layout of the tensor map) and one
+          // thread stores it by TMA, so the warps move on to the next unit
+          // instead of waiting on 8 row-strided stores each.  The staging
+          // tile is free once the previous unit's store has read it.
+          const uint32_t ost = sb + OFF_OST + i * TILE;
+          const bool issuer = row == 0;
+          if (issuer) bulk_wait_read0();
+          named_sync(1 + i, 128);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st_shared_v4(ost + (row >> 3) * 1024 + (row & 7) * 128 + ((c ^ (row & 7)) << 4), pack_bf16(O_(0), O_(1)),
+                         pack_bf16(O_(2), O_(3)), pack_bf16(O_(4), O_(5)), pack_bf16(O_(6), O_(7)));
+          fence_async_smem();
+          named_sync(1 + i, 128);
+          if (issuer) {
+            tma_store_2d(&p.tm_o, h * D, u.sp.start + u.q0, ost);
+            bulk_commit();
+          }
+          p.lse[static_cast<size_t>(h) * p.T + u.sp.start + q] = lse;
+        } else if (q < u.sp.len) {
           uint4* dst = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(u.sp.start + q) * p.hq + h) * D);
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-#define O_(e) __uint_as_float(o[c >> 2][(c & 3) * 8 + (e)]) * fac
             uint4 v;
             v.x = pack_bf16(O_(0), O_(1));
             v.y = pack_bf16(O_(2), O_(3));
             v.z = pack_bf16(O_(4), O_(5));
             v.w = pack_bf16(O_(6), O_(7));
-#undef O_
             dst[c] = v;
           }
           p.lse[static_cast<size_t>(h) * p.T + u.sp.start + q] = lse;
         }
+#undef O_
       }
+      if (row == 0) bulk_wait0();  // this thread's tile stores have completed
     }
   }
   // ------------------------------------------------------------ common exit
@@ -469,7 +503,8 @@ cudaError_t launch_fwd_tc(const Problem& pr, const FwdArgs& a, int* status, cuda
   thread_local FwdTcK k;  // 17 KB parameter block; host-side staging, one per host thread
   if (!make_rows_map(&k.tm_q, a.q, pr.total_tokens, pr.hq, BM) ||
       !make_rows_map(&k.tm_k, a.k, pr.total_tokens, pr.hkv, BN) ||
-      !make_rows_map(&k.tm_v, a.v, pr.total_tokens, pr.hkv, BN))
+      !make_rows_map(&k.tm_v, a.v, pr.total_tokens, pr.hkv, BN) ||
+      !make_rows_map(&k.tm_o, a.o, pr.total_tokens, pr.hq, BM))
     return cudaErrorInvalidValue;
   const int sms = device_sms();
   k.sink = a.sink;

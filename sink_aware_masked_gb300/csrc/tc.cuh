@@ -148,6 +148,14 @@ SA_DEV void tma_reduce_add_2d(const CUtensorMap* map, int c0, int c1, uint32_t s
       "r"(c0), "r"(c1), "r"(src)
       : "memory");
 }
+// Tile store shared -> global through the tensor map (bulk group; both
+// coordinates non-negative, the innermost one 16-byte aligned).
+SA_DEV void tma_store_2d(const CUtensorMap* map, int c0, int c1, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];\n" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(src)
+               : "memory");
+}
 SA_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
 // Wait until the source shared memory of committed bulk groups may be reused.
 SA_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
