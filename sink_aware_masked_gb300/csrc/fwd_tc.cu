@@ -104,7 +104,7 @@ struct FwdTcK {
   MaskParams mask;
   float scale_log2;
   int n_items;
-  long long n_units;  // n_items * npairs
+  int n_units;  // n_items * npairs
   uint32_t items[4096];  // this launch's slice of the work list: b | (query tile << 16)
 };
 static_assert(sizeof(FwdTcK) < 32000, "kernel parameter block too large");
@@ -129,11 +129,12 @@ struct Unit {
 };
 
 SA_DEV bool get_unit(const FwdTcK& p, int r, Unit& u) {
-  const long long G = gridDim.x, c = blockIdx.x;
-  const long long pos = r * G + ((r & 1) ? G - 1 - c : c);
+  // 32-bit: a launch holds at most 4096 items x 128 head pairs.
+  const int G = gridDim.x, c = blockIdx.x;
+  const int pos = r * G + ((r & 1) ? G - 1 - c : c);
   if (pos >= p.n_units) return false;
   const uint32_t item = p.items[pos / p.npairs];
-  u.h0 = static_cast<int>(pos % p.npairs) * p.nh;
+  u.h0 = (pos % p.npairs) * p.nh;
   u.g = u.h0 / p.group;
   u.sp = seq_span(p.cu, p.seqlen, static_cast<int>(item & 0xFFFFu));
   u.q0 = static_cast<int>(item >> 16) * BM;
@@ -530,8 +531,8 @@ cudaError_t launch_fwd_tc(const Problem& pr, const FwdArgs& a, int* status, cuda
     const int n = static_cast<int>(std::min<size_t>(kMax, items.size() - first));
     std::copy(items.begin() + first, items.begin() + first + n, k.items);
     k.n_items = n;
-    k.n_units = static_cast<long long>(n) * k.npairs;
-    const int grid = static_cast<int>(std::min<long long>(sms, k.n_units));
+    k.n_units = n * k.npairs;
+    const int grid = std::min(sms, k.n_units);
     fwd_tc_kernel<<<grid, NTHR, SMEM_DYN, stream>>>(k);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
