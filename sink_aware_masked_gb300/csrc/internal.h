@@ -83,6 +83,9 @@ struct BwdItem {
 // Work lists (schedule.cu), longest first.
 std::vector<uint32_t> fwd_work_list(const Problem& p);  // b | (query tile << 16)
 int bwd_qchunk(const Problem& p);
+// Query tiles the key tiles of all sequences see (the backward's steps per kv
+// head and query head).
+long long bwd_query_tiles_total(const Problem& p);
 std::vector<BwdItem> bwd_work_list(const Problem& p, int qchunk);
 // Partial-sum slots the items of a list use (items with nchunks > 1).
 int bwd_split_slots(const std::vector<BwdItem>& items);

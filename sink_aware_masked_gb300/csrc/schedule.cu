@@ -89,6 +89,14 @@ std::vector<uint32_t> fwd_work_list(const Problem& p) {
   return out;
 }
 
+long long bwd_query_tiles_total(const Problem& p) {
+  const auto s = spans(p);
+  long long total = 0;
+  for (int b = 0; b < p.num_seqs; ++b)
+    for (int k0 = 0; k0 < s[b].len; k0 += TILE_ROWS) total += bwd_query_tiles(p, k0, s[b].len);
+  return total;
+}
+
 int bwd_qchunk(const Problem& p) {
   const auto s = spans(p);
   long long total = 0;
