@@ -429,9 +429,17 @@ __global__ void __launch_bounds__(NTHR, 1) fwd_tc_kernel(const __grid_constant__
           const float2 at = fadd2(a01, a23);
           l += at.x + at.y;
         }
-        if (!ok) break;
+        // The warpgroup's four warps decide together whether to go on: the
+        // tile store below meets at named barriers, and a warp whose bounded
+        // wait gave up (or saw another role give up) leaves the tile loop
+        // early, while a sibling may find its barrier complete.  Every warp
+        // of the warpgroup meets the unit's agreement barrier, failed or not.
+        if (!ok) {
+          named_sync_and(1 + i, 128, false);
+          break;
+        }
         // ------------------------------------------------------ epilogue
-        if (!(ok = wait_all(b_pv(1), (nt - 1) & 1))) break;
+        if (!(ok = named_sync_and(1 + i, 128, wait_all(b_pv(1), (nt - 1) & 1)))) break;
         fence_after_sync();
         uint32_t o[2][32];
         tmem_ld32(tO, o[0]);
