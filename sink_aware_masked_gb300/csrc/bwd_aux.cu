@@ -54,10 +54,13 @@ __device__ __forceinline__ float dot8_bf16(const uint4& a, const uint4& b) {
   return s;
 }
 
-// Block = kPreTokens tokens x all heads; thread = (head slot, 16-byte chunk
-// of a 128-byte row).  For each head slot the block walks its tokens in
-// batches of kPreBatch, issuing every load of a batch (O, dO, l) before any
-// arithmetic so that enough bytes are in flight to reach HBM bandwidth.
+// Block = kPreTokens tokens x 32 heads (a token group's heads take
+// ceil(Hq / 32) consecutive blocks, so that a few thousand tokens still give
+// the SMs an even share); thread = (head, 16-byte chunk of a 128-byte row).
+// The block walks its tokens in batches of kPreBatch, issuing every load of
+// a batch (O, dO, l) before any arithmetic so that enough bytes are in
+// flight to reach HBM bandwidth.  The dsink partial sums stay one per
+// (token group, head).
 constexpr int kPreBatch = 4;
 
 // v as hi + mid + lo, three round-to-nearest bf16 values (the remainder of
@@ -72,13 +75,15 @@ __device__ __forceinline__ void split3_bf16(float v, uint16_t (&out)[3]) {
 }
 
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreK p) {
-  const int sub = threadIdx.x & 7;   // 16-byte chunk of a 128-byte row
-  const int hs = threadIdx.x >> 3;   // 0..31
-  const long long t0 = static_cast<long long>(blockIdx.x) * kPreTokens;
+  const int sub = threadIdx.x & 7;  // 16-byte chunk of a 128-byte row
+  const int nslots = (p.hq + 31) / 32;
+  const int grp = static_cast<int>(blockIdx.x) / nslots;
+  const int h = (static_cast<int>(blockIdx.x) - grp * nslots) * 32 + (threadIdx.x >> 3);
+  const long long t0 = static_cast<long long>(grp) * kPreTokens;
   const long long t1 = min(t0 + kPreTokens, p.T);
   if (blockIdx.x == 0)
     for (int i = threadIdx.x; i < p.n_counters; i += blockDim.x) p.counters[i] = 0;
-  for (int h = hs; h < ((p.hq + 31) & ~31); h += 32) {
+  {
     const bool ok = h < p.hq;
     const float sk = ok ? __ldg(p.sink + h) : 0.f;
     float part = 0.f;
@@ -135,7 +140,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreK p) {
         }
       }
     }
-    if (ok && sub == 0) p.dsink_part[static_cast<size_t>(blockIdx.x) * p.hq + h] = part;
+    if (ok && sub == 0) p.dsink_part[static_cast<size_t>(grp) * p.hq + h] = part;
   }
 }
 
@@ -149,7 +154,7 @@ cudaError_t launch_bwd(const Problem& pr, const BwdArgs& a, int* status, cudaStr
   PreK k{static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.sink,
          static_cast<uint4*>(a.bias), a.dq_accum, a.dsink_part, a.unit_counters, a.n_unit_counters,
          T, pr.hq, pr.scale};
-  if (a.preprocess_blocks > 0) bwd_pre_kernel<<<a.preprocess_blocks, 256, 0, stream>>>(k);
+  if (a.preprocess_blocks > 0) bwd_pre_kernel<<<a.preprocess_blocks * ((pr.hq + 31) / 32), 256, 0, stream>>>(k);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_bwd_tc_main(pr, a, status, stream);
