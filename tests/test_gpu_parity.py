@@ -86,6 +86,9 @@ SMALL = [
     # an odd GQA group larger than one (the forward pairs heads only for even groups)
     W.custom((333, 70), 6, 2, window=50, prefix=7, seed=27, name="varlen_group3_w50_p7"),
     W.custom((1100,), 6, 2, window=12, prefix=140, seed=28, name="s1100_group3_w12_p140_split"),
+    # 40 query heads: the backward preprocess takes a token group's heads in
+    # blocks of 32, the second one partly idle
+    W.custom((300, 77), 40, 8, window=64, prefix=3, seed=29, name="varlen_h40_group5_w64_p3"),
 ]
 
 
