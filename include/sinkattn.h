@@ -113,7 +113,7 @@ sinkattn_status sinkattn_fwd(const sinkattn_problem* prob,
  * The workspace holds an fp32 dQ accumulator [T, Hq, 64], one 16-byte row
  * per (head, token) with the per-row terms -D and -l'/scale, where
  * l' = l + softplus(sink - l), as three bf16 summands each ([Hq, T]),
- * per-block partial sums of dsink, and, when key tiles are split over
+ * partial sums of dsink per 8-token group and head, and, when key tiles are split over
  * several work items, per-chunk dK/dV partial sums.
  * Its contents on entry do not matter (the call clears what it accumulates
  * into).  dK, dV and dsink are bitwise reproducible run to run; dQ is summed
